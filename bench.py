@@ -1,0 +1,386 @@
+"""Throughput of the top-2 sparse MoE layer (Mixtral shape) on B300.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl ours|reference]
+
+One step = one moe_layer_forward over one batch of synthetic tokens: router,
+grouping, both expert GEMMs and the combine (plus the load-balancing statistics
+for the T=16384 workload). Default workload: the decode batch (T=16, d=4096,
+ffn=14336, 8 experts, top-2, bf16), which is bound by reading the touched
+experts' weights from HBM. ``--config`` selects another of the five named
+workloads.
+
+Prints one JSON line (rank 0). For N > 1 every rank runs its own replica of
+the workload on its own GPU (the layer has no exchange step in this data-parallel
+form); value = tokens of all ranks / slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+from pathlib import Path
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+METRIC = "MoE-layer tokens/s at Mixtral shape (bf16); % of BF16 TC peak / HBM BW"
+UNIT = "tokens/s"
+DEFAULT_CONFIG = 1
+PROFILES = ROOT / "profiles"
+
+
+def _peaks() -> dict:
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        d = json.loads(p.read_text())
+        return dict(hbm_gbs=d["hbm_gbs"], bf16_tflops=d["bf16_tflops"],
+                    bf16_tflops_sustained=d.get("bf16_tflops_sustained", d["bf16_tflops"]), source="measured")
+    return dict(hbm_gbs=6400.0, bf16_tflops=1800.0, bf16_tflops_sustained=1400.0, source="fallback")
+
+
+class ClockSampler:
+    """Samples SM clock and throttle reasons with NVML while the timed region runs."""
+
+    REASONS = {
+        0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
+        0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+        0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting",
+    }
+
+    def __init__(self, index: int, period_s: float = 0.02):
+        self.index, self.period = index, period_s
+        self.samples, self.reasons = [], set()
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._thread = None
+        self.ok = False
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self.nvml = pynvml
+            self.h = self._handle(pynvml, index)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+            self.ok = True
+        except Exception as exc:  # pragma: no cover - reported in the JSON line
+            self.error = repr(exc)
+
+    @staticmethod
+    def _handle(pynvml, index):
+        """NVML handle of the CUDA device `index` (NVML counts all GPUs, CUDA only the visible ones)."""
+        try:
+            import torch
+            p = torch.cuda.get_device_properties(index)
+            bus = "%08X:%02X:%02X.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
+            return pynvml.nvmlDeviceGetHandleByPciBusId(bus.encode())
+        except Exception:
+            pass
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        ids = [v for v in vis.split(",") if v.strip().isdigit()]
+        return pynvml.nvmlDeviceGetHandleByIndex(int(ids[index]) if index < len(ids) else index)
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                self.samples.append(self.nvml.nvmlDeviceGetClockInfo(self.h, self.nvml.NVML_CLOCK_SM))
+                mask = self.nvml.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+                for bit, name in self.REASONS.items():
+                    if mask & bit:
+                        self.reasons.add(name)
+            except Exception:
+                pass
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self.ok:
+            self._thread = threading.Thread(target=self._run, daemon=True)
+            self._thread.start()
+        return self
+
+    def __exit__(self, *exc):
+        self._stop.set()
+        if self._thread is not None:
+            self._thread.join()
+
+    def summary(self) -> dict:
+        if not self.ok:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "error": getattr(self, "error", "")}
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None, "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(self.reasons - {"gpu_idle"}), "samples": len(self.samples)}
+
+
+def _source_digest() -> str:
+    h = hashlib.sha256()
+    for p in sorted((ROOT / "sparse_mixture_experts_53_b300" / "csrc").glob("*")):
+        h.update(p.read_bytes())
+    return h.hexdigest()[:16]
+
+
+def _profile_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it matches the current source."""
+    f = PROFILES / f"{kernel}__{workload}.json"
+    if not f.exists():
+        return None
+    try:
+        d = json.loads(f.read_text())
+    except Exception:
+        return None
+    if d.get("source_digest") != _source_digest():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+def _dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def _algorithmic(cfg: dict, counts) -> dict:
+    """Work of one step from the per-expert row counts (the router's decision)."""
+    T, d, F = cfg["T"], cfg["d"], cfg["ffn"]
+    touched = int(sum(1 for c in counts if c > 0))
+    flops = 2 * T * 6 * d * F + 2 * T * d * cfg["E"]
+    w_bytes = touched * 3 * d * F * 2
+    return dict(touched=touched, flops=flops, weight_bytes=w_bytes,
+                up_bytes=touched * 2 * d * F * 2, down_bytes=touched * d * F * 2,
+                up_flops=2 * T * 4 * d * F, down_flops=2 * T * 2 * d * F,
+                act_bytes=T * d * 2 * 2)
+
+
+def run_ours(args, rank, world, local) -> dict | None:
+    import torch
+
+    from moe_inputs import CONFIGS, make_config
+    from sparse_mixture_experts_53_b300 import moe
+
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    k = args.config
+    cfg = CONFIGS[k]
+    t0 = time.time()
+    L = make_config(k)
+    gen_s = time.time() - t0
+    aux = bool(cfg["aux"])
+    x = L.x.cuda()
+    wg, w1, w3, w2 = L.w_gate.cuda(), L.w1.cuda(), L.w3.cuda(), L.w2.cuda()
+    shape = moe.shape_of(x, w1)
+    ws = moe.workspace(shape)
+    y = torch.empty_like(x)
+    stats = (torch.empty(8, device="cuda"), torch.empty(8, device="cuda"), torch.empty(1, device="cuda")) if aux \
+        else None
+    stream = torch.cuda.current_stream()
+
+    def step():
+        moe.moe_layer_forward(shape, x, wg, w1, w3, w2, y, ws, stats, stream)
+
+    for _ in range(args.warmup):
+        step()
+    code, detail = moe.moe_get_device_status()
+    if code != moe.MOE_OK:
+        raise RuntimeError(f"device status after warm-up: {moe.status_string(code)} ({detail})")
+
+    # ---- timed region: device-resident inputs
+    sampler = ClockSampler(torch.cuda.current_device())
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    with sampler:
+        start.record(stream)
+        for _ in range(args.steps):
+            step()
+        stop.record(stream)
+        barrier()
+    ms = start.elapsed_time(stop) / args.steps
+    code, detail = moe.moe_get_device_status()
+    if code != moe.MOE_OK:
+        raise RuntimeError(f"device status after timing: {moe.status_string(code)} ({detail})")
+
+    # ---- per-kernel times (CUDA events on the launching stream), same steps
+    moe.moe_timing_enable(True)
+    for _ in range(args.steps):
+        step()
+    torch.cuda.synchronize()
+    kern = moe.moe_timing_read()
+    moe.moe_timing_enable(False)
+
+    # ---- end to end through the public call, host buffers: copy x in, y out
+    x_host = L.x.pin_memory()
+    y_host = torch.empty_like(L.x).pin_memory()
+    for _ in range(2):
+        x.copy_(x_host, non_blocking=True)
+        step()
+        y_host.copy_(y, non_blocking=True)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        x.copy_(x_host, non_blocking=True)
+        step()
+        y_host.copy_(y, non_blocking=True)
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+
+    # per-expert counts of this batch (read once, outside every timed region)
+    idx = torch.empty((L.T, 2), dtype=torch.int32, device="cuda")
+    gw = torch.empty((L.T, 2), dtype=torch.float32, device="cuda")
+    moe.moe_route_top2(shape, x, wg, idx, gw)
+    counts = torch.bincount(idx.flatten().long(), minlength=8).cpu().tolist()
+
+    if dist is not None:
+        t = torch.tensor([ms, e2e_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, e2e_ms = float(t[0]), float(t[1])
+
+    work = _algorithmic(cfg, counts)
+    peaks = _peaks()
+    tokens = cfg["T"] * world
+    launches_per_step = sum(v[0] for v in kern.values()) / max(1, args.steps)
+    streaming = cfg["T"] <= 64
+    if streaming:
+        dom = "stream_up"
+        per = kern.get(dom, [1, float("nan")])
+        dom_ms = per[1] / max(1, per[0])
+        achieved = work["up_bytes"] / (dom_ms * 1e-3) / 1e9
+        peak = peaks["hbm_gbs"]
+        roof = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "peak_source": peaks["source"],
+                "algorithmic_bytes_per_launch": work["up_bytes"], "launch_ms": round(dom_ms, 5),
+                "traffic": _profile_traffic(dom, cfg["name"])}
+    else:
+        dom = "tile_up_swiglu"
+        per = kern.get(dom, [1, float("nan")])
+        dom_ms = per[1] / max(1, per[0])
+        achieved = work["up_flops"] / (dom_ms * 1e-3) / 1e12
+        peak = peaks["bf16_tflops_sustained"]
+        roof = {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4), "peak_source": peaks["source"] + " (sustained)",
+                "algorithmic_flops_per_launch": work["up_flops"], "launch_ms": round(dom_ms, 5),
+                "traffic": _profile_traffic(dom, cfg["name"])}
+    step_s = ms * 1e-3
+    line = {
+        "metric": METRIC, "value": round(tokens / step_s, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded Mixtral-shape tensors, random init)",
+        "config": {"workload": cfg["name"], "T": cfg["T"], "d": cfg["d"], "ffn": cfg["ffn"], "E": cfg["E"], "k": 2,
+                   "aux_stats": aux, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "ffn_path": "weight-streaming (swap-AB)" if streaming else "token tiles 128x256",
+                   "l2": "inputs larger than L2: each step reads %.2f GB of expert weights" % (work["weight_bytes"] / 1e9),
+                   "experts_touched": work["touched"], "input_gen_s": round(gen_s, 1)},
+        "step": {"tflops": round(work["flops"] / step_s / 1e12, 2),
+                 "weight_gbs": round(work["weight_bytes"] / step_s / 1e9, 1),
+                 "frac_hbm": round(work["weight_bytes"] / step_s / 1e9 / peaks["hbm_gbs"], 4),
+                 "frac_bf16_sustained": round(work["flops"] / step_s / 1e12 / peaks["bf16_tflops_sustained"], 4)},
+        "roofline": roof,
+        "kernels_ms_per_step": {n: round(v[1] / max(1, args.steps), 5) for n, v in kern.items()},
+        "gpu_launches": int(round(launches_per_step * args.steps)),
+        "e2e": {"value": round(tokens / (e2e_ms * 1e-3), 1), "unit": UNIT,
+                "h2d_bytes_per_step": int(L.x.numel() * L.x.element_size()),
+                "d2h_bytes_per_step": int(L.x.numel() * L.x.element_size()), "ms_per_step": round(e2e_ms, 5)},
+        "clocks": sampler.summary(),
+    }
+    if dist is not None:
+        dist.destroy_process_group()
+    return line if rank == 0 else None
+
+
+def cpu_baseline(k: int, max_tokens: int | None = None, budget_s: float = 20.0) -> dict:
+    """The fp64 oracle, as it stands, on a bounded sample of the workload's tokens."""
+    import oracle
+    from moe_inputs import CONFIGS, make_config, to_f64
+
+    try:
+        from threadpoolctl import threadpool_info
+        cores = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
+    except Exception:
+        cores = os.cpu_count() or 1
+    cfg = CONFIGS[k]
+    L = make_config(k)
+    w = tuple(t.float().numpy() for t in (L.w1, L.w3, L.w2))
+    x64, wg64 = to_f64(L.x), to_f64(L.w_gate)
+    n = cfg["T"] if max_tokens is None else min(cfg["T"], max_tokens)
+    done, t0 = 0, time.time()
+    while done < n and (time.time() - t0) < budget_s:
+        oracle.layer_forward_tokens(x64, wg64, *w, [done])
+        done += 1
+    dt = time.time() - t0
+    return {"value": round(done / dt, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{done} of the workload's {cfg['T']} tokens, one oracle call per token "
+                      f"(fp64 router, both experts incl. weight widening), {dt:.1f} s"}
+
+
+def run_reference(args, rank, world) -> dict | None:
+    """The fp64 CPU oracle as the reference arm: each step is one token of the workload."""
+    if rank != 0:
+        return None
+    import oracle
+    from moe_inputs import CONFIGS, make_config, to_f64
+
+    try:
+        from threadpoolctl import threadpool_info
+        cores = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
+    except Exception:
+        cores = os.cpu_count() or 1
+    k = args.config
+    cfg = CONFIGS[k]
+    L = make_config(k)
+    w = tuple(t.float().numpy() for t in (L.w1, L.w3, L.w2))
+    x64, wg64 = to_f64(L.x), to_f64(L.w_gate)
+    for i in range(args.warmup):
+        oracle.layer_forward_tokens(x64, wg64, *w, [i % cfg["T"]])
+    t0 = time.time()
+    for i in range(args.steps):
+        oracle.layer_forward_tokens(x64, wg64, *w, [(args.warmup + i) % cfg["T"]])
+    dt = (time.time() - t0) / args.steps
+    v = round(1.0 / dt, 4)
+    sample = f"one token of the {cfg['T']}-token batch per step (fp64 oracle: router + both experts)"
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded Mixtral-shape tensors, random init)",
+            "config": {"workload": cfg["name"], "T": cfg["T"], "d": cfg["d"], "ffn": cfg["ffn"], "E": cfg["E"],
+                       "k": 2},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", type=int, default=DEFAULT_CONFIG, choices=[1, 2, 3, 4])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank, world, local = _dist_env()
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    line = run_ours(args, rank, world, local)
+    if line is None:
+        return
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.config)
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,193 @@
+/*
+ * moe.h — C ABI of the top-2 sparse mixture-of-experts feed-forward layer
+ * (Mixtral shape: d = 4096, ffn = 14336, E = 8 experts, k = 2), for NVIDIA
+ * B300 (sm_103a).
+ *
+ * The operation, as stated on the web pages about "Mixtral of Experts"
+ * (arXiv 2401.04088):
+ *   - router: one linear layer gives E scores l = x . W_g; a top-2 mask keeps
+ *     the two largest and a softmax over them gives two weights that sum to 1
+ *     ("Mixtral of Experts" lecture, router walkthrough; flashpapers.ai
+ *     summary, "How It Works"; tokentrails.org "Mixtral", step "The router");
+ *   - experts: E_i(x) = W2_i (SiLU(W1_i x) * W3_i x), a SwiGLU block
+ *     (tokentrails.org "Mixtral", Code; fdeinterviews.com breakdown, "The paper
+ *     in one minute");
+ *   - output: y = g_a E_a(x) + g_b E_b(x); the other experts are not run and
+ *     their weights are not read (tokentrails.org step "Two experts per token";
+ *     lecture, router walkthrough);
+ *   - training statistic: L_aux = E * sum_i f_i P_i (tokentrails.org step
+ *     "Load balancing").
+ *
+ * Conventions shared by every call:
+ *   - Layouts are row-major and contiguous. Weights use the [out][in] layout of
+ *     a linear layer: w_gate [E][d] (row e is the page's column e of W_g),
+ *     w1 and w3 [E][ffn][d], w2 [E][d][ffn]. Activations: x [T][d], y [T][d].
+ *   - Element type of x, weights, x_perm and y is shape->dtype (MOE_F32 or
+ *     MOE_BF16). Router scores, gate weights, y_slot and statistics are float;
+ *     indices are int32.
+ *   - Every data pointer is DEVICE memory owned by the caller, 16-byte aligned
+ *     (the bf16 path reads x_perm, the hidden activations and the weights with
+ *     TMA). The library allocates no device memory in any call; intermediates
+ *     live in a caller-provided workspace sized by the *_workspace_bytes calls.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream). Calls only
+ *     enqueue work: they do not synchronise the host and copy nothing back.
+ *   - Errors: argument checks happen on the host before anything is enqueued
+ *     and return MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED / MOE_ERR_WORKSPACE
+ *     synchronously. A failed launch returns MOE_ERR_CUDA. Faults found on the
+ *     device (a bounded wait that ran out, an index out of range) are latched
+ *     in a per-device status word and read with moe_get_device_status().
+ *   - Results are deterministic: no floating-point atomics; every reduction
+ *     has a fixed order for a given shape.
+ *   - Slot order ("expert-contiguous order"): one slot is a (token t, choice j)
+ *     pair, j = 0 for the higher score. Rows of x_perm / y_slot list the 2T
+ *     slots by expert ascending, then token ascending. offsets[e] is the first
+ *     row of expert e; offsets[E] = 2T.
+ */
+#ifndef MOE_B300_H
+#define MOE_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,  /* null pointer, negative size, misaligned pointer */
+    MOE_ERR_UNSUPPORTED = 2,  /* shape the kernels do not cover (E != 8, k != 2, d or ffn not a tile multiple) */
+    MOE_ERR_WORKSPACE = 3,    /* workspace smaller than the *_workspace_bytes figure */
+    MOE_ERR_CUDA = 4,         /* a CUDA runtime call or kernel launch failed */
+    MOE_ERR_TIMEOUT = 5,      /* device: a bounded wait ran out (kernel returned early) */
+    MOE_ERR_DEVICE_CHECK = 6  /* device: an index or count was out of range */
+} moe_status;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+
+typedef struct {
+    int64_t T;     /* tokens, >= 0 */
+    int32_t d;     /* model dimension */
+    int32_t ffn;   /* expert hidden dimension */
+    int32_t E;     /* experts; must be 8 */
+    int32_t k;     /* experts per token; must be 2 */
+    int32_t dtype; /* moe_dtype */
+} moe_shape;
+
+/* Supported shapes:
+ *   MOE_F32 : any d, ffn >= 1 (CUDA-core FFMA path, no TF32).
+ *   MOE_BF16: d % 256 == 0 and ffn % 128 == 0 (tcgen05 tensor-core path). */
+
+/* Library version string (static storage). */
+const char* moe_version(void);
+
+/* Human-readable name of a status code (static storage). */
+const char* moe_status_string(moe_status s);
+
+/* Workspace bytes needed by moe_layer_forward for this shape (0 on a bad
+ * shape). Covers routing arrays, x_perm, the hidden activations and y_slot. */
+size_t moe_workspace_bytes(const moe_shape* s);
+
+/* Workspace bytes needed by moe_expert_ffn for this shape (0 on a bad shape). */
+size_t moe_ffn_workspace_bytes(const moe_shape* s);
+
+/* Router (lecture router walkthrough; flashpapers "How It Works";
+ * tokentrails step "The router").
+ *   x        [T][d]   dtype      token rows
+ *   w_gate   [E][d]   dtype      router weights
+ *   topk_idx [T][2]   int32 out  selected experts, higher score first; equal
+ *                                scores go to the lower expert index
+ *   topk_w   [T][2]   float out  softmax of the two selected scores
+ *   logits   [T][E]   float out  router scores, or NULL to skip writing them
+ * Scores are accumulated in fp32 from the stored values. */
+moe_status moe_route_top2(const moe_shape* s, const void* x, const void* w_gate,
+                          int32_t* topk_idx, float* topk_w, float* logits, void* stream);
+
+/* Grouping of slots by expert (this library's structure; the pages say only
+ * that different tokens pick different experts and some experts get none).
+ *   topk_idx, topk_w  [T][2]       from moe_route_top2
+ *   x                 [T][d]       dtype
+ *   counts            [E]   out    slots per expert
+ *   offsets           [E+1] out    exclusive prefix sum of counts
+ *   perm_token        [2T]  out    token of each row (expert-contiguous order)
+ *   slot_row          [T][2] out   row of slot (t, j)
+ *   perm_w            [2T]  out    gate weight of each row
+ *   x_perm            [2T][d] out  x_perm[r] = x[perm_token[r]]
+ * An index outside [0, E) latches MOE_ERR_DEVICE_CHECK; that slot gets row -1. */
+moe_status moe_permute(const moe_shape* s, const int32_t* topk_idx, const float* topk_w,
+                       const void* x, int32_t* counts, int32_t* offsets, int32_t* perm_token,
+                       int32_t* slot_row, float* perm_w, void* x_perm, void* stream);
+
+/* Expert FFNs on the grouped rows, scaled by the gate weight (tokentrails
+ * Code: expert = w2(silu(w1 x) * w3 x)):
+ *   y_slot[r] = perm_w[r] * W2_e (SiLU(W1_e x_perm[r]) * (W3_e x_perm[r])),
+ *   for offsets[e] <= r < offsets[e+1].
+ *   x_perm [2T][d] dtype, offsets [E+1] int32 (device), perm_w [2T] float,
+ *   w1, w3 [E][ffn][d] dtype, w2 [E][d][ffn] dtype, y_slot [2T][d] float out.
+ *   ws / ws_bytes: workspace of at least moe_ffn_workspace_bytes(s) bytes.
+ * The bf16 path accumulates in fp32 and rounds SiLU(u)*v to bf16 before the
+ * W2 product. Experts with no rows read none of their weights. The row counts
+ * stay on the device: the host never waits for them. */
+moe_status moe_expert_ffn(const moe_shape* s, const void* x_perm, const int32_t* offsets,
+                          const float* perm_w, const void* w1, const void* w3, const void* w2,
+                          float* y_slot, void* ws, size_t ws_bytes, void* stream);
+
+/* Weighted sum back in token order (tokentrails step "Two experts per token"):
+ *   y[t] = y_slot[slot_row[t][0]] + y_slot[slot_row[t][1]]  (in that order,
+ *   fp32, rounded once to dtype). */
+moe_status moe_combine(const moe_shape* s, const float* y_slot, const int32_t* slot_row,
+                       void* y, void* stream);
+
+/* Load-balancing statistics (tokentrails step "Load balancing"):
+ *   f[i] = counts[i] / (2T), P[i] = mean over tokens of softmax(logits[t])[i]
+ *   (all E scores), l_aux[0] = E * sum_i f[i] P[i].
+ *   logits [T][E] float, counts [E] int32, f [E], P [E], l_aux [1] float out. */
+moe_status moe_aux_stats(const moe_shape* s, const float* logits, const int32_t* counts,
+                         float* f, float* P, float* l_aux, void* stream);
+
+/* The whole layer: route, group, expert FFNs, combine (and, when aux_f,
+ * aux_P and aux_l_aux are all non-NULL, the load-balancing statistics).
+ *   x [T][d], w_gate [E][d], w1, w3 [E][ffn][d], w2 [E][d][ffn], y [T][d] out.
+ *   ws / ws_bytes: at least moe_workspace_bytes(s) bytes of device memory.
+ * Nothing is copied to the host and the host never waits. */
+moe_status moe_layer_forward(const moe_shape* s, const void* x, const void* w_gate,
+                             const void* w1, const void* w3, const void* w2, void* y,
+                             float* aux_f, float* aux_P, float* aux_l_aux,
+                             void* ws, size_t ws_bytes, void* stream);
+
+/* Synchronises the current device, then reports and clears its status word.
+ * *code receives MOE_OK or the first device-side error since the last read;
+ * *detail (nullable) receives a kernel/where code for diagnostics. Returns
+ * MOE_ERR_CUDA if the device itself reports an error. */
+moe_status moe_get_device_status(int32_t* code, int32_t* detail);
+
+/* Upper bound, in nanoseconds, on every device-side wait of the tensor-core
+ * kernels (default 2e9). A wait that runs out latches MOE_ERR_TIMEOUT and the
+ * kernel returns early after its in-flight copies and MMAs have landed. */
+moe_status moe_set_wait_timeout_ns(uint64_t ns);
+
+/* Tuning / test knobs (host-side, process-wide):
+ *   MOE_KNOB_FFN_PATH   0 = automatic, 1 = token-tile path (128 tokens x 256
+ *                       columns per tile), 2 = weight-streaming path (128
+ *                       weight rows x up to 64 tokens per tile; needs T <= 64)
+ *   MOE_KNOB_KSLICE     K-slice of the weight-streaming path (multiple of 64;
+ *                       0 = automatic)
+ *   MOE_KNOB_GRID       CTAs of the persistent tensor-core kernels (0 = one
+ *                       per SM)
+ * Returns MOE_ERR_INVALID_ARG for an unknown knob or value. */
+enum { MOE_KNOB_FFN_PATH = 1, MOE_KNOB_KSLICE = 2, MOE_KNOB_GRID = 3 };
+moe_status moe_set_knob(int32_t knob, int64_t value);
+
+/* Per-kernel timing with CUDA events recorded on the launching stream.
+ * moe_timing_enable(1) starts recording every kernel this library launches;
+ * moe_timing_read() synchronises on the recorded events, writes a JSON object
+ * {"kernel": [launches, total_ms], ...} into buf (NUL-terminated, truncated to
+ * n bytes) and clears the record. Returns MOE_ERR_CUDA on an event error. */
+moe_status moe_timing_enable(int32_t enable);
+moe_status moe_timing_read(char* buf, size_t n);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_B300_H */

@@ -1,0 +1,563 @@
+// Expert FFNs on the 5th-generation tensor cores (tcgen05.mma kind::f16,
+// bf16 operands, fp32 accumulators in tensor memory), operands staged by TMA
+// into 128-byte-swizzled shared memory.
+//
+// Each expert is a SwiGLU block, E(x) = W2 (SiLU(W1 x) * W3 x)
+// (tokentrails.org "Mixtral", Code; fdeinterviews.com breakdown "The paper in
+// one minute"). Rows are in expert-contiguous order, so expert e owns rows
+// [offsets[e], offsets[e+1]); experts with no rows produce no work and none of
+// their weights are read (lecture, router walkthrough: unused experts are not
+// touched).
+//
+// Two kernel families, both persistent (one CTA per SM) and warp-specialised:
+// warp 0 issues TMA loads, warp 1 issues MMAs, warps 2-5 run the epilogue
+// (warp w reads tensor-memory lanes 32*(w%4) .. 32*(w%4)+31).
+//
+//  * token-tile kernels (many tokens per expert): a tile is 128 rows of one
+//    expert x 256 output columns, K stepped by 64.
+//      up:   columns are 128 rows of W1 followed by the same 128 rows of W3, so
+//            one N=256 MMA yields u and v side by side and the epilogue writes
+//            h = SiLU(u) * v in bf16;
+//      down: columns are 256 rows of W2; the epilogue writes perm_w[r] * acc.
+//    Tiles run expert-major, then column tile, then row tile, so the CTAs
+//    running at one time share weight tiles and activations through L2.
+//
+//  * weight-streaming kernels (few tokens per expert): the MMA's M side is 128
+//    weight rows and its N side is the expert's tokens (<= 64), so all SMs
+//    stream weights at full width. The reduction dimension is split into
+//    slices so that the units of work outnumber the SMs; each unit writes an
+//    fp32 partial, and a separate pass sums the partials in a fixed order.
+#pragma once
+
+#include "common.cuh"
+
+namespace moe {
+
+constexpr int kTcThreads = 192;
+constexpr int kBK = 64;          // K elements per stage (128 bytes of bf16)
+constexpr int kTileM = 128;
+constexpr int kTileN = 256;
+constexpr int kTileStages = 4;
+constexpr uint32_t kTileABytes = kTileM * kBK * 2;   // 16 KB
+constexpr uint32_t kTileBBytes = kTileN * kBK * 2;   // 32 KB
+constexpr uint32_t kTileStageBytes = kTileABytes + kTileBBytes;
+constexpr int kTileAccCols = 256;
+constexpr int kMaxStreamStages = 12;
+constexpr int kStreamAcc = 4;
+constexpr int kStreamMaxNB = 64;
+constexpr uint32_t kStreamABytes = 128 * kBK * 2;     // 16 KB of weights per stage
+
+struct TcControl {
+    uint64_t full[kMaxStreamStages];
+    uint64_t empty[kMaxStreamStages];
+    uint64_t tfull[kStreamAcc];
+    uint64_t tempty[kStreamAcc];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort_flag;
+    int n_work;
+    int n_act;
+    int off[kMaxExperts + 1];
+    int cnt[kMaxExperts];
+    int mt[kMaxExperts];
+    int base[kMaxExperts + 1];
+    int act[kMaxExperts];
+};
+
+constexpr size_t kTileSmemBytes = 1024 + (size_t)kTileStages * kTileStageBytes + sizeof(TcControl);
+
+__device__ __forceinline__ unsigned char* align1024(unsigned char* p) {
+    return reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+// Waits for the last issued phase of a barrier without looking at the abort
+// flag: used on the way out to let in-flight copies and MMAs land.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
+                                           int kernel) {
+    const uint64_t t0 = global_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_ns() - t0 > timeout_ns) {
+            report_error(MOE_ERR_TIMEOUT, kernel, W_DRAIN);
+            return;
+        }
+    }
+}
+
+__device__ __forceinline__ void raise_abort(TcControl* c, int kernel, int where) {
+    report_error(MOE_ERR_TIMEOUT, kernel, where);
+    *reinterpret_cast<volatile int*>(&c->abort_flag) = 1;
+}
+
+struct TileArgs {
+    const int32_t* offsets;  // [E+1]
+    const float* perm_w;     // [R] (down only)
+    void* out;               // up: H bf16 [R][ldo]; down: y_slot fp32 [R][ldo]
+    int E;
+    int K;          // reduction length (d for up, ffn for down)
+    int n_tiles_n;  // column tiles per expert
+    int w_rows;     // rows of one expert in the weight maps (ffn for up, d for down)
+    int ldo;        // output row stride in elements
+    uint64_t timeout_ns;
+};
+
+// UP = true: SwiGLU up-projection; UP = false: W2 down-projection + gate scale.
+template <bool UP>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    tile_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b0,
+                     const __grid_constant__ CUtensorMap map_b1, const TileArgs args) {
+    extern __shared__ unsigned char tc_smem_raw[];
+    unsigned char* smem = align1024(tc_smem_raw);
+    TcControl* ctl = reinterpret_cast<TcControl*>(smem + (size_t)kTileStages * kTileStageBytes);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int kid = UP ? K_TILE_UP : K_TILE_DOWN;
+    const uint64_t tmo = args.timeout_ns;
+    volatile int* abort_flag = &ctl->abort_flag;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kTileStages; ++s) {
+            mbar_init(smem_u32(&ctl->full[s]), 1);
+            mbar_init(smem_u32(&ctl->empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&ctl->tfull[b]), 1);
+            mbar_init(smem_u32(&ctl->tempty[b]), 4);
+        }
+        mbar_init(smem_u32(&ctl->drain), 1);
+        ctl->abort_flag = 0;
+        int tiles = 0;
+        for (int e = 0; e <= args.E; ++e) ctl->off[e] = args.offsets[e];
+        for (int e = 0; e < args.E; ++e) {
+            const int c = ctl->off[e + 1] - ctl->off[e];
+            ctl->cnt[e] = c;
+            ctl->mt[e] = (c + kTileM - 1) / kTileM;
+            ctl->base[e] = tiles;
+            tiles += ctl->mt[e] * args.n_tiles_n;
+        }
+        ctl->base[args.E] = tiles;
+        ctl->n_work = tiles;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&map_a);
+        tma_prefetch_desc(&map_b0);
+        if (UP) tma_prefetch_desc(&map_b1);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&ctl->tmem_base), 2 * kTileAccCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = ctl->tmem_base;
+    const int n_work = ctl->n_work;
+    const int E = args.E;
+    const int ntn = args.n_tiles_n;
+    const int KB = args.K / kBK;
+
+    auto decode = [&](int tile, int& e, int& nt, int& mt) {
+        e = 0;
+        while (e < E - 1 && tile >= ctl->base[e + 1]) ++e;
+        const int rem = tile - ctl->base[e];
+        nt = rem / ctl->mt[e];
+        mt = rem - nt * ctl->mt[e];
+    };
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            const uint64_t pol_act = policy_evict_last();
+            const uint64_t pol_w = policy_evict_first();
+            uint32_t s = 0, ph = 0;
+            uint32_t issued_mask = 0, issued_ph = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < n_work; tile += gridDim.x) {
+                int e, nt, mt;
+                decode(tile, e, nt, mt);
+                const int arow = ctl->off[e] + mt * kTileM;
+                const int brow = e * args.w_rows + nt * (UP ? kTileM : kTileN);
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!mbar_wait(smem_u32(&ctl->empty[s]), ph ^ 1, tmo, abort_flag)) {
+                        raise_abort(ctl, kid, W_PRODUCER);
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = smem_u32(&ctl->full[s]);
+                    const uint32_t sa = smem_u32(smem + (size_t)s * kTileStageBytes);
+                    const uint32_t sb = sa + kTileABytes;
+                    mbar_arrive_expect_tx(fb, kTileStageBytes);
+                    tma_load_2d(sa, &map_a, fb, kb * kBK, arow, pol_act);
+                    if (UP) {
+                        tma_load_2d(sb, &map_b0, fb, kb * kBK, brow, pol_w);
+                        tma_load_2d(sb + kTileBBytes / 2, &map_b1, fb, kb * kBK, brow, pol_w);
+                    } else {
+                        tma_load_2d(sb, &map_b0, fb, kb * kBK, brow, pol_w);
+                    }
+                    issued_mask |= 1u << s;
+                    issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
+                    if (++s == kTileStages) { s = 0; ph ^= 1; }
+                }
+            }
+            if (!ok) {
+                for (int q = 0; q < kTileStages; ++q)
+                    if (issued_mask & (1u << q))
+                        drain_wait(smem_u32(&ctl->full[q]), (issued_ph >> q) & 1u, tmo, kid);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16_f32(kTileM, kTileN);
+            uint32_t s = 0, ph = 0;
+            bool ok = true, any = false;
+            int it = 0;
+            for (int tile = blockIdx.x; ok && tile < n_work; tile += gridDim.x, ++it) {
+                const int b = it & 1;
+                const uint32_t aph = (it >> 1) & 1;
+                if (!mbar_wait(smem_u32(&ctl->tempty[b]), aph ^ 1, tmo, abort_flag)) {
+                    raise_abort(ctl, kid, W_MMA);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + b * kTileAccCols;
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!mbar_wait(smem_u32(&ctl->full[s]), ph, tmo, abort_flag)) {
+                        raise_abort(ctl, kid, W_MMA);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(smem + (size_t)s * kTileStageBytes);
+                    const uint64_t adesc = sw128_kmajor_desc(sa);
+                    const uint64_t bdesc = sw128_kmajor_desc(sa + kTileABytes);
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk)
+                        mma_bf16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (kb | kk) != 0);
+                    any = true;
+                    mma_commit(smem_u32(&ctl->empty[s]));
+                    if (++s == kTileStages) { s = 0; ph ^= 1; }
+                }
+                if (!ok) break;
+                mma_commit(smem_u32(&ctl->tfull[b]));
+            }
+            if (any) {
+                mma_commit(smem_u32(&ctl->drain));
+                drain_wait(smem_u32(&ctl->drain), 0, tmo, kid);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------ epilogue (warps 2-5)
+        const int sub = warp & 3;
+        const int row_in_tile = sub * 32 + lane;
+        int it = 0;
+        for (int tile = blockIdx.x; tile < n_work; tile += gridDim.x, ++it) {
+            int e, nt, mt;
+            decode(tile, e, nt, mt);
+            const int b = it & 1;
+            const uint32_t aph = (it >> 1) & 1;
+            if (!mbar_wait(smem_u32(&ctl->tfull[b]), aph, tmo, abort_flag)) {
+                raise_abort(ctl, kid, W_EPILOGUE);
+                break;
+            }
+            tc_fence_after();
+            const uint32_t taddr = tmem_base + b * kTileAccCols + ((uint32_t)(sub * 32) << 16);
+            const int grow = mt * kTileM + row_in_tile;
+            const bool valid = grow < ctl->cnt[e];
+            const int64_t r = ctl->off[e] + grow;
+            if (UP) {
+                __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(args.out) + r * args.ldo + nt * kTileM;
+#pragma unroll 1
+                for (int j = 0; j < kTileM; j += 16) {
+                    uint32_t u[16], v[16];
+                    tmem_ld16(taddr + j, u);
+                    tmem_ld16(taddr + kTileM + j, v);
+                    tmem_wait_ld();
+                    uint32_t pk[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const float h0 = silu_f32(__uint_as_float(u[2 * i])) * __uint_as_float(v[2 * i]);
+                        const float h1 = silu_f32(__uint_as_float(u[2 * i + 1])) * __uint_as_float(v[2 * i + 1]);
+                        pk[i] = pack_bf16x2(h0, h1);
+                    }
+                    if (valid) {
+                        uint4* dst = reinterpret_cast<uint4*>(out + j);
+                        dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                        dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                    }
+                }
+            } else {
+                const float pw = valid ? args.perm_w[r] : 0.f;
+                float* out = reinterpret_cast<float*>(args.out) + r * args.ldo + nt * kTileN;
+#pragma unroll 1
+                for (int j = 0; j < kTileN; j += 16) {
+                    uint32_t a[16];
+                    tmem_ld16(taddr + j, a);
+                    tmem_wait_ld();
+                    if (valid) {
+                        float4* dst = reinterpret_cast<float4*>(out + j);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            dst[i] = make_float4(pw * __uint_as_float(a[4 * i]), pw * __uint_as_float(a[4 * i + 1]),
+                                                 pw * __uint_as_float(a[4 * i + 2]), pw * __uint_as_float(a[4 * i + 3]));
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[b]));
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, 2 * kTileAccCols);
+}
+
+// ---------------------------------------------------------------------------
+// weight-streaming kernels
+// ---------------------------------------------------------------------------
+struct StreamArgs {
+    const int32_t* offsets;  // [E+1]
+    float* part;             // fp32 partials
+    int E;
+    int R;          // rows of x_perm / H (= 2T)
+    int kslice;     // K elements per unit
+    int S;          // K slices
+    int RB;         // 128-row blocks per weight matrix of one expert
+    int nmat;       // 2 (W1 and W3) or 1 (W2)
+    int w_rows;     // rows of one expert in the weight map (ffn or d)
+    int nb;         // token rows per MMA (N), multiple of 16, <= 64
+    int stages;     // pipeline depth
+    uint32_t stage_bytes;
+    uint64_t timeout_ns;
+};
+
+inline size_t stream_smem_bytes(int nb, int stages) {
+    const size_t stage = kStreamABytes + (size_t)((nb * 128 + 1023) / 1024) * 1024;
+    return 1024 + stage * stages + sizeof(TcControl);
+}
+
+// UP = true: partials of W1 x and W3 x, layout [S][2][R][ffn].
+// UP = false: partials of W2 h, layout [S][R][d].
+template <bool UP>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    stream_gemm_kernel(const __grid_constant__ CUtensorMap map_w0, const __grid_constant__ CUtensorMap map_w1,
+                       const __grid_constant__ CUtensorMap map_x, const StreamArgs args) {
+    extern __shared__ unsigned char tc_smem_raw[];
+    unsigned char* smem = align1024(tc_smem_raw);
+    TcControl* ctl = reinterpret_cast<TcControl*>(smem + (size_t)args.stages * args.stage_bytes);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int kid = UP ? K_STREAM_UP : K_STREAM_DOWN;
+    const uint64_t tmo = args.timeout_ns;
+    volatile int* abort_flag = &ctl->abort_flag;
+    const int stages = args.stages;
+    const int units_per_expert = args.nmat * args.RB * args.S;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(smem_u32(&ctl->full[s]), 1);
+            mbar_init(smem_u32(&ctl->empty[s]), 1);
+        }
+        for (int b = 0; b < kStreamAcc; ++b) {
+            mbar_init(smem_u32(&ctl->tfull[b]), 1);
+            mbar_init(smem_u32(&ctl->tempty[b]), 4);
+        }
+        mbar_init(smem_u32(&ctl->drain), 1);
+        ctl->abort_flag = 0;
+        int n_act = 0;
+        for (int e = 0; e <= args.E; ++e) ctl->off[e] = args.offsets[e];
+        bool too_many = false;
+        for (int e = 0; e < args.E; ++e) {
+            const int c = ctl->off[e + 1] - ctl->off[e];
+            ctl->cnt[e] = c;
+            if (c > args.nb) too_many = true;
+            if (c > 0) ctl->act[n_act++] = e;
+        }
+        if (too_many) {
+            report_error(MOE_ERR_DEVICE_CHECK, kid, W_COUNT);
+            n_act = 0;
+        }
+        ctl->n_act = n_act;
+        ctl->n_work = n_act * units_per_expert;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&map_w0);
+        if (UP) tma_prefetch_desc(&map_w1);
+        tma_prefetch_desc(&map_x);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&ctl->tmem_base), kStreamAcc * kStreamMaxNB);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = ctl->tmem_base;
+    const int n_work = ctl->n_work;
+    const int KB = args.kslice / kBK;
+    const int S = args.S, RB = args.RB;
+
+    auto decode = [&](int u, int& e, int& m, int& rb, int& ks) {
+        const int ae = u / units_per_expert;
+        int rem = u - ae * units_per_expert;
+        ks = rem % S;
+        rem /= S;
+        rb = rem % RB;
+        m = rem / RB;
+        e = ctl->act[ae];
+    };
+
+    if (warp == 0) {
+        if (lane == 0) {
+            const uint64_t pol_w = policy_evict_first();
+            const uint64_t pol_x = policy_evict_last();
+            const uint32_t x_bytes = (uint32_t)args.nb * 128u;
+            uint32_t s = 0, ph = 0;
+            uint32_t issued_mask = 0, issued_ph = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; ok && u < n_work; u += gridDim.x) {
+                int e, m, rb, ks;
+                decode(u, e, m, rb, ks);
+                const int wrow = e * args.w_rows + rb * 128;
+                const int xrow = ctl->off[e];
+                const CUtensorMap* mw = (UP && m == 1) ? &map_w1 : &map_w0;
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!mbar_wait(smem_u32(&ctl->empty[s]), ph ^ 1, tmo, abort_flag)) {
+                        raise_abort(ctl, kid, W_PRODUCER);
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = smem_u32(&ctl->full[s]);
+                    const uint32_t sa = smem_u32(smem + (size_t)s * args.stage_bytes);
+                    const int kx = ks * args.kslice + kb * kBK;
+                    mbar_arrive_expect_tx(fb, kStreamABytes + x_bytes);
+                    tma_load_2d(sa, mw, fb, kx, wrow, pol_w);
+                    tma_load_2d(sa + kStreamABytes, &map_x, fb, kx, xrow, pol_x);
+                    issued_mask |= 1u << s;
+                    issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
+                    if (++s == (uint32_t)stages) { s = 0; ph ^= 1; }
+                }
+            }
+            if (!ok) {
+                for (int q = 0; q < stages; ++q)
+                    if (issued_mask & (1u << q))
+                        drain_wait(smem_u32(&ctl->full[q]), (issued_ph >> q) & 1u, tmo, kid);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16_f32(128, (uint32_t)args.nb);
+            uint32_t s = 0, ph = 0;
+            bool ok = true, any = false;
+            int it = 0;
+            for (int u = blockIdx.x; ok && u < n_work; u += gridDim.x, ++it) {
+                const int b = it % kStreamAcc;
+                const uint32_t aph = (it / kStreamAcc) & 1;
+                if (!mbar_wait(smem_u32(&ctl->tempty[b]), aph ^ 1, tmo, abort_flag)) {
+                    raise_abort(ctl, kid, W_MMA);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + b * kStreamMaxNB;
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!mbar_wait(smem_u32(&ctl->full[s]), ph, tmo, abort_flag)) {
+                        raise_abort(ctl, kid, W_MMA);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(smem + (size_t)s * args.stage_bytes);
+                    const uint64_t adesc = sw128_kmajor_desc(sa);
+                    const uint64_t bdesc = sw128_kmajor_desc(sa + kStreamABytes);
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk)
+                        mma_bf16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (kb | kk) != 0);
+                    any = true;
+                    mma_commit(smem_u32(&ctl->empty[s]));
+                    if (++s == (uint32_t)stages) { s = 0; ph ^= 1; }
+                }
+                if (!ok) break;
+                mma_commit(smem_u32(&ctl->tfull[b]));
+            }
+            if (any) {
+                mma_commit(smem_u32(&ctl->drain));
+                drain_wait(smem_u32(&ctl->drain), 0, tmo, kid);
+            }
+        }
+        __syncwarp();
+    } else {
+        const int sub = warp & 3;
+        const int wr = sub * 32 + lane;  // weight row inside the 128-row block
+        int it = 0;
+        for (int u = blockIdx.x; u < n_work; u += gridDim.x, ++it) {
+            int e, m, rb, ks;
+            decode(u, e, m, rb, ks);
+            const int b = it % kStreamAcc;
+            const uint32_t aph = (it / kStreamAcc) & 1;
+            if (!mbar_wait(smem_u32(&ctl->tfull[b]), aph, tmo, abort_flag)) {
+                raise_abort(ctl, kid, W_EPILOGUE);
+                break;
+            }
+            tc_fence_after();
+            const uint32_t taddr = tmem_base + b * kStreamMaxNB + ((uint32_t)(sub * 32) << 16);
+            const int cnt = ctl->cnt[e];
+            const int64_t plane = UP ? ((int64_t)ks * 2 + m) : (int64_t)ks;
+            float* dst = args.part + (plane * args.R + ctl->off[e]) * (int64_t)args.w_rows + rb * 128 + wr;
+            for (int n0 = 0; n0 < args.nb; n0 += 16) {
+                uint32_t a[16];
+                tmem_ld16(taddr + n0, a);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    if (n0 + i < cnt) dst[(int64_t)(n0 + i) * args.w_rows] = __uint_as_float(a[i]);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[b]));
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, kStreamAcc * kStreamMaxNB);
+}
+
+// H[r][f] = bf16( SiLU(sum_s U_s[r][f]) * sum_s V_s[r][f] ), partials [S][2][R][F]
+__global__ void __launch_bounds__(256)
+    reduce_swiglu_kernel(const float* __restrict__ part, int S, int64_t R, int F,
+                         __nv_bfloat16* __restrict__ H) {
+    const int64_t n = R * F;
+    const int64_t plane = R * F;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        float u = 0.f, v = 0.f;
+        for (int s = 0; s < S; ++s) {
+            u += part[(2 * (int64_t)s) * plane + i];
+            v += part[(2 * (int64_t)s + 1) * plane + i];
+        }
+        H[i] = __float2bfloat16_rn(silu_f32(u) * v);
+    }
+}
+
+// y_slot[r][c] = perm_w[r] * sum_s P_s[r][c], partials [S][R][d]
+__global__ void __launch_bounds__(256)
+    reduce_down_kernel(const float* __restrict__ part, int S, int64_t R, int d,
+                       const float* __restrict__ perm_w, float* __restrict__ y_slot) {
+    const int64_t n = R * d;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        float acc = 0.f;
+        for (int s = 0; s < S; ++s) acc += part[(int64_t)s * n + i];
+        y_slot[i] = perm_w[i / d] * acc;
+    }
+}
+
+}  // namespace moe

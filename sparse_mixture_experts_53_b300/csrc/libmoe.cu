@@ -1,0 +1,590 @@
+// C ABI of the top-2 sparse MoE layer (declared in include/moe.h): argument
+// checks, workspace layout, tensor-map encoding, kernel dispatch, per-kernel
+// timing and the device status word. All device work is in the kernels
+// included below; this file only marshals arguments and enqueues launches on
+// the caller's stream.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <string>
+#include <vector>
+
+#include "common.cuh"
+#include "ffn_f32.cuh"
+#include "ffn_tc.cuh"
+#include "permute.cuh"
+#include "router.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr size_t kAlign = 1024;
+constexpr int kStreamMaxTokens = 64;     // weight-streaming path needs T <= 64
+constexpr size_t kSmemBudget = 225 * 1024;
+
+struct TimingRecord {
+    const char* name;
+    cudaEvent_t start, stop;
+};
+
+struct HostState {
+    int ffn_path = 0;          // 0 auto, 1 token tiles, 2 weight streaming
+    int64_t kslice = 0;        // 0 auto
+    int grid = 0;              // 0 = one CTA per SM
+    uint64_t timeout_ns = 2000000000ull;
+    bool timing = false;
+    std::vector<TimingRecord> records;
+    std::vector<cudaEvent_t> pool;
+    int sms[kMaxDevices] = {0};
+    bool attr_set[kMaxDevices][8] = {{false}};
+};
+HostState g;
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int current_device() {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    return dev;
+}
+
+int sm_count() {
+    const int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices) return 148;
+    if (g.sms[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+        g.sms[dev] = n;
+    }
+    return g.sms[dev];
+}
+
+// Raises a kernel's dynamic shared-memory limit once per device.
+template <typename K>
+bool ensure_smem(K kernel, int slot, size_t bytes) {
+    const int dev = current_device();
+    if (dev >= 0 && dev < kMaxDevices && g.attr_set[dev][slot]) return true;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) != cudaSuccess)
+        return false;
+    if (dev >= 0 && dev < kMaxDevices) g.attr_set[dev][slot] = true;
+    return true;
+}
+
+cudaEvent_t take_event() {
+    if (!g.pool.empty()) {
+        cudaEvent_t e = g.pool.back();
+        g.pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+}
+
+template <typename F>
+moe_status launch(const char* name, cudaStream_t st, F&& f) {
+    cudaEvent_t a = nullptr, b = nullptr;
+    if (g.timing) {
+        a = take_event();
+        b = take_event();
+        cudaEventRecord(a, st);
+    }
+    f();
+    const cudaError_t err = cudaGetLastError();
+    if (g.timing) {
+        cudaEventRecord(b, st);
+        g.records.push_back({name, a, b});
+    }
+    return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+#define MOE_TRY(expr)                         \
+    do {                                      \
+        const moe_status _st = (expr);        \
+        if (_st != MOE_OK) return _st;        \
+    } while (0)
+
+// ------------------------------------------------------------- tensor maps
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// 2-D bf16 matrix [rows][inner], boxes of box_rows x 64 elements, 128-byte
+// swizzle (the layout the MMA descriptors expect), zero fill outside.
+bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {inner, rows};
+    const cuuint64_t strides[1] = {inner * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)kBK, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------ validation
+moe_status check_shape(const moe_shape* s) {
+    if (s == nullptr) return MOE_ERR_INVALID_ARG;
+    if (s->T < 0 || s->T > (int64_t(1) << 29) || s->d <= 0 || s->ffn <= 0) return MOE_ERR_INVALID_ARG;
+    if (s->dtype != MOE_F32 && s->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+    if (s->E != 8 || s->k != 2) return MOE_ERR_UNSUPPORTED;
+    if (s->dtype == MOE_BF16 && (s->d % 256 != 0 || s->ffn % 128 != 0)) return MOE_ERR_UNSUPPORTED;
+    if ((int64_t)s->d * s->ffn > (int64_t(1) << 31) / 8) return MOE_ERR_UNSUPPORTED;  // int32 weight rows
+    return MOE_OK;
+}
+
+bool ok_ptr(const void* p) { return p != nullptr && aligned16(p); }
+
+size_t esize(const moe_shape& s) { return s.dtype == MOE_BF16 ? 2 : 4; }
+
+int pick_kslice(int K) {
+    if (g.kslice > 0 && g.kslice % kBK == 0 && K % g.kslice == 0) return (int)g.kslice;
+    for (int ks = 1024; ks >= kBK; ks -= kBK)
+        if (K % ks == 0) return ks;
+    return K;
+}
+
+// 1 = token tiles, 2 = weight streaming, 0 = unsupported request
+int choose_path(const moe_shape& s) {
+    if (s.dtype != MOE_BF16) return 0;
+    if (g.ffn_path == 1) return 1;
+    if (g.ffn_path == 2) return s.T <= kStreamMaxTokens ? 2 : 0;
+    return s.T <= kStreamMaxTokens ? 2 : 1;
+}
+
+struct FfnLayout {
+    int path = 0;
+    int nb = 0, ks_up = 0, ks_down = 0, S_up = 0, S_down = 0;
+    size_t h = 0, part_up = 0, part_down = 0, total = 0;
+};
+
+FfnLayout ffn_layout(const moe_shape& s) {
+    FfnLayout L;
+    const size_t R = (size_t)(2 * s.T);
+    size_t off = 0;
+    L.h = off;
+    off = align_up(off + R * s.ffn * esize(s), kAlign);
+    if (s.dtype == MOE_BF16) {
+        L.path = choose_path(s);
+        if (L.path == 2) {
+            L.nb = (int)align_up((size_t)(s.T > 0 ? s.T : 1), 16);
+            L.ks_up = pick_kslice(s.d);
+            L.ks_down = pick_kslice(s.ffn);
+            L.S_up = s.d / L.ks_up;
+            L.S_down = s.ffn / L.ks_down;
+            L.part_up = off;
+            off = align_up(off + (size_t)L.S_up * 2 * R * s.ffn * 4, kAlign);
+            L.part_down = off;
+            off = align_up(off + (size_t)L.S_down * R * s.d * 4, kAlign);
+        }
+    }
+    L.total = off;
+    return L;
+}
+
+struct FwdLayout {
+    size_t idx, w, logits, counts, offsets, perm_token, slot_row, perm_w, x_perm, y_slot, ffn, total;
+    FfnLayout f;
+};
+
+FwdLayout fwd_layout(const moe_shape& s) {
+    FwdLayout L;
+    const size_t T = (size_t)s.T, R = 2 * T, E = (size_t)s.E;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off = align_up(off + bytes, kAlign);
+        return at;
+    };
+    L.idx = take(R * 4);
+    L.w = take(R * 4);
+    L.logits = take(T * E * 4);
+    L.counts = take(E * 4);
+    L.offsets = take((E + 1) * 4);
+    L.perm_token = take(R * 4);
+    L.slot_row = take(R * 4);
+    L.perm_w = take(R * 4);
+    L.x_perm = take(R * s.d * esize(s));
+    L.y_slot = take(R * s.d * 4);
+    L.f = ffn_layout(s);
+    L.ffn = take(L.f.total);
+    L.total = off;
+    return L;
+}
+
+// --------------------------------------------------------------- stages
+moe_status run_router(const moe_shape& s, const void* x, const void* wg, int32_t* idx, float* w, float* logits,
+                      cudaStream_t st) {
+    if (s.T == 0) return MOE_OK;
+    const size_t es = esize(s);
+    const size_t wbytes = (size_t)s.E * s.d * es;
+    const int use_smem = wbytes <= 200 * 1024 ? 1 : 0;
+    const int V = (int)(16 / es);
+    const int vec = (s.d % V == 0 && aligned16(x) && aligned16(wg)) ? 1 : 0;
+    const int64_t blocks = (s.T + kRouterWarps - 1) / kRouterWarps;
+    const int grid = (int)std::min<int64_t>(blocks, (int64_t)sm_count() * 4);
+    const size_t smem = use_smem ? wbytes : 0;
+    if (s.dtype == MOE_BF16) {
+        if (!ensure_smem(router_top2_kernel<__nv_bfloat16>, 0, 200 * 1024)) return MOE_ERR_CUDA;
+        return launch("router_top2", st, [&] {
+            router_top2_kernel<__nv_bfloat16><<<grid, kRouterWarps * 32, smem, st>>>(
+                static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(wg), s.T, s.d, s.E,
+                use_smem, vec, idx, w, logits);
+        });
+    }
+    if (!ensure_smem(router_top2_kernel<float>, 1, 200 * 1024)) return MOE_ERR_CUDA;
+    return launch("router_top2", st, [&] {
+        router_top2_kernel<float><<<grid, kRouterWarps * 32, smem, st>>>(
+            static_cast<const float*>(x), static_cast<const float*>(wg), s.T, s.d, s.E, use_smem, vec, idx, w,
+            logits);
+    });
+}
+
+moe_status run_permute(const moe_shape& s, const int32_t* idx, const float* w, const void* x, int32_t* counts,
+                       int32_t* offsets, int32_t* perm_token, int32_t* slot_row, float* perm_w, void* x_perm,
+                       cudaStream_t st) {
+    MOE_TRY(launch("permute", st, [&] {
+        permute_kernel<<<1, kPermuteThreads, 0, st>>>(idx, w, s.T, s.E, counts, offsets, perm_token, slot_row,
+                                                      perm_w);
+    }));
+    if (s.T == 0) return MOE_OK;
+    const int64_t R = 2 * s.T;
+    const int grid = (int)std::min<int64_t>(R, (int64_t)sm_count() * 8);
+    return launch("gather_rows", st, [&] {
+        gather_rows_kernel<<<grid, 256, 0, st>>>(static_cast<const unsigned char*>(x), perm_token, offsets, s.E, R,
+                                                  (int64_t)s.d * esize(s), static_cast<unsigned char*>(x_perm));
+    });
+}
+
+int tc_grid(int64_t work_upper) {
+    const int sms = g.grid > 0 ? g.grid : sm_count();
+    return (int)std::max<int64_t>(1, std::min<int64_t>(work_upper, sms));
+}
+
+moe_status run_ffn(const moe_shape& s, const void* x_perm, const int32_t* offsets, const float* perm_w,
+                   const void* w1, const void* w3, const void* w2, float* y_slot, unsigned char* ws,
+                   const FfnLayout& L, cudaStream_t st) {
+    if (s.T == 0) return MOE_OK;
+    const int64_t R = 2 * s.T;
+    const int d = s.d, F = s.ffn, E = s.E;
+    if (s.dtype == MOE_F32) {
+        float* H = reinterpret_cast<float*>(ws + L.h);
+        const int gy = (int)((R + kF32Tile - 1) / kF32Tile + E);
+        MOE_TRY(launch("f32_up", st, [&] {
+            f32_ffn_kernel<true><<<dim3((F + kF32Tile - 1) / kF32Tile, gy), dim3(32, 8), 0, st>>>(
+                static_cast<const float*>(x_perm), offsets, E, static_cast<const float*>(w1),
+                static_cast<const float*>(w3), nullptr, d, F, H);
+        }));
+        return launch("f32_down", st, [&] {
+            f32_ffn_kernel<false><<<dim3((d + kF32Tile - 1) / kF32Tile, gy), dim3(32, 8), 0, st>>>(
+                H, offsets, E, static_cast<const float*>(w2), nullptr, perm_w, F, d, y_slot);
+        });
+    }
+    __nv_bfloat16* H = reinterpret_cast<__nv_bfloat16*>(ws + L.h);
+    if (L.path == 1) {
+        CUtensorMap ma, mb0, mb1;
+        if (!make_map(&ma, x_perm, d, R, kTileM) || !make_map(&mb0, w1, d, (uint64_t)E * F, kTileM) ||
+            !make_map(&mb1, w3, d, (uint64_t)E * F, kTileM))
+            return MOE_ERR_CUDA;
+        if (!ensure_smem(tile_gemm_kernel<true>, 2, kTileSmemBytes)) return MOE_ERR_CUDA;
+        TileArgs up{offsets, perm_w, H, E, d, F / kTileM, F, F, g.timeout_ns};
+        const int64_t tiles_up = ((R + kTileM - 1) / kTileM + E) * (F / kTileM);
+        MOE_TRY(launch("tile_up_swiglu", st, [&] {
+            tile_gemm_kernel<true><<<tc_grid(tiles_up), kTcThreads, kTileSmemBytes, st>>>(ma, mb0, mb1, up);
+        }));
+        CUtensorMap mh, mw2;
+        if (!make_map(&mh, H, F, R, kTileM) || !make_map(&mw2, w2, F, (uint64_t)E * d, kTileN)) return MOE_ERR_CUDA;
+        if (!ensure_smem(tile_gemm_kernel<false>, 3, kTileSmemBytes)) return MOE_ERR_CUDA;
+        TileArgs down{offsets, perm_w, y_slot, E, F, d / kTileN, d, d, g.timeout_ns};
+        const int64_t tiles_down = ((R + kTileM - 1) / kTileM + E) * (d / kTileN);
+        return launch("tile_down_scale", st, [&] {
+            tile_gemm_kernel<false><<<tc_grid(tiles_down), kTcThreads, kTileSmemBytes, st>>>(mh, mw2, mw2, down);
+        });
+    }
+    if (L.path != 2) return MOE_ERR_UNSUPPORTED;
+    float* part_up = reinterpret_cast<float*>(ws + L.part_up);
+    float* part_down = reinterpret_cast<float*>(ws + L.part_down);
+    const uint32_t stage_bytes = kStreamABytes + (uint32_t)align_up((size_t)L.nb * 128, 1024);
+    const int stages = (int)std::min<size_t>(kMaxStreamStages, (kSmemBudget - 1024 - sizeof(TcControl)) / stage_bytes);
+    const size_t smem = stream_smem_bytes(L.nb, stages);
+    CUtensorMap mw1, mw3, mx;
+    if (!make_map(&mw1, w1, d, (uint64_t)E * F, 128) || !make_map(&mw3, w3, d, (uint64_t)E * F, 128) ||
+        !make_map(&mx, x_perm, d, R, L.nb))
+        return MOE_ERR_CUDA;
+    if (!ensure_smem(stream_gemm_kernel<true>, 4, kSmemBudget)) return MOE_ERR_CUDA;
+    StreamArgs up{offsets, part_up, E, (int)R, L.ks_up, L.S_up, F / 128, 2, F, L.nb, stages, stage_bytes,
+                  g.timeout_ns};
+    MOE_TRY(launch("stream_up", st, [&] {
+        stream_gemm_kernel<true><<<tc_grid((int64_t)E * 2 * (F / 128) * L.S_up), kTcThreads, smem, st>>>(mw1, mw3,
+                                                                                                       mx, up);
+    }));
+    const int rgrid = (int)std::min<int64_t>((R * F + 255) / 256, (int64_t)sm_count() * 8);
+    MOE_TRY(launch("reduce_swiglu", st, [&] {
+        reduce_swiglu_kernel<<<rgrid, 256, 0, st>>>(part_up, L.S_up, R, F, H);
+    }));
+    CUtensorMap mw2, mh;
+    if (!make_map(&mw2, w2, F, (uint64_t)E * d, 128) || !make_map(&mh, H, F, R, L.nb)) return MOE_ERR_CUDA;
+    if (!ensure_smem(stream_gemm_kernel<false>, 5, kSmemBudget)) return MOE_ERR_CUDA;
+    StreamArgs down{offsets, part_down, E, (int)R, L.ks_down, L.S_down, d / 128, 1, d, L.nb, stages, stage_bytes,
+                    g.timeout_ns};
+    MOE_TRY(launch("stream_down", st, [&] {
+        stream_gemm_kernel<false><<<tc_grid((int64_t)E * (d / 128) * L.S_down), kTcThreads, smem, st>>>(mw2, mw2,
+                                                                                                      mh, down);
+    }));
+    const int dgrid = (int)std::min<int64_t>((R * d + 255) / 256, (int64_t)sm_count() * 8);
+    return launch("reduce_down", st, [&] {
+        reduce_down_kernel<<<dgrid, 256, 0, st>>>(part_down, L.S_down, R, d, perm_w, y_slot);
+    });
+}
+
+moe_status run_combine(const moe_shape& s, const float* y_slot, const int32_t* slot_row, void* y,
+                       cudaStream_t st) {
+    if (s.T == 0) return MOE_OK;
+    const bool v4 = (s.d % 4 == 0) && aligned16(y_slot) && aligned16(y);
+    const int64_t n = v4 ? s.T * (s.d / 4) : s.T * s.d;
+    const int grid = (int)std::min<int64_t>((n + 255) / 256, (int64_t)sm_count() * 8);
+    if (s.dtype == MOE_BF16) {
+        return launch("combine", st, [&] {
+            if (v4)
+                combine4_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(y_slot, slot_row, s.T, s.d,
+                                                                     static_cast<__nv_bfloat16*>(y));
+            else
+                combine_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(y_slot, slot_row, s.T, s.d,
+                                                                    static_cast<__nv_bfloat16*>(y));
+        });
+    }
+    return launch("combine", st, [&] {
+        if (v4)
+            combine4_kernel<float><<<grid, 256, 0, st>>>(y_slot, slot_row, s.T, s.d, static_cast<float*>(y));
+        else
+            combine_kernel<float><<<grid, 256, 0, st>>>(y_slot, slot_row, s.T, s.d, static_cast<float*>(y));
+    });
+}
+
+moe_status run_aux(const moe_shape& s, const float* logits, const int32_t* counts, float* f, float* P,
+                   float* l_aux, cudaStream_t st) {
+    if (s.T == 0) {
+        if (cudaMemsetAsync(f, 0, sizeof(float) * s.E, st) != cudaSuccess ||
+            cudaMemsetAsync(P, 0, sizeof(float) * s.E, st) != cudaSuccess ||
+            cudaMemsetAsync(l_aux, 0, sizeof(float), st) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        return MOE_OK;
+    }
+    return launch("aux_stats", st, [&] {
+        aux_stats_kernel<<<1, kAuxThreads, 0, st>>>(logits, counts, s.T, s.E, f, P, l_aux);
+    });
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char* moe_version(void) { return "moe-b300 0.1 (sm_103a)"; }
+
+const char* moe_status_string(moe_status s) {
+    switch (s) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID_ARG: return "invalid argument";
+        case MOE_ERR_UNSUPPORTED: return "unsupported shape";
+        case MOE_ERR_WORKSPACE: return "workspace too small";
+        case MOE_ERR_CUDA: return "CUDA error";
+        case MOE_ERR_TIMEOUT: return "device wait timed out";
+        case MOE_ERR_DEVICE_CHECK: return "device index check failed";
+    }
+    return "unknown status";
+}
+
+size_t moe_workspace_bytes(const moe_shape* s) {
+    if (check_shape(s) != MOE_OK) return 0;
+    if (s->dtype == MOE_BF16 && choose_path(*s) == 0) return 0;
+    return fwd_layout(*s).total;
+}
+
+size_t moe_ffn_workspace_bytes(const moe_shape* s) {
+    if (check_shape(s) != MOE_OK) return 0;
+    if (s->dtype == MOE_BF16 && choose_path(*s) == 0) return 0;
+    return ffn_layout(*s).total;
+}
+
+moe_status moe_route_top2(const moe_shape* s, const void* x, const void* w_gate, int32_t* topk_idx, float* topk_w,
+                          float* logits, void* stream) {
+    MOE_TRY(check_shape(s));
+    if (s->T > 0 && (!ok_ptr(x) || !ok_ptr(w_gate) || !ok_ptr(topk_idx) || !ok_ptr(topk_w) ||
+                     (logits != nullptr && !aligned16(logits))))
+        return MOE_ERR_INVALID_ARG;
+    return run_router(*s, x, w_gate, topk_idx, topk_w, logits, static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_permute(const moe_shape* s, const int32_t* topk_idx, const float* topk_w, const void* x,
+                       int32_t* counts, int32_t* offsets, int32_t* perm_token, int32_t* slot_row, float* perm_w,
+                       void* x_perm, void* stream) {
+    MOE_TRY(check_shape(s));
+    if (!ok_ptr(counts) || !ok_ptr(offsets)) return MOE_ERR_INVALID_ARG;
+    if (s->T > 0 && (!ok_ptr(topk_idx) || !ok_ptr(topk_w) || !ok_ptr(x) || !ok_ptr(perm_token) ||
+                     !ok_ptr(slot_row) || !ok_ptr(perm_w) || !ok_ptr(x_perm)))
+        return MOE_ERR_INVALID_ARG;
+    return run_permute(*s, topk_idx, topk_w, x, counts, offsets, perm_token, slot_row, perm_w, x_perm,
+                       static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_expert_ffn(const moe_shape* s, const void* x_perm, const int32_t* offsets, const float* perm_w,
+                          const void* w1, const void* w3, const void* w2, float* y_slot, void* ws, size_t ws_bytes,
+                          void* stream) {
+    MOE_TRY(check_shape(s));
+    if (s->T == 0) return MOE_OK;
+    if (!ok_ptr(x_perm) || !ok_ptr(offsets) || !ok_ptr(perm_w) || !ok_ptr(w1) || !ok_ptr(w3) || !ok_ptr(w2) ||
+        !ok_ptr(y_slot) || !ok_ptr(ws))
+        return MOE_ERR_INVALID_ARG;
+    if (s->dtype == MOE_BF16 && choose_path(*s) == 0) return MOE_ERR_UNSUPPORTED;
+    const FfnLayout L = ffn_layout(*s);
+    if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+    return run_ffn(*s, x_perm, offsets, perm_w, w1, w3, w2, y_slot, static_cast<unsigned char*>(ws), L,
+                   static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_combine(const moe_shape* s, const float* y_slot, const int32_t* slot_row, void* y, void* stream) {
+    MOE_TRY(check_shape(s));
+    if (s->T > 0 && (!ok_ptr(y_slot) || !ok_ptr(slot_row) || !ok_ptr(y))) return MOE_ERR_INVALID_ARG;
+    return run_combine(*s, y_slot, slot_row, y, static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_aux_stats(const moe_shape* s, const float* logits, const int32_t* counts, float* f, float* P,
+                         float* l_aux, void* stream) {
+    MOE_TRY(check_shape(s));
+    if (!ok_ptr(counts) || !ok_ptr(f) || !ok_ptr(P) || !ok_ptr(l_aux)) return MOE_ERR_INVALID_ARG;
+    if (s->T > 0 && !ok_ptr(logits)) return MOE_ERR_INVALID_ARG;
+    return run_aux(*s, logits, counts, f, P, l_aux, static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_layer_forward(const moe_shape* s, const void* x, const void* w_gate, const void* w1, const void* w3,
+                             const void* w2, void* y, float* aux_f, float* aux_P, float* aux_l_aux, void* ws,
+                             size_t ws_bytes, void* stream) {
+    MOE_TRY(check_shape(s));
+    const bool aux = aux_f != nullptr && aux_P != nullptr && aux_l_aux != nullptr;
+    if ((aux_f != nullptr || aux_P != nullptr || aux_l_aux != nullptr) && !aux) return MOE_ERR_INVALID_ARG;
+    if (aux && (!ok_ptr(aux_f) || !ok_ptr(aux_P) || !ok_ptr(aux_l_aux))) return MOE_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (s->T == 0) return aux ? run_aux(*s, nullptr, nullptr, aux_f, aux_P, aux_l_aux, st) : MOE_OK;
+    if (!ok_ptr(x) || !ok_ptr(w_gate) || !ok_ptr(w1) || !ok_ptr(w3) || !ok_ptr(w2) || !ok_ptr(y) || !ok_ptr(ws))
+        return MOE_ERR_INVALID_ARG;
+    if (s->dtype == MOE_BF16 && choose_path(*s) == 0) return MOE_ERR_UNSUPPORTED;
+    const FwdLayout L = fwd_layout(*s);
+    if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+    unsigned char* w = static_cast<unsigned char*>(ws);
+    int32_t* idx = reinterpret_cast<int32_t*>(w + L.idx);
+    float* gw = reinterpret_cast<float*>(w + L.w);
+    float* logits = aux ? reinterpret_cast<float*>(w + L.logits) : nullptr;
+    int32_t* counts = reinterpret_cast<int32_t*>(w + L.counts);
+    int32_t* offsets = reinterpret_cast<int32_t*>(w + L.offsets);
+    int32_t* perm_token = reinterpret_cast<int32_t*>(w + L.perm_token);
+    int32_t* slot_row = reinterpret_cast<int32_t*>(w + L.slot_row);
+    float* perm_w = reinterpret_cast<float*>(w + L.perm_w);
+    void* x_perm = w + L.x_perm;
+    float* y_slot = reinterpret_cast<float*>(w + L.y_slot);
+    MOE_TRY(run_router(*s, x, w_gate, idx, gw, logits, st));
+    MOE_TRY(run_permute(*s, idx, gw, x, counts, offsets, perm_token, slot_row, perm_w, x_perm, st));
+    MOE_TRY(run_ffn(*s, x_perm, offsets, perm_w, w1, w3, w2, y_slot, w + L.ffn, L.f, st));
+    MOE_TRY(run_combine(*s, y_slot, slot_row, y, st));
+    if (aux) MOE_TRY(run_aux(*s, logits, counts, aux_f, aux_P, aux_l_aux, st));
+    return MOE_OK;
+}
+
+moe_status moe_get_device_status(int32_t* code, int32_t* detail) {
+    if (code == nullptr) return MOE_ERR_INVALID_ARG;
+    if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
+    int h[4] = {0, 0, 0, 0};
+    if (cudaMemcpyFromSymbol(h, g_status, sizeof(h)) != cudaSuccess) return MOE_ERR_CUDA;
+    const int zero[4] = {0, 0, 0, 0};
+    if (cudaMemcpyToSymbol(g_status, zero, sizeof(zero)) != cudaSuccess) return MOE_ERR_CUDA;
+    *code = h[0];
+    if (detail != nullptr) *detail = h[1] * 100 + h[2];
+    return MOE_OK;
+}
+
+moe_status moe_set_wait_timeout_ns(uint64_t ns) {
+    if (ns == 0) return MOE_ERR_INVALID_ARG;
+    g.timeout_ns = ns;
+    return MOE_OK;
+}
+
+moe_status moe_set_knob(int32_t knob, int64_t value) {
+    switch (knob) {
+        case MOE_KNOB_FFN_PATH:
+            if (value < 0 || value > 2) return MOE_ERR_INVALID_ARG;
+            g.ffn_path = (int)value;
+            return MOE_OK;
+        case MOE_KNOB_KSLICE:
+            if (value < 0 || value % kBK != 0) return MOE_ERR_INVALID_ARG;
+            g.kslice = value;
+            return MOE_OK;
+        case MOE_KNOB_GRID:
+            if (value < 0 || value > 65535) return MOE_ERR_INVALID_ARG;
+            g.grid = (int)value;
+            return MOE_OK;
+    }
+    return MOE_ERR_INVALID_ARG;
+}
+
+moe_status moe_timing_enable(int32_t enable) {
+    g.timing = enable != 0;
+    return MOE_OK;
+}
+
+moe_status moe_timing_read(char* buf, size_t n) {
+    std::map<std::string, std::pair<long, double>> agg;
+    moe_status rc = MOE_OK;
+    for (const TimingRecord& r : g.records) {
+        float ms = 0.f;
+        if (cudaEventSynchronize(r.stop) != cudaSuccess || cudaEventElapsedTime(&ms, r.start, r.stop) != cudaSuccess)
+            rc = MOE_ERR_CUDA;
+        auto& a = agg[r.name];
+        a.first += 1;
+        a.second += ms;
+        g.pool.push_back(r.start);
+        g.pool.push_back(r.stop);
+    }
+    g.records.clear();
+    std::string out = "{";
+    bool first = true;
+    for (const auto& kv : agg) {
+        char line[160];
+        std::snprintf(line, sizeof(line), "%s\"%s\": [%ld, %.6f]", first ? "" : ", ", kv.first.c_str(),
+                      kv.second.first, kv.second.second);
+        out += line;
+        first = false;
+    }
+    out += "}";
+    if (buf != nullptr && n > 0) {
+        std::strncpy(buf, out.c_str(), n - 1);
+        buf[n - 1] = '\0';
+    }
+    return rc;
+}
+
+}  // extern "C"

@@ -1,0 +1,142 @@
+// Router: scores l = x . W_g, top-2 selection and the softmax over the two
+// kept scores ("Mixtral of Experts" lecture, router walkthrough;
+// tokentrails.org "Mixtral", step "The router").
+//
+// One warp per token. W_g (E x d, 64 KB in bf16 at d = 4096) is staged once
+// per CTA in shared memory; each lane accumulates a fixed, strided share of
+// the d products for all E experts in fp32, then a butterfly of warp shuffles
+// leaves the E totals in every lane. The reduction order is fixed, so the
+// result does not depend on the grid.
+#pragma once
+
+#include "common.cuh"
+
+namespace moe {
+
+constexpr int kRouterWarps = 8;
+
+template <typename T>
+struct Vec16;  // 16-byte vector of stored elements
+template <>
+struct Vec16<__nv_bfloat16> {
+    static constexpr int N = 8;
+};
+template <>
+struct Vec16<float> {
+    static constexpr int N = 4;
+};
+
+template <typename T>
+__device__ __forceinline__ void load_vec(const T* p, float (&v)[Vec16<T>::N]) {
+    const uint4 raw = *reinterpret_cast<const uint4*>(p);
+    if constexpr (sizeof(T) == 2) {
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float2 f = __bfloat1622float2(h[i]);
+            v[2 * i] = f.x;
+            v[2 * i + 1] = f.y;
+        }
+    } else {
+        const float* f = reinterpret_cast<const float*>(&raw);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = f[i];
+    }
+}
+
+// use_smem: W_g is copied to shared memory (E * d * sizeof(T) bytes of
+// dynamic shared memory); otherwise it is read through L1/L2.
+// vec: rows are 16-byte aligned and d is a multiple of the vector width.
+template <typename T>
+__global__ void __launch_bounds__(kRouterWarps * 32)
+    router_top2_kernel(const T* __restrict__ x, const T* __restrict__ wg, int64_t T_tokens, int d,
+                       int E, int use_smem, int vec, int32_t* __restrict__ topk_idx,
+                       float* __restrict__ topk_w, float* __restrict__ logits) {
+    extern __shared__ __align__(16) unsigned char router_smem[];
+    const T* w = wg;
+    if (use_smem) {
+        T* s = reinterpret_cast<T*>(router_smem);
+        const int64_t n = (int64_t)E * d;
+        if (vec) {
+            const int64_t nv = n / Vec16<T>::N;
+            for (int64_t i = threadIdx.x; i < nv; i += blockDim.x)
+                reinterpret_cast<uint4*>(s)[i] = reinterpret_cast<const uint4*>(wg)[i];
+        } else {
+            for (int64_t i = threadIdx.x; i < n; i += blockDim.x) s[i] = wg[i];
+        }
+        __syncthreads();
+        w = s;
+    }
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    constexpr int V = Vec16<T>::N;
+
+    for (int64_t t = (int64_t)blockIdx.x * kRouterWarps + warp; t < T_tokens;
+         t += (int64_t)gridDim.x * kRouterWarps) {
+        const T* xr = x + t * d;
+        float acc[kMaxExperts];
+#pragma unroll
+        for (int e = 0; e < kMaxExperts; ++e) acc[e] = 0.f;
+
+        int j0 = 0;
+        if (vec) {
+            const int nchunks = d / V;
+            for (int c = lane; c < nchunks; c += 32) {
+                float xv[V];
+                load_vec<T>(xr + c * V, xv);
+#pragma unroll
+                for (int e = 0; e < kMaxExperts; ++e) {
+                    if (e < E) {
+                        float wv[V];
+                        load_vec<T>(w + (int64_t)e * d + c * V, wv);
+#pragma unroll
+                        for (int i = 0; i < V; ++i) acc[e] = fmaf(xv[i], wv[i], acc[e]);
+                    }
+                }
+            }
+            j0 = nchunks * V;
+        }
+        for (int j = j0 + lane; j < d; j += 32) {
+            const float xv = to_f32<T>(xr[j]);
+#pragma unroll
+            for (int e = 0; e < kMaxExperts; ++e)
+                if (e < E) acc[e] = fmaf(xv, to_f32<T>(w[(int64_t)e * d + j]), acc[e]);
+        }
+        // butterfly: every lane ends with the full sums, in the same order
+#pragma unroll
+        for (int e = 0; e < kMaxExperts; ++e) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], o);
+        }
+        if (logits != nullptr && lane < E) {
+            float v = acc[0];
+#pragma unroll
+            for (int e = 1; e < kMaxExperts; ++e)
+                if (lane == e) v = acc[e];
+            logits[t * E + lane] = v;
+        }
+        if (lane == 0) {
+            // strict '>' keeps the lower index among equal scores
+            int a = 0;
+            float la = acc[0];
+#pragma unroll
+            for (int e = 1; e < kMaxExperts; ++e)
+                if (e < E && acc[e] > la) { la = acc[e]; a = e; }
+            int b = -1;
+            float lb = 0.f;
+#pragma unroll
+            for (int e = 0; e < kMaxExperts; ++e)
+                if (e < E && e != a && (b < 0 || acc[e] > lb)) { lb = acc[e]; b = e; }
+            // softmax over the two kept scores: weights 1/(1+r) and r/(1+r),
+            // r = exp(l_b - l_a) in (0, 1]
+            const float r = expf(lb - la);
+            const float inv = 1.0f / (1.0f + r);
+            topk_idx[2 * t] = a;
+            topk_idx[2 * t + 1] = b;
+            topk_w[2 * t] = inv;
+            topk_w[2 * t + 1] = r * inv;
+        }
+    }
+}
+
+}  // namespace moe

@@ -1,0 +1,226 @@
+"""Thin ctypes binding of libmoe.so (include/moe.h).
+
+Argument marshalling only: each function takes torch tensors that already live
+on the GPU, passes their device pointers and the current CUDA stream to the C
+ABI, and raises ``MoEError`` on a non-OK status. Every step of the layer runs in
+the library's CUDA kernels; there is no fallback of any kind. Importing this
+module fails loudly when the shared library is missing.
+"""
+from __future__ import annotations
+
+import ctypes
+import json
+from pathlib import Path
+
+import torch
+
+_LIB_PATH = Path(__file__).resolve().parent / "libmoe.so"
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = 1
+MOE_ERR_UNSUPPORTED = 2
+MOE_ERR_WORKSPACE = 3
+MOE_ERR_CUDA = 4
+MOE_ERR_TIMEOUT = 5
+MOE_ERR_DEVICE_CHECK = 6
+
+MOE_F32 = 0
+MOE_BF16 = 1
+
+MOE_KNOB_FFN_PATH = 1
+MOE_KNOB_KSLICE = 2
+MOE_KNOB_GRID = 3
+
+EXPORTED = (
+    "moe_version", "moe_status_string", "moe_workspace_bytes", "moe_ffn_workspace_bytes",
+    "moe_route_top2", "moe_permute", "moe_expert_ffn", "moe_combine", "moe_aux_stats",
+    "moe_layer_forward", "moe_get_device_status", "moe_set_wait_timeout_ns", "moe_set_knob",
+    "moe_timing_enable", "moe_timing_read",
+)
+
+
+class moe_shape(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int64), ("d", ctypes.c_int32), ("ffn", ctypes.c_int32),
+                ("E", ctypes.c_int32), ("k", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+
+
+class MoEError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        self.code = code
+        super().__init__(f"{fn} failed: {status_string(code)} ({code})")
+
+
+def _load() -> ctypes.CDLL:
+    if not _LIB_PATH.exists():
+        raise ImportError(
+            f"{_LIB_PATH} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'` "
+            "or `python sparse_mixture_experts_53_b300/build.py`")
+    lib = ctypes.CDLL(str(_LIB_PATH))
+    P = ctypes.c_void_p
+    S = ctypes.POINTER(moe_shape)
+    I = ctypes.c_int
+    sig = {
+        "moe_version": ([], ctypes.c_char_p),
+        "moe_status_string": ([I], ctypes.c_char_p),
+        "moe_workspace_bytes": ([S], ctypes.c_size_t),
+        "moe_ffn_workspace_bytes": ([S], ctypes.c_size_t),
+        "moe_route_top2": ([S, P, P, P, P, P, P], I),
+        "moe_permute": ([S, P, P, P, P, P, P, P, P, P, P], I),
+        "moe_expert_ffn": ([S, P, P, P, P, P, P, P, P, ctypes.c_size_t, P], I),
+        "moe_combine": ([S, P, P, P, P], I),
+        "moe_aux_stats": ([S, P, P, P, P, P, P], I),
+        "moe_layer_forward": ([S, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P], I),
+        "moe_get_device_status": ([ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)], I),
+        "moe_set_wait_timeout_ns": ([ctypes.c_uint64], I),
+        "moe_set_knob": ([ctypes.c_int32, ctypes.c_int64], I),
+        "moe_timing_enable": ([ctypes.c_int32], I),
+        "moe_timing_read": ([ctypes.c_char_p, ctypes.c_size_t], I),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    return lib
+
+
+lib = _load()
+
+
+def status_string(code: int) -> str:
+    return lib.moe_status_string(int(code)).decode()
+
+
+def _check(fn: str, code: int) -> None:
+    if code != MOE_OK:
+        raise MoEError(fn, code)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("expected a torch.Tensor")
+    if t.numel() and not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return ctypes.c_void_p(t.data_ptr()) if t.numel() else ctypes.c_void_p(0)
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return MOE_BF16
+    if t.dtype == torch.float32:
+        return MOE_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def make_shape(T: int, d: int, ffn: int, dtype: int, E: int = 8, k: int = 2) -> moe_shape:
+    return moe_shape(int(T), int(d), int(ffn), int(E), int(k), int(dtype))
+
+
+def shape_of(x: torch.Tensor, w1: torch.Tensor) -> moe_shape:
+    E, ffn, d = w1.shape
+    return make_shape(x.shape[0], d, ffn, dtype_code(x), E=E)
+
+
+def version() -> str:
+    return lib.moe_version().decode()
+
+
+def moe_workspace_bytes(shape: moe_shape) -> int:
+    return int(lib.moe_workspace_bytes(ctypes.byref(shape)))
+
+
+def moe_ffn_workspace_bytes(shape: moe_shape) -> int:
+    return int(lib.moe_ffn_workspace_bytes(ctypes.byref(shape)))
+
+
+def moe_route_top2(shape, x, w_gate, topk_idx, topk_w, logits=None, stream=None):
+    _check("moe_route_top2", lib.moe_route_top2(ctypes.byref(shape), _ptr(x), _ptr(w_gate), _ptr(topk_idx),
+                                                _ptr(topk_w), _ptr(logits), _stream(stream)))
+
+
+def moe_permute(shape, topk_idx, topk_w, x, counts, offsets, perm_token, slot_row, perm_w, x_perm, stream=None):
+    _check("moe_permute", lib.moe_permute(ctypes.byref(shape), _ptr(topk_idx), _ptr(topk_w), _ptr(x),
+                                          _ptr(counts), _ptr(offsets), _ptr(perm_token), _ptr(slot_row),
+                                          _ptr(perm_w), _ptr(x_perm), _stream(stream)))
+
+
+def moe_expert_ffn(shape, x_perm, offsets, perm_w, w1, w3, w2, y_slot, ws, stream=None):
+    _check("moe_expert_ffn", lib.moe_expert_ffn(ctypes.byref(shape), _ptr(x_perm), _ptr(offsets), _ptr(perm_w),
+                                                _ptr(w1), _ptr(w3), _ptr(w2), _ptr(y_slot), _ptr(ws),
+                                                ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def moe_combine(shape, y_slot, slot_row, y, stream=None):
+    _check("moe_combine", lib.moe_combine(ctypes.byref(shape), _ptr(y_slot), _ptr(slot_row), _ptr(y),
+                                          _stream(stream)))
+
+
+def moe_aux_stats(shape, logits, counts, f, P, l_aux, stream=None):
+    _check("moe_aux_stats", lib.moe_aux_stats(ctypes.byref(shape), _ptr(logits), _ptr(counts), _ptr(f), _ptr(P),
+                                              _ptr(l_aux), _stream(stream)))
+
+
+def moe_layer_forward(shape, x, w_gate, w1, w3, w2, y, ws, aux=None, stream=None):
+    """aux: None or a tuple of (f [E], P [E], l_aux [1]) float32 device tensors."""
+    f, P, l = aux if aux is not None else (None, None, None)
+    _check("moe_layer_forward", lib.moe_layer_forward(
+        ctypes.byref(shape), _ptr(x), _ptr(w_gate), _ptr(w1), _ptr(w3), _ptr(w2), _ptr(y), _ptr(f), _ptr(P),
+        _ptr(l), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def moe_get_device_status() -> tuple[int, int]:
+    code = ctypes.c_int32(0)
+    detail = ctypes.c_int32(0)
+    _check("moe_get_device_status", lib.moe_get_device_status(ctypes.byref(code), ctypes.byref(detail)))
+    return int(code.value), int(detail.value)
+
+
+def moe_set_wait_timeout_ns(ns: int) -> None:
+    _check("moe_set_wait_timeout_ns", lib.moe_set_wait_timeout_ns(int(ns)))
+
+
+def moe_set_knob(knob: int, value: int) -> None:
+    _check("moe_set_knob", lib.moe_set_knob(int(knob), int(value)))
+
+
+def moe_timing_enable(enable: bool) -> None:
+    _check("moe_timing_enable", lib.moe_timing_enable(1 if enable else 0))
+
+
+def moe_timing_read() -> dict:
+    buf = ctypes.create_string_buffer(1 << 16)
+    _check("moe_timing_read", lib.moe_timing_read(buf, len(buf)))
+    return json.loads(buf.value.decode() or "{}")
+
+
+# ------------------------------------------------------------------ helpers
+
+def workspace(shape: moe_shape, device="cuda", ffn_only: bool = False) -> torch.Tensor:
+    """A byte tensor of the size the ABI asks for (allocated by torch, not the library)."""
+    n = moe_ffn_workspace_bytes(shape) if ffn_only else moe_workspace_bytes(shape)
+    if n == 0 and shape.T > 0:
+        raise MoEError("workspace sizing", MOE_ERR_UNSUPPORTED)
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=device)
+
+
+def layer_forward(x, w_gate, w1, w3, w2, aux: bool = False, ws=None, out=None, stream=None):
+    """Allocates y (and the statistics) with torch and calls moe_layer_forward."""
+    shape = shape_of(x, w1)
+    if ws is None:
+        ws = workspace(shape, x.device)
+    y = out if out is not None else torch.empty_like(x)
+    stats = None
+    if aux:
+        E = w1.shape[0]
+        stats = (torch.empty(E, dtype=torch.float32, device=x.device),
+                 torch.empty(E, dtype=torch.float32, device=x.device),
+                 torch.empty(1, dtype=torch.float32, device=x.device))
+    moe_layer_forward(shape, x, w_gate, w1, w3, w2, y, ws, stats, stream)
+    return (y, stats) if aux else y

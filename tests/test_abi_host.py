@@ -1,0 +1,112 @@
+"""Host-side checks of the C ABI: exports and argument validation (no GPU work).
+
+Every check below returns before the library makes any CUDA call, so these run
+on a machine without a GPU.
+"""
+import ctypes
+import re
+from pathlib import Path
+
+import pytest
+import torch
+
+from sparse_mixture_experts_53_b300 import moe
+
+HEADER = Path(__file__).resolve().parent.parent / "include" / "moe.h"
+
+
+def declared_functions():
+    text = HEADER.read_text()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_function_is_exported():
+    names = declared_functions()
+    assert len(names) >= 15
+    for n in names:
+        assert hasattr(moe.lib, n), n
+    assert set(names) == set(moe.EXPORTED)
+
+
+def test_version_and_status_strings():
+    assert "sm_103a" in moe.version()
+    assert moe.status_string(moe.MOE_OK) == "ok"
+    assert moe.status_string(moe.MOE_ERR_TIMEOUT) == "device wait timed out"
+    assert moe.status_string(99) == "unknown status"
+
+
+def _shape(**kw):
+    base = dict(T=16, d=4096, ffn=14336, dtype=moe.MOE_BF16, E=8, k=2)
+    base.update(kw)
+    return moe.make_shape(base["T"], base["d"], base["ffn"], base["dtype"], E=base["E"], k=base["k"])
+
+
+FAKE = ctypes.c_void_p(1 << 20)        # aligned, never dereferenced
+MISALIGNED = ctypes.c_void_p((1 << 20) + 4)
+
+
+def _forward(shape, x=FAKE, ws_bytes=1 << 40, aux=(None, None, None)):
+    return moe.lib.moe_layer_forward(ctypes.byref(shape), x, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                     aux[0], aux[1], aux[2], FAKE, ws_bytes, None)
+
+
+def test_shape_validation_codes():
+    lib = moe.lib
+    assert lib.moe_route_top2(None, FAKE, FAKE, FAKE, FAKE, None, None) == moe.MOE_ERR_INVALID_ARG
+    assert _forward(_shape(E=4)) == moe.MOE_ERR_UNSUPPORTED
+    assert _forward(_shape(k=1)) == moe.MOE_ERR_UNSUPPORTED
+    assert _forward(_shape(d=100)) == moe.MOE_ERR_UNSUPPORTED          # bf16 needs d % 256 == 0
+    assert _forward(_shape(ffn=200)) == moe.MOE_ERR_UNSUPPORTED        # bf16 needs ffn % 128 == 0
+    assert _forward(_shape(T=-1)) == moe.MOE_ERR_INVALID_ARG
+    assert _forward(_shape(dtype=7)) == moe.MOE_ERR_INVALID_ARG
+    assert _forward(_shape(d=0)) == moe.MOE_ERR_INVALID_ARG
+
+
+def test_pointer_and_workspace_validation():
+    s = _shape()
+    assert _forward(s, x=None) == moe.MOE_ERR_INVALID_ARG
+    assert _forward(s, x=MISALIGNED) == moe.MOE_ERR_INVALID_ARG
+    assert _forward(s, ws_bytes=0) == moe.MOE_ERR_WORKSPACE
+    assert _forward(s, ws_bytes=moe.moe_workspace_bytes(s) - 1) == moe.MOE_ERR_WORKSPACE
+    # statistics pointers come all together or not at all
+    assert _forward(s, aux=(FAKE, None, None)) == moe.MOE_ERR_INVALID_ARG
+
+
+def test_empty_batch_is_a_no_op():
+    assert _forward(_shape(T=0), x=None, ws_bytes=0) == moe.MOE_OK
+
+
+def test_workspace_sizes():
+    s = _shape(T=16384)
+    n = moe.moe_workspace_bytes(s)
+    R = 2 * 16384
+    # x_perm (bf16) + hidden (bf16) + y_slot (fp32) dominate
+    assert n >= R * 4096 * 2 + R * 14336 * 2 + R * 4096 * 4
+    assert n < 1.01 * (R * 4096 * 2 + R * 14336 * 2 + R * 4096 * 4) + (1 << 22)
+    assert moe.moe_workspace_bytes(_shape(E=4)) == 0
+    assert moe.moe_ffn_workspace_bytes(_shape(T=16)) > 0
+    f = moe.make_shape(64, 128, 256, moe.MOE_F32)
+    assert moe.moe_workspace_bytes(f) > 0
+
+
+def test_knobs_and_timeouts():
+    lib = moe.lib
+    assert lib.moe_set_knob(99, 0) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_set_knob(moe.MOE_KNOB_FFN_PATH, 3) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_set_knob(moe.MOE_KNOB_KSLICE, 100) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_set_wait_timeout_ns(0) == moe.MOE_ERR_INVALID_ARG
+    try:
+        moe.moe_set_knob(moe.MOE_KNOB_FFN_PATH, 2)
+        # the weight-streaming path covers at most 64 tokens
+        assert moe.moe_workspace_bytes(_shape(T=65)) == 0
+        assert _forward(_shape(T=65)) == moe.MOE_ERR_UNSUPPORTED
+    finally:
+        moe.moe_set_knob(moe.MOE_KNOB_FFN_PATH, 0)
+    assert moe.moe_timing_read() == {}
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device error path")
+def test_device_status_without_a_device_reports_cuda_error():
+    code = ctypes.c_int32(0)
+    assert moe.lib.moe_get_device_status(ctypes.byref(code), None) == moe.MOE_ERR_CUDA
