@@ -43,8 +43,49 @@ def _peaks() -> dict:
     return dict(hbm_gbs=6400.0, bf16_tflops=1800.0, bf16_tflops_sustained=1400.0, source="fallback")
 
 
+class _Nvml:
+    """Minimal read-only NVML access through ctypes (libnvidia-ml ships with the driver)."""
+
+    def __init__(self):
+        import ctypes
+        self.c = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+        self._reasons = fn or self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def handle(self, cuda_index: int):
+        c = self.c
+        h = c.c_void_p()
+        try:
+            import torch
+            p = torch.cuda.get_device_properties(cuda_index)
+            bus = ("%08X:%02X:%02X.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)).encode()
+            if self.lib.nvmlDeviceGetHandleByPciBusId_v2(c.c_char_p(bus), c.byref(h)) == 0:
+                return h
+        except Exception:
+            pass
+        vis = [v for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip().isdigit()]
+        idx = int(vis[cuda_index]) if cuda_index < len(vis) else cuda_index
+        if self.lib.nvmlDeviceGetHandleByIndex_v2(c.c_uint(idx), c.byref(h)) != 0:
+            raise RuntimeError("no NVML handle")
+        return h
+
+    def sm_clock(self, h, max_clock=False) -> int:
+        v = self.c.c_uint(0)
+        f = self.lib.nvmlDeviceGetMaxClockInfo if max_clock else self.lib.nvmlDeviceGetClockInfo
+        f(h, self.c.c_int(1), self.c.byref(v))  # NVML_CLOCK_SM = 1
+        return int(v.value)
+
+    def reasons(self, h) -> int:
+        v = self.c.c_ulonglong(0)
+        self._reasons(h, self.c.byref(v))
+        return int(v.value)
+
+
 class ClockSampler:
-    """Samples SM clock and throttle reasons with NVML while the timed region runs."""
+    """Samples SM clock and clock-event reasons (NVML, read-only) during the timed region."""
 
     REASONS = {
         0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
@@ -52,42 +93,26 @@ class ClockSampler:
         0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting",
     }
 
-    def __init__(self, index: int, period_s: float = 0.02):
-        self.index, self.period = index, period_s
+    def __init__(self, cuda_index: int, period_s: float = 0.002):
+        self.period = period_s
         self.samples, self.reasons = [], set()
         self.max_mhz = None
         self._stop = threading.Event()
         self._thread = None
         self.ok = False
         try:
-            import pynvml
-            pynvml.nvmlInit()
-            self.nvml = pynvml
-            self.h = self._handle(pynvml, index)
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+            self.nvml = _Nvml()
+            self.h = self.nvml.handle(cuda_index)
+            self.max_mhz = self.nvml.sm_clock(self.h, max_clock=True)
             self.ok = True
         except Exception as exc:  # pragma: no cover - reported in the JSON line
             self.error = repr(exc)
 
-    @staticmethod
-    def _handle(pynvml, index):
-        """NVML handle of the CUDA device `index` (NVML counts all GPUs, CUDA only the visible ones)."""
-        try:
-            import torch
-            p = torch.cuda.get_device_properties(index)
-            bus = "%08X:%02X:%02X.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
-            return pynvml.nvmlDeviceGetHandleByPciBusId(bus.encode())
-        except Exception:
-            pass
-        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
-        ids = [v for v in vis.split(",") if v.strip().isdigit()]
-        return pynvml.nvmlDeviceGetHandleByIndex(int(ids[index]) if index < len(ids) else index)
-
     def _run(self):
         while not self._stop.is_set():
             try:
-                self.samples.append(self.nvml.nvmlDeviceGetClockInfo(self.h, self.nvml.NVML_CLOCK_SM))
-                mask = self.nvml.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+                self.samples.append(self.nvml.sm_clock(self.h))
+                mask = self.nvml.reasons(self.h)
                 for bit, name in self.REASONS.items():
                     if mask & bit:
                         self.reasons.add(name)
@@ -113,10 +138,14 @@ class ClockSampler:
                 "reasons": sorted(self.reasons - {"gpu_idle"}), "samples": len(self.samples)}
 
 
+KERNEL_SOURCES = ("ffn_tc.cuh", "common.cuh")
+
+
 def _source_digest() -> str:
+    """Digest of the files that define the tensor-core kernels (ncu figures go stale when they change)."""
     h = hashlib.sha256()
-    for p in sorted((ROOT / "sparse_mixture_experts_53_b300" / "csrc").glob("*")):
-        h.update(p.read_bytes())
+    for name in KERNEL_SOURCES:
+        h.update((ROOT / "sparse_mixture_experts_53_b300" / "csrc" / name).read_bytes())
     return h.hexdigest()[:16]
 
 

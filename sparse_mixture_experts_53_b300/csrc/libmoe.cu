@@ -25,6 +25,7 @@ namespace {
 constexpr int kMaxDevices = 64;
 constexpr size_t kAlign = 1024;
 constexpr int kStreamMaxTokens = 64;     // weight-streaming path needs T <= 64
+constexpr int64_t kRouterSplitMaxTokens = 256;  // one CTA per token below this
 constexpr size_t kSmemBudget = 225 * 1024;
 
 struct TimingRecord {
@@ -247,6 +248,20 @@ moe_status run_router(const moe_shape& s, const void* x, const void* wg, int32_t
     const int64_t blocks = (s.T + kRouterWarps - 1) / kRouterWarps;
     const int grid = (int)std::min<int64_t>(blocks, (int64_t)sm_count() * 4);
     const size_t smem = use_smem ? wbytes : 0;
+    if (vec && s.T <= kRouterSplitMaxTokens) {
+        // small batch: one CTA per token, the model dimension split over 8 warps
+        const int sgrid = (int)s.T;
+        if (s.dtype == MOE_BF16)
+            return launch("router_top2", st, [&] {
+                router_top2_split_kernel<__nv_bfloat16><<<sgrid, kRouterWarps * 32, 0, st>>>(
+                    static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(wg), s.T, s.d, s.E, idx,
+                    w, logits);
+            });
+        return launch("router_top2", st, [&] {
+            router_top2_split_kernel<float><<<sgrid, kRouterWarps * 32, 0, st>>>(
+                static_cast<const float*>(x), static_cast<const float*>(wg), s.T, s.d, s.E, idx, w, logits);
+        });
+    }
     if (s.dtype == MOE_BF16) {
         if (!ensure_smem(router_top2_kernel<__nv_bfloat16>, 0, 200 * 1024)) return MOE_ERR_CUDA;
         return launch("router_top2", st, [&] {

@@ -44,6 +44,27 @@ __device__ __forceinline__ void load_vec(const T* p, float (&v)[Vec16<T>::N]) {
     }
 }
 
+// Top-2 selection and the two-way softmax from the E scores of one token.
+__device__ __forceinline__ void top2_softmax(const float (&acc)[kMaxExperts], int E, int32_t* idx, float* w) {
+    // strict '>' keeps the lower index among equal scores
+    int a = 0;
+    float la = acc[0];
+#pragma unroll
+    for (int e = 1; e < kMaxExperts; ++e)
+        if (e < E && acc[e] > la) { la = acc[e]; a = e; }
+    int b = -1;
+    float lb = 0.f;
+#pragma unroll
+    for (int e = 0; e < kMaxExperts; ++e)
+        if (e < E && e != a && (b < 0 || acc[e] > lb)) { lb = acc[e]; b = e; }
+    const float r = expf(lb - la);
+    const float inv = 1.0f / (1.0f + r);
+    idx[0] = a;
+    idx[1] = b;
+    w[0] = inv;
+    w[1] = r * inv;
+}
+
 // use_smem: W_g is copied to shared memory (E * d * sizeof(T) bytes of
 // dynamic shared memory); otherwise it is read through L1/L2.
 // vec: rows are 16-byte aligned and d is a multiple of the vector width.
@@ -115,27 +136,71 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
                 if (lane == e) v = acc[e];
             logits[t * E + lane] = v;
         }
-        if (lane == 0) {
-            // strict '>' keeps the lower index among equal scores
-            int a = 0;
-            float la = acc[0];
+        if (lane == 0) top2_softmax(acc, E, topk_idx + 2 * t, topk_w + 2 * t);
+    }
+}
+
+// Small batches: one CTA per token, the d products split over 8 warps. Each
+// lane sums its own chunks in order, a butterfly adds the lanes, and warp 0
+// adds the 8 warp totals in warp order, so the result is deterministic and the
+// longest chain of additions is d/256 + 13 terms. W_g is read through L1/L2
+// (64 KB), so no CTA waits for a whole copy of it.
+template <typename T>
+__global__ void __launch_bounds__(kRouterWarps * 32)
+    router_top2_split_kernel(const T* __restrict__ x, const T* __restrict__ wg, int64_t T_tokens, int d, int E,
+                             int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, float* __restrict__ logits) {
+    __shared__ float part[kRouterWarps][kMaxExperts];
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    constexpr int V = Vec16<T>::N;
+    const int nchunks = d / V;  // d % V == 0 and 16-byte rows (checked on the host)
+    for (int64_t t = blockIdx.x; t < T_tokens; t += gridDim.x) {
+        const T* xr = x + t * d;
+        float acc[kMaxExperts];
 #pragma unroll
-            for (int e = 1; e < kMaxExperts; ++e)
-                if (e < E && acc[e] > la) { la = acc[e]; a = e; }
-            int b = -1;
-            float lb = 0.f;
+        for (int e = 0; e < kMaxExperts; ++e) acc[e] = 0.f;
+        for (int c = warp * 32 + lane; c < nchunks; c += kRouterWarps * 32) {
+            float xv[V];
+            load_vec<T>(xr + c * V, xv);
 #pragma unroll
-            for (int e = 0; e < kMaxExperts; ++e)
-                if (e < E && e != a && (b < 0 || acc[e] > lb)) { lb = acc[e]; b = e; }
-            // softmax over the two kept scores: weights 1/(1+r) and r/(1+r),
-            // r = exp(l_b - l_a) in (0, 1]
-            const float r = expf(lb - la);
-            const float inv = 1.0f / (1.0f + r);
-            topk_idx[2 * t] = a;
-            topk_idx[2 * t + 1] = b;
-            topk_w[2 * t] = inv;
-            topk_w[2 * t + 1] = r * inv;
+            for (int e = 0; e < kMaxExperts; ++e) {
+                if (e < E) {
+                    float wv[V];
+                    load_vec<T>(wg + (int64_t)e * d + c * V, wv);
+#pragma unroll
+                    for (int i = 0; i < V; ++i) acc[e] = fmaf(xv[i], wv[i], acc[e]);
+                }
+            }
         }
+#pragma unroll
+        for (int e = 0; e < kMaxExperts; ++e) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], o);
+        }
+        if (lane == 0) {
+#pragma unroll
+            for (int e = 0; e < kMaxExperts; ++e) part[warp][e] = acc[e];
+        }
+        __syncthreads();
+        if (warp == 0) {
+            float tot[kMaxExperts];
+#pragma unroll
+            for (int e = 0; e < kMaxExperts; ++e) {
+                float v = part[0][e];
+#pragma unroll
+                for (int q = 1; q < kRouterWarps; ++q) v += part[q][e];
+                tot[e] = v;
+            }
+            if (logits != nullptr && lane < E) {
+                float v = tot[0];
+#pragma unroll
+                for (int e = 1; e < kMaxExperts; ++e)
+                    if (lane == e) v = tot[e];
+                logits[t * E + lane] = v;
+            }
+            if (lane == 0) top2_softmax(tot, E, topk_idx + 2 * t, topk_w + 2 * t);
+        }
+        __syncthreads();
     }
 }
 
