@@ -155,6 +155,29 @@ moe_status moe_layer_forward(const moe_shape* s, const void* x, const void* w_ga
                              float* aux_f, float* aux_P, float* aux_l_aux,
                              void* ws, size_t ws_bytes, void* stream);
 
+/* The whole layer without any caller-provided workspace and without any
+ * device allocation (the pages have no counterpart: this is a library
+ * convenience). It is for callers that cannot call cudaMalloc at the point
+ * where they run the layer: for example a plugin inside a host application
+ * that reserves all device memory through its own pool, or a latency-critical
+ * serving loop that must not call cudaMalloc because an allocation can
+ * synchronise the device.
+ *   Same arguments and results as moe_layer_forward without statistics; the
+ *   caller still passes x, the weights and y (device memory).
+ *   Intermediates live in one 24 MiB array of static device memory inside the
+ *   library; every GPU that loads the library holds it until the process
+ *   exits. A shape whose moe_workspace_bytes() exceeds 24 MiB (25165824 bytes)
+ *   is rejected with MOE_ERR_WORKSPACE before anything is enqueued; the
+ *   Mixtral decode batch (bf16, d = 4096, ffn = 14336, T <= 16) fits.
+ *   The first call on each device looks up the array's device address with
+ *   that device current; make that first call before any stream capture.
+ *   All calls share the one array and it keeps the previous call's contents
+ *   (no part of it needs to start at zero). Calls whose work overlaps on the
+ *   GPU (other streams, other host threads) race on it: serialise them. */
+moe_status moe_layer_forward_noalloc(const moe_shape* s, const void* x, const void* w_gate,
+                                     const void* w1, const void* w3, const void* w2, void* y,
+                                     void* stream);
+
 /* Synchronises the current device, then reports and clears its status word.
  * *code receives MOE_OK or the first device-side error since the last read;
  * *detail (nullable) receives a kernel/where code for diagnostics. Returns

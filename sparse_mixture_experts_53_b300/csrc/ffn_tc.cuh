@@ -153,7 +153,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t tmem_base = ctl->tmem_base;
     const int n_work = ctl->n_work;
     const int E = args.E;
-    const int ntn = args.n_tiles_n;
     const int KB = args.K / kBK;
 
     auto decode = [&](int tile, int& e, int& nt, int& mt) {

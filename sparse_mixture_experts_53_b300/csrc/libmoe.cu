@@ -413,6 +413,26 @@ moe_status run_aux(const moe_shape& s, const float* logits, const int32_t* count
     });
 }
 
+// Scratch of moe_layer_forward_noalloc: a fixed array of static device memory,
+// one copy per device that loads the library, held until the process exits.
+constexpr size_t kNoAllocScratchBytes = size_t(24) << 20;
+__device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of the scratch array on the current device. The array's name
+// is only a host-side stand-in in host code, so its address is looked up once
+// per device (with that device current) and cached.
+void* noalloc_scratch() {
+    static void* addr[kMaxDevices] = {nullptr};
+    const int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices) return nullptr;
+    if (addr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+        addr[dev] = p;
+    }
+    return addr[dev];
+}
+
 }  // namespace
 }  // namespace moe
 
@@ -528,6 +548,18 @@ moe_status moe_layer_forward(const moe_shape* s, const void* x, const void* w_ga
     MOE_TRY(run_combine(*s, y_slot, slot_row, y, st));
     if (aux) MOE_TRY(run_aux(*s, logits, counts, aux_f, aux_P, aux_l_aux, st));
     return MOE_OK;
+}
+
+moe_status moe_layer_forward_noalloc(const moe_shape* s, const void* x, const void* w_gate, const void* w1,
+                                     const void* w3, const void* w2, void* y, void* stream) {
+    MOE_TRY(check_shape(s));
+    if (s->T == 0) return MOE_OK;
+    if (s->dtype == MOE_BF16 && choose_path(*s) == 0) return MOE_ERR_UNSUPPORTED;
+    if (fwd_layout(*s).total > kNoAllocScratchBytes) return MOE_ERR_WORKSPACE;
+    void* scratch = noalloc_scratch();
+    if (scratch == nullptr) return MOE_ERR_CUDA;
+    return moe_layer_forward(s, x, w_gate, w1, w3, w2, y, nullptr, nullptr, nullptr, scratch, kNoAllocScratchBytes,
+                             stream);
 }
 
 moe_status moe_get_device_status(int32_t* code, int32_t* detail) {

@@ -34,7 +34,7 @@ MOE_KNOB_GRID = 3
 EXPORTED = (
     "moe_version", "moe_status_string", "moe_workspace_bytes", "moe_ffn_workspace_bytes",
     "moe_route_top2", "moe_permute", "moe_expert_ffn", "moe_combine", "moe_aux_stats",
-    "moe_layer_forward", "moe_get_device_status", "moe_set_wait_timeout_ns", "moe_set_knob",
+    "moe_layer_forward", "moe_layer_forward_noalloc", "moe_get_device_status", "moe_set_wait_timeout_ns", "moe_set_knob",
     "moe_timing_enable", "moe_timing_read",
 )
 
@@ -70,6 +70,7 @@ def _load() -> ctypes.CDLL:
         "moe_combine": ([S, P, P, P, P], I),
         "moe_aux_stats": ([S, P, P, P, P, P, P], I),
         "moe_layer_forward": ([S, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P], I),
+        "moe_layer_forward_noalloc": ([S, P, P, P, P, P, P, P], I),
         "moe_get_device_status": ([ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)], I),
         "moe_set_wait_timeout_ns": ([ctypes.c_uint64], I),
         "moe_set_knob": ([ctypes.c_int32, ctypes.c_int64], I),
@@ -173,6 +174,12 @@ def moe_layer_forward(shape, x, w_gate, w1, w3, w2, y, ws, aux=None, stream=None
     _check("moe_layer_forward", lib.moe_layer_forward(
         ctypes.byref(shape), _ptr(x), _ptr(w_gate), _ptr(w1), _ptr(w3), _ptr(w2), _ptr(y), _ptr(f), _ptr(P),
         _ptr(l), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def moe_layer_forward_noalloc(shape, x, w_gate, w1, w3, w2, y, stream=None):
+    """moe_layer_forward on the library's fixed static scratch (no workspace, no allocation)."""
+    _check("moe_layer_forward_noalloc", lib.moe_layer_forward_noalloc(
+        ctypes.byref(shape), _ptr(x), _ptr(w_gate), _ptr(w1), _ptr(w3), _ptr(w2), _ptr(y), _stream(stream)))
 
 
 def moe_get_device_status() -> tuple[int, int]:
