@@ -189,6 +189,7 @@ def run_ours(args, rank, world, local) -> dict | None:
     from sparse_mixture_experts_53_b300 import moe
 
     torch.cuda.set_device(local)
+    moe.moe_set_knob(moe.MOE_KNOB_PDL, args.pdl)
     dist = None
     if world > 1:
         import torch.distributed as dist
@@ -308,6 +309,7 @@ def run_ours(args, rank, world, local) -> dict | None:
         "config": {"workload": cfg["name"], "T": cfg["T"], "d": cfg["d"], "ffn": cfg["ffn"], "E": cfg["E"], "k": 2,
                    "aux_stats": aux, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "ffn_path": "weight-streaming (swap-AB)" if streaming else "token tiles 128x256",
+                   "pdl": bool(args.pdl),
                    "l2": "inputs larger than L2: each step reads %.2f GB of expert weights" % (work["weight_bytes"] / 1e9),
                    "experts_touched": work["touched"], "input_gen_s": round(gen_s, 1)},
         "step": {"tflops": round(work["flops"] / step_s / 1e12, 2),
@@ -394,6 +396,8 @@ def main():
     ap.add_argument("--config", type=int, default=DEFAULT_CONFIG, choices=[1, 2, 3, 4])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--pdl", type=int, default=1, choices=[0, 1],
+                    help="programmatic dependent launch between the library's kernels")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

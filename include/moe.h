@@ -197,8 +197,12 @@ moe_status moe_set_wait_timeout_ns(uint64_t ns);
  *                       0 = automatic)
  *   MOE_KNOB_GRID       CTAs of the persistent tensor-core kernels (0 = one
  *                       per SM)
+ *   MOE_KNOB_PDL        1 (default) = launch each kernel with programmatic
+ *                       dependent launch, so it starts while its predecessor
+ *                       drains (it still waits for the predecessor's results
+ *                       before touching memory); 0 = plain serialised launches
  * Returns MOE_ERR_INVALID_ARG for an unknown knob or value. */
-enum { MOE_KNOB_FFN_PATH = 1, MOE_KNOB_KSLICE = 2, MOE_KNOB_GRID = 3 };
+enum { MOE_KNOB_FFN_PATH = 1, MOE_KNOB_KSLICE = 2, MOE_KNOB_GRID = 3, MOE_KNOB_PDL = 4 };
 moe_status moe_set_knob(int32_t knob, int64_t value);
 
 /* Per-kernel timing with CUDA events recorded on the launching stream.

@@ -39,6 +39,8 @@ __global__ void __launch_bounds__(256)
     __shared__ float sx[kF32Tile][kF32Tile + 1];
     __shared__ float sa[kF32Tile][kF32Tile + 1];
     __shared__ float sb[kF32Tile][kF32Tile + 1];
+    pdl_trigger();
+    pdl_wait();
     int e, r0, r1;
     if (!f32_find_tile(offsets, E, blockIdx.y, e, r0, r1)) return;
     const int tx = threadIdx.x, ty = threadIdx.y;
@@ -84,6 +86,8 @@ template <typename T>
 __global__ void __launch_bounds__(256)
     combine_kernel(const float* __restrict__ y_slot, const int32_t* __restrict__ slot_row, int64_t T_tokens,
                    int d, T* __restrict__ y) {
+    pdl_trigger();
+    pdl_wait();
     const int64_t n = T_tokens * d;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t t = i / d;
@@ -102,6 +106,8 @@ template <typename T>
 __global__ void __launch_bounds__(256)
     combine4_kernel(const float* __restrict__ y_slot, const int32_t* __restrict__ slot_row, int64_t T_tokens,
                     int d, T* __restrict__ y) {
+    pdl_trigger();
+    pdl_wait();
     const int d4 = d / 4;
     const int64_t n = T_tokens * d4;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
@@ -129,6 +135,8 @@ __global__ void __launch_bounds__(kAuxThreads)
     aux_stats_kernel(const float* __restrict__ logits, const int32_t* __restrict__ counts, int64_t T_tokens,
                      int E, float* __restrict__ f, float* __restrict__ P, float* __restrict__ l_aux) {
     __shared__ float red[kAuxThreads / 32][kMaxExperts];
+    pdl_trigger();
+    pdl_wait();
     float acc[kMaxExperts];
 #pragma unroll
     for (int e = 0; e < kMaxExperts; ++e) acc[e] = 0.f;

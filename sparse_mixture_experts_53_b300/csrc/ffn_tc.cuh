@@ -125,6 +125,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         mbar_init(smem_u32(&ctl->drain), 1);
         ctl->abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&map_a);
+        tma_prefetch_desc(&map_b0);
+        if (UP) tma_prefetch_desc(&map_b1);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&ctl->tmem_base), 2 * kTileAccCols);
+        tmem_relinquish();
+    }
+    pdl_trigger();
+    pdl_wait();
+    if (threadIdx.x == 0) {
         int tiles = 0;
         for (int e = 0; e <= args.E; ++e) ctl->off[e] = args.offsets[e];
         for (int e = 0; e < args.E; ++e) {
@@ -136,16 +150,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         ctl->base[args.E] = tiles;
         ctl->n_work = tiles;
-        fence_mbar_init();
-    }
-    if (warp == 0 && lane == 0) {
-        tma_prefetch_desc(&map_a);
-        tma_prefetch_desc(&map_b0);
-        if (UP) tma_prefetch_desc(&map_b1);
-    }
-    if (warp == 1) {
-        tmem_alloc(smem_u32(&ctl->tmem_base), 2 * kTileAccCols);
-        tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
@@ -166,8 +170,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
+            // activations are re-read for every column tile: keep them; a
+            // weight tile is shared by the CTAs working on the expert's row
+            // tiles at the same time: normal priority
             const uint64_t pol_act = policy_evict_last();
-            const uint64_t pol_w = policy_evict_first();
+            const uint64_t pol_w = policy_evict_normal();
             uint32_t s = 0, ph = 0;
             uint32_t issued_mask = 0, issued_ph = 0;
             bool ok = true;
@@ -369,6 +376,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         mbar_init(smem_u32(&ctl->drain), 1);
         ctl->abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&map_w0);
+        if (UP) tma_prefetch_desc(&map_w1);
+        tma_prefetch_desc(&map_x);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&ctl->tmem_base), kStreamAcc * kStreamMaxNB);
+        tmem_relinquish();
+    }
+    pdl_trigger();
+    pdl_wait();
+    if (threadIdx.x == 0) {
         int n_act = 0;
         for (int e = 0; e <= args.E; ++e) ctl->off[e] = args.offsets[e];
         bool too_many = false;
@@ -384,16 +405,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         ctl->n_act = n_act;
         ctl->n_work = n_act * units_per_expert;
-        fence_mbar_init();
-    }
-    if (warp == 0 && lane == 0) {
-        tma_prefetch_desc(&map_w0);
-        if (UP) tma_prefetch_desc(&map_w1);
-        tma_prefetch_desc(&map_x);
-    }
-    if (warp == 1) {
-        tmem_alloc(smem_u32(&ctl->tmem_base), kStreamAcc * kStreamMaxNB);
-        tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
@@ -535,6 +546,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 __global__ void __launch_bounds__(256)
     reduce_swiglu_kernel(const float* __restrict__ part, int S, int64_t R, int F,
                          __nv_bfloat16* __restrict__ H) {
+    pdl_trigger();
+    pdl_wait();
     const int64_t n = R * F;
     const int64_t plane = R * F;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
@@ -551,11 +564,47 @@ __global__ void __launch_bounds__(256)
 __global__ void __launch_bounds__(256)
     reduce_down_kernel(const float* __restrict__ part, int S, int64_t R, int d,
                        const float* __restrict__ perm_w, float* __restrict__ y_slot) {
+    pdl_trigger();
+    pdl_wait();
     const int64_t n = R * d;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
         float acc = 0.f;
         for (int s = 0; s < S; ++s) acc += part[(int64_t)s * n + i];
         y_slot[i] = perm_w[i / d] * acc;
+    }
+}
+
+// Weight-streaming path of the whole layer: the K-slice sum, the gate scale and
+// the two-slot combine in one pass,
+//   y[t] = (perm_w[r0] * sum_s P_s[r0]) + (perm_w[r1] * sum_s P_s[r1]),
+// with the same operations in the same order as reduce_down_kernel followed
+// by the combine, so both routes give bit-identical y.
+template <typename T>
+__global__ void __launch_bounds__(256)
+    reduce_combine_kernel(const float* __restrict__ part, int S, int64_t R, int d, const float* __restrict__ perm_w,
+                          const int32_t* __restrict__ slot_row, int64_t T_tokens, T* __restrict__ y) {
+    pdl_trigger();
+    pdl_wait();
+    const int64_t n = T_tokens * d;
+    const int64_t plane = R * d;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t t = i / d;
+        const int64_t c = i - t * d;
+        float ab[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int r = slot_row[2 * t + j];
+            float v = 0.f;
+            if (r >= 0) {
+                float acc = 0.f;
+                for (int s = 0; s < S; ++s) acc += part[(int64_t)s * plane + (int64_t)r * d + c];
+                v = perm_w[r] * acc;
+            }
+            ab[j] = v;
+        }
+        const float sum = ab[0] + ab[1];
+        if constexpr (sizeof(T) == 2) y[i] = __float2bfloat16_rn(sum);
+        else y[i] = sum;
     }
 }
 

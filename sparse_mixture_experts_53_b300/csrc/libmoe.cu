@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <utility>
 #include <cstdio>
 #include <cstring>
 #include <map>
@@ -26,6 +27,7 @@ constexpr int kMaxDevices = 64;
 constexpr size_t kAlign = 1024;
 constexpr int kStreamMaxTokens = 64;     // weight-streaming path needs T <= 64
 constexpr int64_t kRouterSplitMaxTokens = 256;  // one CTA per token below this
+constexpr int64_t kFusedGatherBytes = 512 * 1024;  // the permutation CTA gathers x_perm below this
 constexpr size_t kSmemBudget = 225 * 1024;
 
 struct TimingRecord {
@@ -39,6 +41,7 @@ struct HostState {
     int grid = 0;              // 0 = one CTA per SM
     uint64_t timeout_ns = 2000000000ull;
     bool timing = false;
+    bool pdl = true;           // programmatic dependent launch between the library's kernels
     std::vector<TimingRecord> records;
     std::vector<cudaEvent_t> pool;
     int sms[kMaxDevices] = {0};
@@ -89,6 +92,25 @@ cudaEvent_t take_event() {
     return e;
 }
 
+// Launches a kernel with programmatic dependent launch allowed (unless the
+// knob turned it off): the kernel may start while its predecessor in the
+// stream drains, and waits inside (griddepcontrol.wait) before touching memory.
+template <typename... KArgs, typename... Args>
+cudaError_t klaunch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                    Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = g.pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 template <typename F>
 moe_status launch(const char* name, cudaStream_t st, F&& f) {
     cudaEvent_t a = nullptr, b = nullptr;
@@ -97,8 +119,8 @@ moe_status launch(const char* name, cudaStream_t st, F&& f) {
         b = take_event();
         cudaEventRecord(a, st);
     }
-    f();
-    const cudaError_t err = cudaGetLastError();
+    const cudaError_t lerr = f();
+    const cudaError_t err = lerr != cudaSuccess ? lerr : cudaGetLastError();
     if (g.timing) {
         cudaEventRecord(b, st);
         g.records.push_back({name, a, b});
@@ -253,26 +275,26 @@ moe_status run_router(const moe_shape& s, const void* x, const void* wg, int32_t
         const int sgrid = (int)s.T;
         if (s.dtype == MOE_BF16)
             return launch("router_top2", st, [&] {
-                router_top2_split_kernel<__nv_bfloat16><<<sgrid, kRouterWarps * 32, 0, st>>>(
+                return klaunch(router_top2_split_kernel<__nv_bfloat16>, sgrid, kRouterWarps * 32, 0, st, 
                     static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(wg), s.T, s.d, s.E, idx,
                     w, logits);
             });
         return launch("router_top2", st, [&] {
-            router_top2_split_kernel<float><<<sgrid, kRouterWarps * 32, 0, st>>>(
+            return klaunch(router_top2_split_kernel<float>, sgrid, kRouterWarps * 32, 0, st, 
                 static_cast<const float*>(x), static_cast<const float*>(wg), s.T, s.d, s.E, idx, w, logits);
         });
     }
     if (s.dtype == MOE_BF16) {
         if (!ensure_smem(router_top2_kernel<__nv_bfloat16>, 0, 200 * 1024)) return MOE_ERR_CUDA;
         return launch("router_top2", st, [&] {
-            router_top2_kernel<__nv_bfloat16><<<grid, kRouterWarps * 32, smem, st>>>(
+            return klaunch(router_top2_kernel<__nv_bfloat16>, grid, kRouterWarps * 32, smem, st, 
                 static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(wg), s.T, s.d, s.E,
                 use_smem, vec, idx, w, logits);
         });
     }
     if (!ensure_smem(router_top2_kernel<float>, 1, 200 * 1024)) return MOE_ERR_CUDA;
     return launch("router_top2", st, [&] {
-        router_top2_kernel<float><<<grid, kRouterWarps * 32, smem, st>>>(
+        return klaunch(router_top2_kernel<float>, grid, kRouterWarps * 32, smem, st, 
             static_cast<const float*>(x), static_cast<const float*>(wg), s.T, s.d, s.E, use_smem, vec, idx, w,
             logits);
     });
@@ -281,16 +303,21 @@ moe_status run_router(const moe_shape& s, const void* x, const void* wg, int32_t
 moe_status run_permute(const moe_shape& s, const int32_t* idx, const float* w, const void* x, int32_t* counts,
                        int32_t* offsets, int32_t* perm_token, int32_t* slot_row, float* perm_w, void* x_perm,
                        cudaStream_t st) {
-    MOE_TRY(launch("permute", st, [&] {
-        permute_kernel<<<1, kPermuteThreads, 0, st>>>(idx, w, s.T, s.E, counts, offsets, perm_token, slot_row,
-                                                      perm_w);
-    }));
-    if (s.T == 0) return MOE_OK;
     const int64_t R = 2 * s.T;
+    const int64_t row_bytes = (int64_t)s.d * esize(s);
+    // small batches: the permutation CTA also copies the rows (one launch less)
+    const bool fused = s.T > 0 && row_bytes % 16 == 0 && R * row_bytes <= kFusedGatherBytes &&
+                       aligned16(x) && aligned16(x_perm);
+    MOE_TRY(launch("permute", st, [&] {
+        return klaunch(permute_kernel, 1, kPermuteThreads, 0, st, idx, w, s.T, s.E, counts, offsets, perm_token,
+                       slot_row, perm_w, fused ? static_cast<const unsigned char*>(x) : nullptr, row_bytes,
+                       static_cast<unsigned char*>(x_perm));
+    }));
+    if (s.T == 0 || fused) return MOE_OK;
     const int grid = (int)std::min<int64_t>(R, (int64_t)sm_count() * 8);
     return launch("gather_rows", st, [&] {
-        gather_rows_kernel<<<grid, 256, 0, st>>>(static_cast<const unsigned char*>(x), perm_token, offsets, s.E, R,
-                                                  (int64_t)s.d * esize(s), static_cast<unsigned char*>(x_perm));
+        return klaunch(gather_rows_kernel, grid, 256, 0, st, static_cast<const unsigned char*>(x), perm_token,
+                       offsets, s.E, R, row_bytes, static_cast<unsigned char*>(x_perm));
     });
 }
 
@@ -299,9 +326,13 @@ int tc_grid(int64_t work_upper) {
     return (int)std::max<int64_t>(1, std::min<int64_t>(work_upper, sms));
 }
 
+// With slot_row and y given (the whole-layer call), the weight-streaming path
+// finishes with the fused K-slice sum + gate scale + combine and sets
+// *combined; otherwise it writes y_slot.
 moe_status run_ffn(const moe_shape& s, const void* x_perm, const int32_t* offsets, const float* perm_w,
                    const void* w1, const void* w3, const void* w2, float* y_slot, unsigned char* ws,
-                   const FfnLayout& L, cudaStream_t st) {
+                   const FfnLayout& L, cudaStream_t st, const int32_t* slot_row = nullptr, void* y = nullptr,
+                   bool* combined = nullptr) {
     if (s.T == 0) return MOE_OK;
     const int64_t R = 2 * s.T;
     const int d = s.d, F = s.ffn, E = s.E;
@@ -309,12 +340,12 @@ moe_status run_ffn(const moe_shape& s, const void* x_perm, const int32_t* offset
         float* H = reinterpret_cast<float*>(ws + L.h);
         const int gy = (int)((R + kF32Tile - 1) / kF32Tile + E);
         MOE_TRY(launch("f32_up", st, [&] {
-            f32_ffn_kernel<true><<<dim3((F + kF32Tile - 1) / kF32Tile, gy), dim3(32, 8), 0, st>>>(
+            return klaunch(f32_ffn_kernel<true>, dim3((F + kF32Tile - 1) / kF32Tile, gy), dim3(32, 8), 0, st, 
                 static_cast<const float*>(x_perm), offsets, E, static_cast<const float*>(w1),
                 static_cast<const float*>(w3), nullptr, d, F, H);
         }));
         return launch("f32_down", st, [&] {
-            f32_ffn_kernel<false><<<dim3((d + kF32Tile - 1) / kF32Tile, gy), dim3(32, 8), 0, st>>>(
+            return klaunch(f32_ffn_kernel<false>, dim3((d + kF32Tile - 1) / kF32Tile, gy), dim3(32, 8), 0, st, 
                 H, offsets, E, static_cast<const float*>(w2), nullptr, perm_w, F, d, y_slot);
         });
     }
@@ -328,7 +359,7 @@ moe_status run_ffn(const moe_shape& s, const void* x_perm, const int32_t* offset
         TileArgs up{offsets, perm_w, H, E, d, F / kTileM, F, F, g.timeout_ns};
         const int64_t tiles_up = ((R + kTileM - 1) / kTileM + E) * (F / kTileM);
         MOE_TRY(launch("tile_up_swiglu", st, [&] {
-            tile_gemm_kernel<true><<<tc_grid(tiles_up), kTcThreads, kTileSmemBytes, st>>>(ma, mb0, mb1, up);
+            return klaunch(tile_gemm_kernel<true>, tc_grid(tiles_up), kTcThreads, kTileSmemBytes, st, ma, mb0, mb1, up);
         }));
         CUtensorMap mh, mw2;
         if (!make_map(&mh, H, F, R, kTileM) || !make_map(&mw2, w2, F, (uint64_t)E * d, kTileN)) return MOE_ERR_CUDA;
@@ -336,7 +367,7 @@ moe_status run_ffn(const moe_shape& s, const void* x_perm, const int32_t* offset
         TileArgs down{offsets, perm_w, y_slot, E, F, d / kTileN, d, d, g.timeout_ns};
         const int64_t tiles_down = ((R + kTileM - 1) / kTileM + E) * (d / kTileN);
         return launch("tile_down_scale", st, [&] {
-            tile_gemm_kernel<false><<<tc_grid(tiles_down), kTcThreads, kTileSmemBytes, st>>>(mh, mw2, mw2, down);
+            return klaunch(tile_gemm_kernel<false>, tc_grid(tiles_down), kTcThreads, kTileSmemBytes, st, mh, mw2, mw2, down);
         });
     }
     if (L.path != 2) return MOE_ERR_UNSUPPORTED;
@@ -353,12 +384,12 @@ moe_status run_ffn(const moe_shape& s, const void* x_perm, const int32_t* offset
     StreamArgs up{offsets, part_up, E, (int)R, L.ks_up, L.S_up, F / 128, 2, F, L.nb, stages, stage_bytes,
                   g.timeout_ns};
     MOE_TRY(launch("stream_up", st, [&] {
-        stream_gemm_kernel<true><<<tc_grid((int64_t)E * 2 * (F / 128) * L.S_up), kTcThreads, smem, st>>>(mw1, mw3,
+        return klaunch(stream_gemm_kernel<true>, tc_grid((int64_t)E * 2 * (F / 128) * L.S_up), kTcThreads, smem, st, mw1, mw3,
                                                                                                        mx, up);
     }));
     const int rgrid = (int)std::min<int64_t>((R * F + 255) / 256, (int64_t)sm_count() * 8);
     MOE_TRY(launch("reduce_swiglu", st, [&] {
-        reduce_swiglu_kernel<<<rgrid, 256, 0, st>>>(part_up, L.S_up, R, F, H);
+        return klaunch(reduce_swiglu_kernel, rgrid, 256, 0, st, part_up, L.S_up, R, F, H);
     }));
     CUtensorMap mw2, mh;
     if (!make_map(&mw2, w2, F, (uint64_t)E * d, 128) || !make_map(&mh, H, F, R, L.nb)) return MOE_ERR_CUDA;
@@ -366,12 +397,20 @@ moe_status run_ffn(const moe_shape& s, const void* x_perm, const int32_t* offset
     StreamArgs down{offsets, part_down, E, (int)R, L.ks_down, L.S_down, d / 128, 1, d, L.nb, stages, stage_bytes,
                     g.timeout_ns};
     MOE_TRY(launch("stream_down", st, [&] {
-        stream_gemm_kernel<false><<<tc_grid((int64_t)E * (d / 128) * L.S_down), kTcThreads, smem, st>>>(mw2, mw2,
+        return klaunch(stream_gemm_kernel<false>, tc_grid((int64_t)E * (d / 128) * L.S_down), kTcThreads, smem, st, mw2, mw2,
                                                                                                       mh, down);
     }));
+    if (slot_row != nullptr && y != nullptr && combined != nullptr) {
+        const int cgrid = (int)std::min<int64_t>((s.T * d + 255) / 256, (int64_t)sm_count() * 8);
+        *combined = true;
+        return launch("reduce_combine", st, [&] {
+            return klaunch(reduce_combine_kernel<__nv_bfloat16>, cgrid, 256, 0, st, part_down, L.S_down, R, d,
+                           perm_w, slot_row, s.T, static_cast<__nv_bfloat16*>(y));
+        });
+    }
     const int dgrid = (int)std::min<int64_t>((R * d + 255) / 256, (int64_t)sm_count() * 8);
     return launch("reduce_down", st, [&] {
-        reduce_down_kernel<<<dgrid, 256, 0, st>>>(part_down, L.S_down, R, d, perm_w, y_slot);
+        return klaunch(reduce_down_kernel, dgrid, 256, 0, st, part_down, L.S_down, R, d, perm_w, y_slot);
     });
 }
 
@@ -384,18 +423,18 @@ moe_status run_combine(const moe_shape& s, const float* y_slot, const int32_t* s
     if (s.dtype == MOE_BF16) {
         return launch("combine", st, [&] {
             if (v4)
-                combine4_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(y_slot, slot_row, s.T, s.d,
+                return klaunch(combine4_kernel<__nv_bfloat16>, grid, 256, 0, st, y_slot, slot_row, s.T, s.d,
                                                                      static_cast<__nv_bfloat16*>(y));
             else
-                combine_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(y_slot, slot_row, s.T, s.d,
+                return klaunch(combine_kernel<__nv_bfloat16>, grid, 256, 0, st, y_slot, slot_row, s.T, s.d,
                                                                     static_cast<__nv_bfloat16*>(y));
         });
     }
     return launch("combine", st, [&] {
         if (v4)
-            combine4_kernel<float><<<grid, 256, 0, st>>>(y_slot, slot_row, s.T, s.d, static_cast<float*>(y));
+            return klaunch(combine4_kernel<float>, grid, 256, 0, st, y_slot, slot_row, s.T, s.d, static_cast<float*>(y));
         else
-            combine_kernel<float><<<grid, 256, 0, st>>>(y_slot, slot_row, s.T, s.d, static_cast<float*>(y));
+            return klaunch(combine_kernel<float>, grid, 256, 0, st, y_slot, slot_row, s.T, s.d, static_cast<float*>(y));
     });
 }
 
@@ -409,7 +448,7 @@ moe_status run_aux(const moe_shape& s, const float* logits, const int32_t* count
         return MOE_OK;
     }
     return launch("aux_stats", st, [&] {
-        aux_stats_kernel<<<1, kAuxThreads, 0, st>>>(logits, counts, s.T, s.E, f, P, l_aux);
+        return klaunch(aux_stats_kernel, 1, kAuxThreads, 0, st, logits, counts, s.T, s.E, f, P, l_aux);
     });
 }
 
@@ -544,8 +583,9 @@ moe_status moe_layer_forward(const moe_shape* s, const void* x, const void* w_ga
     float* y_slot = reinterpret_cast<float*>(w + L.y_slot);
     MOE_TRY(run_router(*s, x, w_gate, idx, gw, logits, st));
     MOE_TRY(run_permute(*s, idx, gw, x, counts, offsets, perm_token, slot_row, perm_w, x_perm, st));
-    MOE_TRY(run_ffn(*s, x_perm, offsets, perm_w, w1, w3, w2, y_slot, w + L.ffn, L.f, st));
-    MOE_TRY(run_combine(*s, y_slot, slot_row, y, st));
+    bool combined = false;
+    MOE_TRY(run_ffn(*s, x_perm, offsets, perm_w, w1, w3, w2, y_slot, w + L.ffn, L.f, st, slot_row, y, &combined));
+    if (!combined) MOE_TRY(run_combine(*s, y_slot, slot_row, y, st));
     if (aux) MOE_TRY(run_aux(*s, logits, counts, aux_f, aux_P, aux_l_aux, st));
     return MOE_OK;
 }
@@ -593,6 +633,10 @@ moe_status moe_set_knob(int32_t knob, int64_t value) {
         case MOE_KNOB_GRID:
             if (value < 0 || value > 65535) return MOE_ERR_INVALID_ARG;
             g.grid = (int)value;
+            return MOE_OK;
+        case MOE_KNOB_PDL:
+            if (value < 0 || value > 1) return MOE_ERR_INVALID_ARG;
+            g.pdl = value != 0;
             return MOE_OK;
     }
     return MOE_ERR_INVALID_ARG;

@@ -21,9 +21,12 @@ __global__ void __launch_bounds__(kPermuteThreads)
     permute_kernel(const int32_t* __restrict__ topk_idx, const float* __restrict__ topk_w,
                    int64_t T_tokens, int E, int32_t* __restrict__ counts,
                    int32_t* __restrict__ offsets, int32_t* __restrict__ perm_token,
-                   int32_t* __restrict__ slot_row, float* __restrict__ perm_w) {
+                   int32_t* __restrict__ slot_row, float* __restrict__ perm_w,
+                   const unsigned char* __restrict__ x, int64_t row_bytes, unsigned char* __restrict__ x_perm) {
     __shared__ int warp_tot[kPermuteThreads / 32][kMaxExperts];
     __shared__ int s_off[kMaxExperts + 1];
+    pdl_trigger();
+    pdl_wait();
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int warp = tid >> 5;
@@ -108,6 +111,18 @@ __global__ void __launch_bounds__(kPermuteThreads)
             slot_row[2 * t + j] = r;
         }
     }
+    // Small batches: the same CTA copies the token rows into expert order
+    // (x != nullptr; row_bytes % 16 == 0), saving a launch.
+    if (x != nullptr) {
+        __syncthreads();
+        const int64_t rows = s_off[E];
+        const int64_t c16 = row_bytes / 16;
+        for (int64_t i = tid; i < rows * c16; i += kPermuteThreads) {
+            const int64_t r = i / c16, c = i - r * c16;
+            const int64_t tk = perm_token[r];
+            reinterpret_cast<uint4*>(x_perm + r * row_bytes)[c] = reinterpret_cast<const uint4*>(x + tk * row_bytes)[c];
+        }
+    }
 }
 
 // x_perm[r] = x[perm_token[r]]: one row per warp-group, 16-byte copies when
@@ -116,6 +131,8 @@ __global__ void __launch_bounds__(256)
     gather_rows_kernel(const unsigned char* __restrict__ x, const int32_t* __restrict__ perm_token,
                        const int32_t* __restrict__ offsets, int E, int64_t rows, int64_t row_bytes,
                        unsigned char* __restrict__ x_perm) {
+    pdl_trigger();
+    pdl_wait();
     const int64_t valid_rows = ((int64_t)offsets[E] < rows) ? (int64_t)offsets[E] : rows;
     const int64_t chunks16 = (row_bytes % 16 == 0) ? row_bytes / 16 : 0;
     for (int64_t r = blockIdx.x; r < valid_rows; r += gridDim.x) {

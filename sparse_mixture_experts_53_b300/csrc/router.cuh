@@ -74,6 +74,8 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
                        int E, int use_smem, int vec, int32_t* __restrict__ topk_idx,
                        float* __restrict__ topk_w, float* __restrict__ logits) {
     extern __shared__ __align__(16) unsigned char router_smem[];
+    pdl_trigger();
+    pdl_wait();
     const T* w = wg;
     if (use_smem) {
         T* s = reinterpret_cast<T*>(router_smem);
@@ -150,6 +152,8 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
     router_top2_split_kernel(const T* __restrict__ x, const T* __restrict__ wg, int64_t T_tokens, int d, int E,
                              int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, float* __restrict__ logits) {
     __shared__ float part[kRouterWarps][kMaxExperts];
+    pdl_trigger();
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     constexpr int V = Vec16<T>::N;

@@ -30,6 +30,7 @@ MOE_BF16 = 1
 MOE_KNOB_FFN_PATH = 1
 MOE_KNOB_KSLICE = 2
 MOE_KNOB_GRID = 3
+MOE_KNOB_PDL = 4
 
 EXPORTED = (
     "moe_version", "moe_status_string", "moe_workspace_bytes", "moe_ffn_workspace_bytes",

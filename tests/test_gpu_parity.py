@@ -290,3 +290,22 @@ def test_named_workload_full_size(k, mixtral_weights, mixtral_dev_weights):
     if k == 4:
         counts = got["counts"].numpy()
         assert counts.min() == 0  # the skewed workload leaves one expert empty
+
+
+@pytest.mark.parametrize("T", [16, 300])
+def test_pdl_on_and_off_give_identical_results(T):
+    """Programmatic dependent launch only overlaps launch set-up: results are bit-identical."""
+    L = _margin_layer(T, 512, 1024, "bf16", seed=1200 + T)
+    dev = upload(L)
+    outs = []
+    for pdl in (0, 1):
+        moe.moe_set_knob(moe.MOE_KNOB_PDL, pdl)
+        try:
+            outs.append(run_forward(L, dev))
+            outs.append(run_staged(L, dev)["y"])
+        finally:
+            moe.moe_set_knob(moe.MOE_KNOB_PDL, 1)
+        assert_status_ok()
+    for o in outs[1:]:
+        assert torch.equal(outs[0], o)
+    check_y(L, outs[0])
