@@ -190,6 +190,7 @@ def run_ours(args, rank, world, local) -> dict | None:
 
     torch.cuda.set_device(local)
     moe.moe_set_knob(moe.MOE_KNOB_PDL, args.pdl)
+    moe.moe_set_knob(moe.MOE_KNOB_TILE_CTAS, args.tile_ctas)
     dist = None
     if world > 1:
         import torch.distributed as dist
@@ -308,7 +309,8 @@ def run_ours(args, rank, world, local) -> dict | None:
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded Mixtral-shape tensors, random init)",
         "config": {"workload": cfg["name"], "T": cfg["T"], "d": cfg["d"], "ffn": cfg["ffn"], "E": cfg["E"], "k": 2,
                    "aux_stats": aux, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "ffn_path": "weight-streaming (swap-AB)" if streaming else "token tiles 128x256",
+                   "ffn_path": "weight-streaming (swap-AB)" if streaming else
+                   ("token tiles 256x256 on CTA pairs" if args.tile_ctas == 2 else "token tiles 128x256"),
                    "pdl": bool(args.pdl),
                    "l2": "inputs larger than L2: each step reads %.2f GB of expert weights" % (work["weight_bytes"] / 1e9),
                    "experts_touched": work["touched"], "input_gen_s": round(gen_s, 1)},
@@ -398,6 +400,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--pdl", type=int, default=1, choices=[0, 1],
                     help="programmatic dependent launch between the library's kernels")
+    ap.add_argument("--tile-ctas", type=int, default=2, choices=[1, 2],
+                    help="token tiles on CTA pairs (2) or single CTAs (1)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

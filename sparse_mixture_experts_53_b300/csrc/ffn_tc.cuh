@@ -100,6 +100,54 @@ struct TileArgs {
     uint64_t timeout_ns;
 };
 
+// Epilogue of one token tile for one thread (one row): reads the row's 256
+// accumulator columns from tensor memory and writes
+//   up:   h = SiLU(u) * v in bf16 (u = columns 0-127, v = columns 128-255),
+//   down: perm_w[r] * acc in fp32.
+// Every thread of the warp must call it (tcgen05.ld is warp-collective);
+// `valid` only predicates the stores.
+template <bool UP>
+__device__ __forceinline__ void tile_epilogue(uint32_t taddr, bool valid, int64_t r, int nt, const TileArgs& args) {
+    if (UP) {
+        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(args.out) + r * args.ldo + nt * kTileM;
+#pragma unroll 1
+        for (int j = 0; j < kTileM; j += 16) {
+            uint32_t u[16], v[16];
+            tmem_ld16(taddr + j, u);
+            tmem_ld16(taddr + kTileM + j, v);
+            tmem_wait_ld();
+            uint32_t pk[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float h0 = silu_f32(__uint_as_float(u[2 * i])) * __uint_as_float(v[2 * i]);
+                const float h1 = silu_f32(__uint_as_float(u[2 * i + 1])) * __uint_as_float(v[2 * i + 1]);
+                pk[i] = pack_bf16x2(h0, h1);
+            }
+            if (valid) {
+                uint4* dst = reinterpret_cast<uint4*>(out + j);
+                dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            }
+        }
+    } else {
+        const float pw = valid ? args.perm_w[r] : 0.f;
+        float* out = reinterpret_cast<float*>(args.out) + r * args.ldo + nt * kTileN;
+#pragma unroll 1
+        for (int j = 0; j < kTileN; j += 16) {
+            uint32_t a[16];
+            tmem_ld16(taddr + j, a);
+            tmem_wait_ld();
+            if (valid) {
+                float4* dst = reinterpret_cast<float4*>(out + j);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    dst[i] = make_float4(pw * __uint_as_float(a[4 * i]), pw * __uint_as_float(a[4 * i + 1]),
+                                         pw * __uint_as_float(a[4 * i + 2]), pw * __uint_as_float(a[4 * i + 3]));
+            }
+        }
+    }
+}
+
 // UP = true: SwiGLU up-projection; UP = false: W2 down-projection + gate scale.
 template <bool UP>
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -274,44 +322,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int grow = mt * kTileM + row_in_tile;
             const bool valid = grow < ctl->cnt[e];
             const int64_t r = ctl->off[e] + grow;
-            if (UP) {
-                __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(args.out) + r * args.ldo + nt * kTileM;
-#pragma unroll 1
-                for (int j = 0; j < kTileM; j += 16) {
-                    uint32_t u[16], v[16];
-                    tmem_ld16(taddr + j, u);
-                    tmem_ld16(taddr + kTileM + j, v);
-                    tmem_wait_ld();
-                    uint32_t pk[8];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const float h0 = silu_f32(__uint_as_float(u[2 * i])) * __uint_as_float(v[2 * i]);
-                        const float h1 = silu_f32(__uint_as_float(u[2 * i + 1])) * __uint_as_float(v[2 * i + 1]);
-                        pk[i] = pack_bf16x2(h0, h1);
-                    }
-                    if (valid) {
-                        uint4* dst = reinterpret_cast<uint4*>(out + j);
-                        dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                        dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-                    }
-                }
-            } else {
-                const float pw = valid ? args.perm_w[r] : 0.f;
-                float* out = reinterpret_cast<float*>(args.out) + r * args.ldo + nt * kTileN;
-#pragma unroll 1
-                for (int j = 0; j < kTileN; j += 16) {
-                    uint32_t a[16];
-                    tmem_ld16(taddr + j, a);
-                    tmem_wait_ld();
-                    if (valid) {
-                        float4* dst = reinterpret_cast<float4*>(out + j);
-#pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            dst[i] = make_float4(pw * __uint_as_float(a[4 * i]), pw * __uint_as_float(a[4 * i + 1]),
-                                                 pw * __uint_as_float(a[4 * i + 2]), pw * __uint_as_float(a[4 * i + 3]));
-                    }
-                }
-            }
+            tile_epilogue<UP>(taddr, valid, r, nt, args);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[b]));
@@ -322,6 +333,212 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem_base, 2 * kTileAccCols);
+}
+
+// ---------------------------------------------------------------------------
+// token tiles on CTA pairs: one tcgen05.mma.cta_group::2 spans the tensor cores
+// of two SMs. The pair owns a 256-token x 256-column tile: each CTA stages 128
+// token rows of A and 128 rows of B (up: CTA 0 the W1 rows, CTA 1 the W3 rows;
+// down: the two halves of the 256 W2 rows) and holds the accumulator of its
+// own 128 token rows. Per FLOP, each SM reads two thirds of the operand bytes
+// of the single-CTA tile (L2 -> shared memory and shared memory -> tensor
+// core). The even CTA (rank 0) issues the MMAs; the TMA loads of both CTAs
+// count on its `full` barrier, its commits arrive on `empty`/`tfull` of both
+// CTAs, and the epilogues of both CTAs arrive on its `tempty`.
+// ---------------------------------------------------------------------------
+constexpr int kPairM = 256;
+constexpr int kPairStages = 6;
+constexpr uint32_t kPairHalfBytes = 128 * kBK * 2;          // 16 KB: one CTA's half of A or of B
+constexpr uint32_t kPairStageBytes = 2 * kPairHalfBytes;     // 32 KB per CTA and stage
+constexpr size_t kPairSmemBytes = 1024 + (size_t)kPairStages * kPairStageBytes + sizeof(TcControl);
+
+template <bool UP>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
+    tile_pair_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b0,
+                          const __grid_constant__ CUtensorMap map_b1, const TileArgs args) {
+    extern __shared__ unsigned char tc_smem_raw[];
+    unsigned char* smem = align1024(tc_smem_raw);
+    TcControl* ctl = reinterpret_cast<TcControl*>(smem + (size_t)kPairStages * kPairStageBytes);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int pair = blockIdx.x >> 1;
+    const int n_pairs = gridDim.x >> 1;
+    const int kid = UP ? K_TILE_UP : K_TILE_DOWN;
+    const uint64_t tmo = args.timeout_ns;
+    volatile int* abort_flag = &ctl->abort_flag;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kPairStages; ++s) {
+            mbar_init(smem_u32(&ctl->full[s]), 1);
+            mbar_init(smem_u32(&ctl->empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&ctl->tfull[b]), 1);
+            mbar_init(smem_u32(&ctl->tempty[b]), 8);  // 4 epilogue warps in each CTA
+        }
+        mbar_init(smem_u32(&ctl->drain), 1);
+        ctl->abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&map_a);
+        tma_prefetch_desc(&map_b0);
+        if (UP) tma_prefetch_desc(&map_b1);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(&ctl->tmem_base), 2 * kTileAccCols);
+        tmem_relinquish_pair();
+    }
+    pdl_trigger();
+    pdl_wait();
+    if (threadIdx.x == 0) {
+        int tiles = 0;
+        for (int e = 0; e <= args.E; ++e) ctl->off[e] = args.offsets[e];
+        for (int e = 0; e < args.E; ++e) {
+            const int c = ctl->off[e + 1] - ctl->off[e];
+            ctl->cnt[e] = c;
+            ctl->mt[e] = (c + kPairM - 1) / kPairM;
+            ctl->base[e] = tiles;
+            tiles += ctl->mt[e] * args.n_tiles_n;
+        }
+        ctl->base[args.E] = tiles;
+        ctl->n_work = tiles;
+    }
+    // both CTAs' barriers are initialised and both halves of tensor memory are
+    // allocated before any CTA signals the other
+    tc_fence_before();
+    cluster_sync();
+    tc_fence_after();
+    const uint32_t tmem_base = ctl->tmem_base;
+    const int n_work = ctl->n_work;
+    const int E = args.E;
+    const int KB = args.K / kBK;
+
+    auto decode = [&](int tile, int& e, int& nt, int& mt) {
+        e = 0;
+        while (e < E - 1 && tile >= ctl->base[e + 1]) ++e;
+        const int rem = tile - ctl->base[e];
+        nt = rem / ctl->mt[e];
+        mt = rem - nt * ctl->mt[e];
+    };
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer (both CTAs)
+        if (lane == 0) {
+            const uint64_t pol_act = policy_evict_last();
+            const uint64_t pol_w = policy_evict_normal();
+            const CUtensorMap* map_b = (UP && rank == 1) ? &map_b1 : &map_b0;
+            uint32_t s = 0, ph = 0;
+            uint32_t issued_mask = 0, issued_ph = 0;
+            bool ok = true;
+            for (int tile = pair; ok && tile < n_work; tile += n_pairs) {
+                int e, nt, mt;
+                decode(tile, e, nt, mt);
+                const int arow = ctl->off[e] + mt * kPairM + 128 * (int)rank;
+                const int brow = UP ? e * args.w_rows + nt * kTileM : e * args.w_rows + nt * kTileN + 128 * (int)rank;
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!mbar_wait(smem_u32(&ctl->empty[s]), ph ^ 1, tmo, abort_flag)) {
+                        raise_abort(ctl, kid, W_PRODUCER);
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb_local = smem_u32(&ctl->full[s]);
+                    const uint32_t fb = mapa_shared(fb_local, 0);  // the leader's barrier counts both CTAs
+                    if (leader) mbar_arrive_expect_tx(fb_local, 2 * kPairStageBytes);
+                    const uint32_t sa = smem_u32(smem + (size_t)s * kPairStageBytes);
+                    tma_load_2d_pair(sa, &map_a, fb, kb * kBK, arow, pol_act);
+                    tma_load_2d_pair(sa + kPairHalfBytes, map_b, fb, kb * kBK, brow, pol_w);
+                    issued_mask |= 1u << s;
+                    issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
+                    if (++s == kPairStages) { s = 0; ph ^= 1; }
+                }
+            }
+            if (!ok && leader) {
+                for (int q = 0; q < kPairStages; ++q)
+                    if (issued_mask & (1u << q))
+                        drain_wait(smem_u32(&ctl->full[q]), (issued_ph >> q) & 1u, tmo, kid);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer (even CTA only)
+        if (lane == 0 && leader) {
+            constexpr uint32_t idesc = idesc_bf16_f32(kPairM, kTileN);
+            uint32_t s = 0, ph = 0;
+            bool ok = true, any = false;
+            int it = 0;
+            for (int tile = pair; ok && tile < n_work; tile += n_pairs, ++it) {
+                const int b = it & 1;
+                const uint32_t aph = (it >> 1) & 1;
+                if (!mbar_wait_cluster(smem_u32(&ctl->tempty[b]), aph ^ 1, tmo, abort_flag)) {
+                    raise_abort(ctl, kid, W_MMA);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + b * kTileAccCols;
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!mbar_wait(smem_u32(&ctl->full[s]), ph, tmo, abort_flag)) {
+                        raise_abort(ctl, kid, W_MMA);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(smem + (size_t)s * kPairStageBytes);
+                    const uint64_t adesc = sw128_kmajor_desc(sa);
+                    const uint64_t bdesc = sw128_kmajor_desc(sa + kPairHalfBytes);
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk)
+                        mma_bf16_pair(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (kb | kk) != 0);
+                    any = true;
+                    mma_commit_pair(smem_u32(&ctl->empty[s]), 0x3);
+                    if (++s == kPairStages) { s = 0; ph ^= 1; }
+                }
+                if (!ok) break;
+                mma_commit_pair(smem_u32(&ctl->tfull[b]), 0x3);
+            }
+            if (any) {
+                mma_commit_pair(smem_u32(&ctl->drain), 0x1);
+                drain_wait(smem_u32(&ctl->drain), 0, tmo, kid);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------ epilogue (warps 2-5, both CTAs)
+        const int sub = warp & 3;
+        const int row_in_tile = 128 * (int)rank + sub * 32 + lane;
+        uint32_t tempty_leader[2];
+        for (int b = 0; b < 2; ++b) tempty_leader[b] = mapa_shared(smem_u32(&ctl->tempty[b]), 0);
+        int it = 0;
+        for (int tile = pair; tile < n_work; tile += n_pairs, ++it) {
+            int e, nt, mt;
+            decode(tile, e, nt, mt);
+            const int b = it & 1;
+            const uint32_t aph = (it >> 1) & 1;
+            if (!mbar_wait(smem_u32(&ctl->tfull[b]), aph, tmo, abort_flag)) {
+                raise_abort(ctl, kid, W_EPILOGUE);
+                break;
+            }
+            tc_fence_after();
+            const uint32_t taddr = tmem_base + b * kTileAccCols + ((uint32_t)(sub * 32) << 16);
+            const int grow = mt * kPairM + row_in_tile;
+            const bool valid = grow < ctl->cnt[e];
+            const int64_t r = ctl->off[e] + grow;
+            tile_epilogue<UP>(taddr, valid, r, nt, args);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(tempty_leader[b]);
+        }
+    }
+
+    // no CTA of the pair frees tensor memory or leaves while the other may
+    // still be signalled or read
+    tc_fence_before();
+    cluster_sync();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc_pair(tmem_base, 2 * kTileAccCols);
 }
 
 // ---------------------------------------------------------------------------

@@ -42,6 +42,8 @@ struct HostState {
     uint64_t timeout_ns = 2000000000ull;
     bool timing = false;
     bool pdl = true;           // programmatic dependent launch between the library's kernels
+    int tile_ctas = 2;         // token tiles on CTA pairs (2) or single CTAs (1)
+    int pair_cap[kMaxDevices][2] = {{0}};  // resident CTA pairs per kernel (0 = not queried)
     std::vector<TimingRecord> records;
     std::vector<cudaEvent_t> pool;
     int sms[kMaxDevices] = {0};
@@ -326,6 +328,35 @@ int tc_grid(int64_t work_upper) {
     return (int)std::max<int64_t>(1, std::min<int64_t>(work_upper, sms));
 }
 
+// CTA pairs of a cluster-of-2 kernel that fit on the GPU at once (queried once
+// per device); -1 if none fits.
+template <typename K>
+int pair_capacity(K kernel, size_t smem, int slot) {
+    const int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices) return -1;
+    int& cap = g.pair_cap[dev][slot];
+    if (cap == 0) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2 * (sm_count() / 2));
+        cfg.blockDim = dim3(kTcThreads);
+        cfg.dynamicSmemBytes = smem;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n <= 0) {
+            cudaGetLastError();
+            n = -1;
+        }
+        cap = n;
+    }
+    return cap;
+}
+
+// Grid of a persistent CTA-pair kernel: an even number of CTAs.
+int pair_grid(int64_t pairs_upper, int cap) {
+    int pairs = g.grid > 0 ? std::max(1, g.grid / 2) : cap;
+    pairs = (int)std::max<int64_t>(1, std::min<int64_t>(pairs_upper, pairs));
+    return 2 * pairs;
+}
+
 // With slot_row and y given (the whole-layer call), the weight-streaming path
 // finishes with the fused K-slice sum + gate scale + combine and sets
 // *combined; otherwise it writes y_slot.
@@ -350,6 +381,33 @@ moe_status run_ffn(const moe_shape& s, const void* x_perm, const int32_t* offset
         });
     }
     __nv_bfloat16* H = reinterpret_cast<__nv_bfloat16*>(ws + L.h);
+    if (L.path == 1 && g.tile_ctas == 2) {
+        // CTA pairs: each CTA stages 128 token rows and 128 weight rows per stage
+        const int cap_up = ensure_smem(tile_pair_gemm_kernel<true>, 6, kPairSmemBytes)
+                               ? pair_capacity(tile_pair_gemm_kernel<true>, kPairSmemBytes, 0) : -1;
+        const int cap_down = ensure_smem(tile_pair_gemm_kernel<false>, 7, kPairSmemBytes)
+                                 ? pair_capacity(tile_pair_gemm_kernel<false>, kPairSmemBytes, 1) : -1;
+        if (cap_up > 0 && cap_down > 0) {
+            CUtensorMap ma, mb0, mb1;
+            if (!make_map(&ma, x_perm, d, R, 128) || !make_map(&mb0, w1, d, (uint64_t)E * F, 128) ||
+                !make_map(&mb1, w3, d, (uint64_t)E * F, 128))
+                return MOE_ERR_CUDA;
+            TileArgs up{offsets, perm_w, H, E, d, F / kTileM, F, F, g.timeout_ns};
+            const int64_t pairs_up = ((R + kPairM - 1) / kPairM + E) * (F / kTileM);
+            MOE_TRY(launch("tile_up_swiglu", st, [&] {
+                return klaunch(tile_pair_gemm_kernel<true>, pair_grid(pairs_up, cap_up), kTcThreads, kPairSmemBytes,
+                               st, ma, mb0, mb1, up);
+            }));
+            CUtensorMap mh, mw2;
+            if (!make_map(&mh, H, F, R, 128) || !make_map(&mw2, w2, F, (uint64_t)E * d, 128)) return MOE_ERR_CUDA;
+            TileArgs down{offsets, perm_w, y_slot, E, F, d / kTileN, d, d, g.timeout_ns};
+            const int64_t pairs_down = ((R + kPairM - 1) / kPairM + E) * (d / kTileN);
+            return launch("tile_down_scale", st, [&] {
+                return klaunch(tile_pair_gemm_kernel<false>, pair_grid(pairs_down, cap_down), kTcThreads,
+                               kPairSmemBytes, st, mh, mw2, mw2, down);
+            });
+        }
+    }
     if (L.path == 1) {
         CUtensorMap ma, mb0, mb1;
         if (!make_map(&ma, x_perm, d, R, kTileM) || !make_map(&mb0, w1, d, (uint64_t)E * F, kTileM) ||
@@ -637,6 +695,10 @@ moe_status moe_set_knob(int32_t knob, int64_t value) {
         case MOE_KNOB_PDL:
             if (value < 0 || value > 1) return MOE_ERR_INVALID_ARG;
             g.pdl = value != 0;
+            return MOE_OK;
+        case MOE_KNOB_TILE_CTAS:
+            if (value != 1 && value != 2) return MOE_ERR_INVALID_ARG;
+            g.tile_ctas = (int)value;
             return MOE_OK;
     }
     return MOE_ERR_INVALID_ARG;

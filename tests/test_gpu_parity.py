@@ -24,11 +24,13 @@ def _reset_knobs():
     moe.moe_set_knob(moe.MOE_KNOB_FFN_PATH, 0)
     moe.moe_set_knob(moe.MOE_KNOB_KSLICE, 0)
     moe.moe_set_knob(moe.MOE_KNOB_GRID, 0)
+    moe.moe_set_knob(moe.MOE_KNOB_TILE_CTAS, 2)
     moe.moe_get_device_status()
     yield
     moe.moe_set_knob(moe.MOE_KNOB_FFN_PATH, 0)
     moe.moe_set_knob(moe.MOE_KNOB_KSLICE, 0)
     moe.moe_set_knob(moe.MOE_KNOB_GRID, 0)
+    moe.moe_set_knob(moe.MOE_KNOB_TILE_CTAS, 2)
 
 
 def _margin_layer(T, d, ffn, dtype, seed, weights=None, E=8):
@@ -88,9 +90,12 @@ SMALL_BF16 = [
 ]
 
 
+@pytest.mark.parametrize("ctas", [2, 1])
 @pytest.mark.parametrize("T,d,ffn", SMALL_BF16)
-def test_bf16_token_tile_path(T, d, ffn):
+def test_bf16_token_tile_path(T, d, ffn, ctas):
+    """Token tiles on CTA pairs (256-token tiles, one MMA across two SMs) and on single CTAs."""
     moe.moe_set_knob(moe.MOE_KNOB_FFN_PATH, 1)
+    moe.moe_set_knob(moe.MOE_KNOB_TILE_CTAS, ctas)
     L = _margin_layer(T, d, ffn, "bf16", seed=7 + T)
     got = run_staged(L)
     assert_status_ok()
@@ -133,8 +138,9 @@ def test_both_bf16_paths_agree(T):
 def test_small_grid_many_tiles_per_cta():
     """Few CTAs: each runs many tiles, cycling all stages and both accumulators."""
     moe.moe_set_knob(moe.MOE_KNOB_GRID, 3)
-    for path, T in ((1, 700), (2, 40)):
+    for path, T, ctas in ((1, 700, 2), (1, 700, 1), (2, 40, 1)):
         moe.moe_set_knob(moe.MOE_KNOB_FFN_PATH, path)
+        moe.moe_set_knob(moe.MOE_KNOB_TILE_CTAS, ctas)
         L = _margin_layer(T, 256, 512, "bf16", seed=300 + T)
         got = run_staged(L)
         assert_status_ok()
@@ -309,3 +315,17 @@ def test_pdl_on_and_off_give_identical_results(T):
     for o in outs[1:]:
         assert torch.equal(outs[0], o)
     check_y(L, outs[0])
+
+
+def test_single_and_paired_token_tiles_agree():
+    """Same sums in the same K order: the 1-CTA and CTA-pair tiles give the same y_slot up to rounding."""
+    L = _margin_layer(600, 512, 1024, "bf16", seed=1300)
+    dev = upload(L)
+    moe.moe_set_knob(moe.MOE_KNOB_FFN_PATH, 1)
+    outs = []
+    for ctas in (1, 2):
+        moe.moe_set_knob(moe.MOE_KNOB_TILE_CTAS, ctas)
+        outs.append(run_staged(L, dev))
+        assert_status_ok()
+    a, b = outs[0]["y_slot"].numpy(), outs[1]["y_slot"].numpy()
+    assert np.max(np.abs(a - b)) <= 1e-3 * np.max(np.abs(a))
