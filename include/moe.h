@@ -113,10 +113,19 @@ moe_status moe_route_top2(const moe_shape* s, const void* x, const void* w_gate,
  *   slot_row          [T][2] out   row of slot (t, j)
  *   perm_w            [2T]  out    gate weight of each row
  *   x_perm            [2T][d] out  x_perm[r] = x[perm_token[r]]
- * An index outside [0, E) latches MOE_ERR_DEVICE_CHECK; that slot gets row -1. */
+ *   ws / ws_bytes                  optional scratch of moe_permute_workspace_bytes(s)
+ *                                  bytes; with it, batches of 2048 tokens or more are
+ *                                  grouped by many CTAs (per-chunk counts, then ranks),
+ *                                  without it by one CTA. Both give the same result.
+ * An index outside [0, E) latches MOE_ERR_DEVICE_CHECK; that slot gets row -1.
+ * A non-NULL ws smaller than required returns MOE_ERR_WORKSPACE. */
 moe_status moe_permute(const moe_shape* s, const int32_t* topk_idx, const float* topk_w,
                        const void* x, int32_t* counts, int32_t* offsets, int32_t* perm_token,
-                       int32_t* slot_row, float* perm_w, void* x_perm, void* stream);
+                       int32_t* slot_row, float* perm_w, void* x_perm, void* ws, size_t ws_bytes,
+                       void* stream);
+
+/* Scratch bytes for moe_permute's many-CTA grouping (0 on a bad shape). */
+size_t moe_permute_workspace_bytes(const moe_shape* s);
 
 /* Expert FFNs on the grouped rows, scaled by the gate weight (tokentrails
  * Code: expert = w2(silu(w1 x) * w3 x)):

@@ -28,6 +28,8 @@ constexpr size_t kAlign = 1024;
 constexpr int kStreamMaxTokens = 64;     // weight-streaming path needs T <= 64
 constexpr int64_t kRouterSplitMaxTokens = 256;  // one CTA per token below this
 constexpr int64_t kFusedGatherBytes = 512 * 1024;  // the permutation CTA gathers x_perm below this
+constexpr int64_t kPermuteMultiMinTokens = 2048;  // many-CTA grouping from this batch size on
+constexpr int64_t kPermuteMaxChunks = 4096;       // token chunks (CTAs) of the many-CTA grouping
 constexpr size_t kSmemBudget = 225 * 1024;
 
 struct TimingRecord {
@@ -200,6 +202,17 @@ int choose_path(const moe_shape& s) {
     return s.T <= kStreamMaxTokens ? 2 : 1;
 }
 
+// Tokens per CTA of the many-CTA grouping and the number of chunks.
+int64_t permute_chunk(int64_t T) {
+    const int64_t c = (T + kPermuteMaxChunks - 1) / kPermuteMaxChunks;
+    return std::max<int64_t>(kPlaceSub, (c + kPlaceSub - 1) / kPlaceSub * kPlaceSub);
+}
+
+size_t permute_ws_bytes(const moe_shape& s) {
+    const int64_t chunks = (std::max<int64_t>(s.T, 1) + permute_chunk(s.T) - 1) / permute_chunk(s.T);
+    return align_up((size_t)chunks * kMaxExperts * sizeof(int32_t), 256);
+}
+
 struct FfnLayout {
     int path = 0;
     int nb = 0, ks_up = 0, ks_down = 0, S_up = 0, S_down = 0;
@@ -231,7 +244,7 @@ FfnLayout ffn_layout(const moe_shape& s) {
 }
 
 struct FwdLayout {
-    size_t idx, w, logits, counts, offsets, perm_token, slot_row, perm_w, x_perm, y_slot, ffn, total;
+    size_t idx, w, logits, counts, offsets, perm_token, slot_row, perm_w, perm_ws, x_perm, y_slot, ffn, total;
     FfnLayout f;
 };
 
@@ -252,6 +265,7 @@ FwdLayout fwd_layout(const moe_shape& s) {
     L.perm_token = take(R * 4);
     L.slot_row = take(R * 4);
     L.perm_w = take(R * 4);
+    L.perm_ws = take(permute_ws_bytes(s));
     L.x_perm = take(R * s.d * esize(s));
     L.y_slot = take(R * s.d * 4);
     L.f = ffn_layout(s);
@@ -270,7 +284,10 @@ moe_status run_router(const moe_shape& s, const void* x, const void* wg, int32_t
     const int V = (int)(16 / es);
     const int vec = (s.d % V == 0 && aligned16(x) && aligned16(wg)) ? 1 : 0;
     const int64_t blocks = (s.T + kRouterWarps - 1) / kRouterWarps;
-    const int grid = (int)std::min<int64_t>(blocks, (int64_t)sm_count() * 4);
+    // as many CTAs as fit at once (W_g staged in shared memory limits them)
+    // (126 registers x 256 threads: two CTAs per SM)
+    const int per_sm = use_smem ? (int)std::max<size_t>(1, std::min<size_t>(2, (200 * 1024) / std::max<size_t>(1, wbytes))) : 2;
+    const int grid = (int)std::min<int64_t>(blocks, (int64_t)sm_count() * per_sm);
     const size_t smem = use_smem ? wbytes : 0;
     if (vec && s.T <= kRouterSplitMaxTokens) {
         // small batch: one CTA per token, the model dimension split over 8 warps
@@ -304,18 +321,35 @@ moe_status run_router(const moe_shape& s, const void* x, const void* wg, int32_t
 
 moe_status run_permute(const moe_shape& s, const int32_t* idx, const float* w, const void* x, int32_t* counts,
                        int32_t* offsets, int32_t* perm_token, int32_t* slot_row, float* perm_w, void* x_perm,
-                       cudaStream_t st) {
+                       void* ws, size_t ws_bytes, cudaStream_t st) {
     const int64_t R = 2 * s.T;
     const int64_t row_bytes = (int64_t)s.d * esize(s);
-    // small batches: the permutation CTA also copies the rows (one launch less)
-    const bool fused = s.T > 0 && row_bytes % 16 == 0 && R * row_bytes <= kFusedGatherBytes &&
-                       aligned16(x) && aligned16(x_perm);
-    MOE_TRY(launch("permute", st, [&] {
-        return klaunch(permute_kernel, 1, kPermuteThreads, 0, st, idx, w, s.T, s.E, counts, offsets, perm_token,
-                       slot_row, perm_w, fused ? static_cast<const unsigned char*>(x) : nullptr, row_bytes,
-                       static_cast<unsigned char*>(x_perm));
-    }));
-    if (s.T == 0 || fused) return MOE_OK;
+    const bool rows16 = row_bytes % 16 == 0 && aligned16(x) && aligned16(x_perm);
+    if (s.T >= kPermuteMultiMinTokens && ws != nullptr && ws_bytes >= permute_ws_bytes(s)) {
+        // large batch: per-chunk counts, then ranks + rows + row copies on many CTAs
+        const int64_t chunk = permute_chunk(s.T);
+        const int nchunks = (int)((s.T + chunk - 1) / chunk);
+        int32_t* chunk_counts = static_cast<int32_t*>(ws);
+        MOE_TRY(launch("permute_count", st, [&] {
+            return klaunch(permute_count_kernel, nchunks, kPlaceThreads, 0, st, idx, s.T, s.E, chunk, chunk_counts);
+        }));
+        MOE_TRY(launch("permute_place", st, [&] {
+            return klaunch(permute_place_kernel, nchunks, kPlaceThreads, 0, st, idx, w, s.T, s.E, chunk, nchunks,
+                           static_cast<const int32_t*>(chunk_counts), counts, offsets, perm_token, slot_row, perm_w,
+                           rows16 ? static_cast<const unsigned char*>(x) : nullptr, row_bytes,
+                           static_cast<unsigned char*>(x_perm));
+        }));
+        if (rows16) return MOE_OK;
+    } else {
+        // small batch: one CTA; it also copies the rows when they are few
+        const bool fused = s.T > 0 && rows16 && R * row_bytes <= kFusedGatherBytes;
+        MOE_TRY(launch("permute", st, [&] {
+            return klaunch(permute_kernel, 1, kPermuteThreads, 0, st, idx, w, s.T, s.E, counts, offsets, perm_token,
+                           slot_row, perm_w, fused ? static_cast<const unsigned char*>(x) : nullptr, row_bytes,
+                           static_cast<unsigned char*>(x_perm));
+        }));
+        if (s.T == 0 || fused) return MOE_OK;
+    }
     const int grid = (int)std::min<int64_t>(R, (int64_t)sm_count() * 8);
     return launch("gather_rows", st, [&] {
         return klaunch(gather_rows_kernel, grid, 256, 0, st, static_cast<const unsigned char*>(x), perm_token,
@@ -573,15 +607,21 @@ moe_status moe_route_top2(const moe_shape* s, const void* x, const void* w_gate,
     return run_router(*s, x, w_gate, topk_idx, topk_w, logits, static_cast<cudaStream_t>(stream));
 }
 
+size_t moe_permute_workspace_bytes(const moe_shape* s) {
+    if (check_shape(s) != MOE_OK) return 0;
+    return permute_ws_bytes(*s);
+}
+
 moe_status moe_permute(const moe_shape* s, const int32_t* topk_idx, const float* topk_w, const void* x,
                        int32_t* counts, int32_t* offsets, int32_t* perm_token, int32_t* slot_row, float* perm_w,
-                       void* x_perm, void* stream) {
+                       void* x_perm, void* ws, size_t ws_bytes, void* stream) {
     MOE_TRY(check_shape(s));
     if (!ok_ptr(counts) || !ok_ptr(offsets)) return MOE_ERR_INVALID_ARG;
     if (s->T > 0 && (!ok_ptr(topk_idx) || !ok_ptr(topk_w) || !ok_ptr(x) || !ok_ptr(perm_token) ||
                      !ok_ptr(slot_row) || !ok_ptr(perm_w) || !ok_ptr(x_perm)))
         return MOE_ERR_INVALID_ARG;
-    return run_permute(*s, topk_idx, topk_w, x, counts, offsets, perm_token, slot_row, perm_w, x_perm,
+    if (ws != nullptr && (!aligned16(ws) || ws_bytes < permute_ws_bytes(*s))) return MOE_ERR_WORKSPACE;
+    return run_permute(*s, topk_idx, topk_w, x, counts, offsets, perm_token, slot_row, perm_w, x_perm, ws, ws_bytes,
                        static_cast<cudaStream_t>(stream));
 }
 
@@ -640,7 +680,8 @@ moe_status moe_layer_forward(const moe_shape* s, const void* x, const void* w_ga
     void* x_perm = w + L.x_perm;
     float* y_slot = reinterpret_cast<float*>(w + L.y_slot);
     MOE_TRY(run_router(*s, x, w_gate, idx, gw, logits, st));
-    MOE_TRY(run_permute(*s, idx, gw, x, counts, offsets, perm_token, slot_row, perm_w, x_perm, st));
+    MOE_TRY(run_permute(*s, idx, gw, x, counts, offsets, perm_token, slot_row, perm_w, x_perm, w + L.perm_ws,
+                        permute_ws_bytes(*s), st));
     bool combined = false;
     MOE_TRY(run_ffn(*s, x_perm, offsets, perm_w, w1, w3, w2, y_slot, w + L.ffn, L.f, st, slot_row, y, &combined));
     if (!combined) MOE_TRY(run_combine(*s, y_slot, slot_row, y, st));

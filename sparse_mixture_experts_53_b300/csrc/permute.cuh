@@ -150,3 +150,189 @@ __global__ void __launch_bounds__(256)
 }
 
 }  // namespace moe
+
+namespace moe {
+
+// ---------------------------------------------------------------------------
+// Grouping for large batches on many CTAs. The result is the same unique
+// stable order as permute_kernel (all sums are integer counts, so no order of
+// summation can change them).
+//   pass 1 (permute_count_kernel): CTA c counts the slots of its token chunk
+//            per expert -> chunk_counts[c][e];
+//   pass 2 (permute_place_kernel): CTA c adds up the counts of all chunks
+//            (totals -> offsets) and of the chunks before it (its base), ranks
+//            its tokens 64 at a time with warp ballots, writes slot_row,
+//            perm_token and perm_w, and copies each token row of x to the
+//            token's two rows of x_perm (one read, two writes).
+// ---------------------------------------------------------------------------
+constexpr int kPlaceThreads = 256;
+constexpr int kPlaceSub = 64;  // tokens ranked together (two warps)
+
+__global__ void __launch_bounds__(kPlaceThreads)
+    permute_count_kernel(const int32_t* __restrict__ topk_idx, int64_t T_tokens, int E, int64_t chunk,
+                         int32_t* __restrict__ chunk_counts) {
+    __shared__ int wc[kPlaceThreads / 32][kMaxExperts];
+    pdl_trigger();
+    pdl_wait();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t t0 = (int64_t)blockIdx.x * chunk;
+    const int64_t t1 = (t0 + chunk < T_tokens) ? t0 + chunk : T_tokens;
+    int cnt[kMaxExperts];
+#pragma unroll
+    for (int e = 0; e < kMaxExperts; ++e) cnt[e] = 0;
+    bool bad = false;
+    for (int64_t base = t0; base < t1; base += kPlaceThreads) {
+        const int64_t t = base + threadIdx.x;
+        int i0 = -1, i1 = -1;
+        if (t < t1) {
+            i0 = topk_idx[2 * t];
+            i1 = topk_idx[2 * t + 1];
+            bad |= !(i0 >= 0 && i0 < E) || !(i1 >= 0 && i1 < E);
+        }
+#pragma unroll
+        for (int e = 0; e < kMaxExperts; ++e)
+            cnt[e] += __popc(__ballot_sync(0xffffffffu, i0 == e)) + __popc(__ballot_sync(0xffffffffu, i1 == e));
+    }
+    if (bad) report_error(MOE_ERR_DEVICE_CHECK, K_PERMUTE, W_INDEX);
+    if (lane == 0) {
+#pragma unroll
+        for (int e = 0; e < kMaxExperts; ++e) wc[warp][e] = cnt[e];
+    }
+    __syncthreads();
+    if (threadIdx.x < kMaxExperts) {
+        int s = 0;
+        for (int w = 0; w < kPlaceThreads / 32; ++w) s += wc[w][threadIdx.x];
+        chunk_counts[(int64_t)blockIdx.x * kMaxExperts + threadIdx.x] = s;
+    }
+}
+
+__global__ void __launch_bounds__(kPlaceThreads)
+    permute_place_kernel(const int32_t* __restrict__ topk_idx, const float* __restrict__ topk_w, int64_t T_tokens,
+                         int E, int64_t chunk, int nchunks, const int32_t* __restrict__ chunk_counts,
+                         int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                         int32_t* __restrict__ perm_token, int32_t* __restrict__ slot_row,
+                         float* __restrict__ perm_w, const unsigned char* __restrict__ x, int64_t row_bytes,
+                         unsigned char* __restrict__ x_perm) {
+    __shared__ int red[kPlaceThreads / 32][2 * kMaxExperts];
+    __shared__ int base_s[kMaxExperts];
+    __shared__ int wtot[2][kMaxExperts];
+    __shared__ int rows_s[kPlaceSub][2];
+    pdl_trigger();
+    pdl_wait();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int me = blockIdx.x;
+
+    // totals of every chunk and of the chunks before this one (integer sums)
+    int tot[kMaxExperts], pre[kMaxExperts];
+#pragma unroll
+    for (int e = 0; e < kMaxExperts; ++e) tot[e] = pre[e] = 0;
+    for (int c = tid; c < nchunks; c += kPlaceThreads) {
+#pragma unroll
+        for (int e = 0; e < kMaxExperts; ++e) {
+            const int v = chunk_counts[(int64_t)c * kMaxExperts + e];
+            tot[e] += v;
+            pre[e] += (c < me) ? v : 0;
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < kMaxExperts; ++e) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            tot[e] += __shfl_xor_sync(0xffffffffu, tot[e], o);
+            pre[e] += __shfl_xor_sync(0xffffffffu, pre[e], o);
+        }
+    }
+    if (lane == 0) {
+#pragma unroll
+        for (int e = 0; e < kMaxExperts; ++e) {
+            red[warp][e] = tot[e];
+            red[warp][kMaxExperts + e] = pre[e];
+        }
+    }
+    __syncthreads();
+    if (tid == 0) {
+        int run = 0;
+        for (int e = 0; e < E; ++e) {
+            int te = 0, pe = 0;
+            for (int w = 0; w < kPlaceThreads / 32; ++w) {
+                te += red[w][e];
+                pe += red[w][kMaxExperts + e];
+            }
+            if (me == 0) {
+                counts[e] = te;
+                offsets[e] = run;
+            }
+            base_s[e] = run + pe;
+            run += te;
+        }
+        if (me == 0) offsets[E] = run;
+    }
+    __syncthreads();
+
+    const int64_t t0 = (int64_t)me * chunk;
+    const int64_t t1 = (t0 + chunk < T_tokens) ? t0 + chunk : T_tokens;
+    const int64_t c16 = row_bytes / 16;
+    for (int64_t sub = t0; sub < t1; sub += kPlaceSub) {
+        // ---- ranks of 64 tokens (warps 0 and 1), in token order
+        if (tid < kPlaceSub) {
+            const int64_t t = sub + tid;
+            int i0 = -1, i1 = -1;
+            if (t < t1) {
+                i0 = topk_idx[2 * t];
+                i1 = topk_idx[2 * t + 1];
+            }
+            const unsigned lt = (1u << lane) - 1u;
+            int r0 = -1, r1 = -1;
+#pragma unroll
+            for (int e = 0; e < kMaxExperts; ++e) {
+                const unsigned m0 = __ballot_sync(0xffffffffu, i0 == e);
+                const unsigned m1 = __ballot_sync(0xffffffffu, i1 == e);
+                const int before = __popc(m0 & lt) + __popc(m1 & lt);
+                if (lane == 0) wtot[warp][e] = __popc(m0) + __popc(m1);
+                if (i0 == e) r0 = before;
+                if (i1 == e) r1 = before + (i0 == e ? 1 : 0);
+            }
+            rows_s[tid][0] = r0;
+            rows_s[tid][1] = r1;
+        }
+        __syncthreads();
+        if (tid < kPlaceSub) {
+            const int64_t t = sub + tid;
+            if (t < t1) {
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int e = topk_idx[2 * t + j];
+                    int r = -1;
+                    if (e >= 0 && e < E) {
+                        r = base_s[e] + (warp == 1 ? wtot[0][e] : 0) + rows_s[tid][j];
+                        perm_token[r] = (int32_t)t;
+                        perm_w[r] = topk_w[2 * t + j];
+                    }
+                    slot_row[2 * t + j] = r;
+                    rows_s[tid][j] = r;
+                }
+            }
+        }
+        __syncthreads();
+        if (tid == 0) {
+            for (int e = 0; e < E; ++e) base_s[e] += wtot[0][e] + wtot[1][e];
+        }
+        // ---- copy each token row to its two rows (all 8 warps)
+        if (x != nullptr) {
+            const int64_t n_sub = ((t1 - sub) < kPlaceSub) ? (t1 - sub) : kPlaceSub;
+            for (int q = warp; q < n_sub; q += kPlaceThreads / 32) {
+                const int64_t t = sub + q;
+                const int ra = rows_s[q][0], rb = rows_s[q][1];
+                const uint4* src = reinterpret_cast<const uint4*>(x + t * row_bytes);
+                for (int64_t c = lane; c < c16; c += 32) {
+                    const uint4 v = src[c];
+                    if (ra >= 0) reinterpret_cast<uint4*>(x_perm + (int64_t)ra * row_bytes)[c] = v;
+                    if (rb >= 0) reinterpret_cast<uint4*>(x_perm + (int64_t)rb * row_bytes)[c] = v;
+                }
+            }
+        }
+        __syncthreads();
+    }
+}
+
+}  // namespace moe

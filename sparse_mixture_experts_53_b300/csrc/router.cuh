@@ -27,8 +27,7 @@ struct Vec16<float> {
 };
 
 template <typename T>
-__device__ __forceinline__ void load_vec(const T* p, float (&v)[Vec16<T>::N]) {
-    const uint4 raw = *reinterpret_cast<const uint4*>(p);
+__device__ __forceinline__ void unpack_vec(const uint4 raw, float (&v)[Vec16<T>::N]) {
     if constexpr (sizeof(T) == 2) {
         const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
 #pragma unroll
@@ -43,6 +42,13 @@ __device__ __forceinline__ void load_vec(const T* p, float (&v)[Vec16<T>::N]) {
         for (int i = 0; i < 4; ++i) v[i] = f[i];
     }
 }
+
+template <typename T>
+__device__ __forceinline__ void load_vec(const T* p, float (&v)[Vec16<T>::N]) {
+    unpack_vec<T>(*reinterpret_cast<const uint4*>(p), v);
+}
+
+constexpr int kRouterGroup = 8;  // 16-byte chunks of a token row each lane loads before computing
 
 // Top-2 selection and the two-way softmax from the E scores of one token.
 __device__ __forceinline__ void top2_softmax(const float (&acc)[kMaxExperts], int E, int32_t* idx, float* w) {
@@ -81,9 +87,23 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
         T* s = reinterpret_cast<T*>(router_smem);
         const int64_t n = (int64_t)E * d;
         if (vec) {
+            // several independent 16-byte loads in flight per thread
             const int64_t nv = n / Vec16<T>::N;
-            for (int64_t i = threadIdx.x; i < nv; i += blockDim.x)
-                reinterpret_cast<uint4*>(s)[i] = reinterpret_cast<const uint4*>(wg)[i];
+            const uint4* src = reinterpret_cast<const uint4*>(wg);
+            uint4* dst = reinterpret_cast<uint4*>(s);
+            for (int64_t i0 = threadIdx.x; i0 < nv; i0 += (int64_t)blockDim.x * kRouterGroup) {
+                uint4 tmp[kRouterGroup];
+#pragma unroll
+                for (int u = 0; u < kRouterGroup; ++u) {
+                    const int64_t i = i0 + (int64_t)u * blockDim.x;
+                    if (i < nv) tmp[u] = src[i];
+                }
+#pragma unroll
+                for (int u = 0; u < kRouterGroup; ++u) {
+                    const int64_t i = i0 + (int64_t)u * blockDim.x;
+                    if (i < nv) dst[i] = tmp[u];
+                }
+            }
         } else {
             for (int64_t i = threadIdx.x; i < n; i += blockDim.x) s[i] = wg[i];
         }
@@ -103,17 +123,32 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
 
         int j0 = 0;
         if (vec) {
+            // The lane's chunks are c = lane, lane + 32, ...; a group of them is
+            // loaded before any is used, so the row's loads overlap instead of
+            // waiting one by one. Chunks are still summed in increasing order.
             const int nchunks = d / V;
-            for (int c = lane; c < nchunks; c += 32) {
-                float xv[V];
-                load_vec<T>(xr + c * V, xv);
+            for (int c0 = lane; c0 < nchunks; c0 += 32 * kRouterGroup) {
+                uint4 xg[kRouterGroup];
 #pragma unroll
-                for (int e = 0; e < kMaxExperts; ++e) {
-                    if (e < E) {
-                        float wv[V];
-                        load_vec<T>(w + (int64_t)e * d + c * V, wv);
+                for (int u = 0; u < kRouterGroup; ++u) {
+                    const int c = c0 + 32 * u;
+                    if (c < nchunks) xg[u] = *reinterpret_cast<const uint4*>(xr + c * V);
+                }
 #pragma unroll
-                        for (int i = 0; i < V; ++i) acc[e] = fmaf(xv[i], wv[i], acc[e]);
+                for (int u = 0; u < kRouterGroup; ++u) {
+                    const int c = c0 + 32 * u;
+                    if (c < nchunks) {
+                        float xv[V];
+                        unpack_vec<T>(xg[u], xv);
+#pragma unroll
+                        for (int e = 0; e < kMaxExperts; ++e) {
+                            if (e < E) {
+                                float wv[V];
+                                load_vec<T>(w + (int64_t)e * d + c * V, wv);
+#pragma unroll
+                                for (int i = 0; i < V; ++i) acc[e] = fmaf(xv[i], wv[i], acc[e]);
+                            }
+                        }
                     }
                 }
             }

@@ -35,6 +35,7 @@ MOE_KNOB_TILE_CTAS = 5
 
 EXPORTED = (
     "moe_version", "moe_status_string", "moe_workspace_bytes", "moe_ffn_workspace_bytes",
+    "moe_permute_workspace_bytes",
     "moe_route_top2", "moe_permute", "moe_expert_ffn", "moe_combine", "moe_aux_stats",
     "moe_layer_forward", "moe_layer_forward_noalloc", "moe_get_device_status", "moe_set_wait_timeout_ns", "moe_set_knob",
     "moe_timing_enable", "moe_timing_read",
@@ -67,7 +68,8 @@ def _load() -> ctypes.CDLL:
         "moe_workspace_bytes": ([S], ctypes.c_size_t),
         "moe_ffn_workspace_bytes": ([S], ctypes.c_size_t),
         "moe_route_top2": ([S, P, P, P, P, P, P], I),
-        "moe_permute": ([S, P, P, P, P, P, P, P, P, P, P], I),
+        "moe_permute": ([S, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P], I),
+        "moe_permute_workspace_bytes": ([S], ctypes.c_size_t),
         "moe_expert_ffn": ([S, P, P, P, P, P, P, P, P, ctypes.c_size_t, P], I),
         "moe_combine": ([S, P, P, P, P], I),
         "moe_aux_stats": ([S, P, P, P, P, P, P], I),
@@ -148,10 +150,17 @@ def moe_route_top2(shape, x, w_gate, topk_idx, topk_w, logits=None, stream=None)
                                                 _ptr(topk_w), _ptr(logits), _stream(stream)))
 
 
-def moe_permute(shape, topk_idx, topk_w, x, counts, offsets, perm_token, slot_row, perm_w, x_perm, stream=None):
+def moe_permute_workspace_bytes(shape: moe_shape) -> int:
+    return int(lib.moe_permute_workspace_bytes(ctypes.byref(shape)))
+
+
+def moe_permute(shape, topk_idx, topk_w, x, counts, offsets, perm_token, slot_row, perm_w, x_perm, ws=None,
+                stream=None):
+    """ws: optional byte tensor of moe_permute_workspace_bytes(shape) (many-CTA grouping)."""
+    nbytes = ws.numel() * ws.element_size() if ws is not None else 0
     _check("moe_permute", lib.moe_permute(ctypes.byref(shape), _ptr(topk_idx), _ptr(topk_w), _ptr(x),
                                           _ptr(counts), _ptr(offsets), _ptr(perm_token), _ptr(slot_row),
-                                          _ptr(perm_w), _ptr(x_perm), _stream(stream)))
+                                          _ptr(perm_w), _ptr(x_perm), _ptr(ws), nbytes, _stream(stream)))
 
 
 def moe_expert_ffn(shape, x_perm, offsets, perm_w, w1, w3, w2, y_slot, ws, stream=None):

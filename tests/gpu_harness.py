@@ -40,9 +40,10 @@ def run_staged(layer, dev=None, stream=None):
         y=torch.zeros((T, d), dtype=dev["x"].dtype, device=c),
         f=torch.zeros(E, **f32), P=torch.zeros(E, **f32), l_aux=torch.zeros(1, **f32))
     ws = moe.workspace(s, ffn_only=True)
+    pws = torch.empty(max(16, moe.moe_permute_workspace_bytes(s)), dtype=torch.uint8, device=c)
     moe.moe_route_top2(s, dev["x"], dev["w_gate"], out["idx"], out["w"], out["logits"], stream)
     moe.moe_permute(s, out["idx"], out["w"], dev["x"], out["counts"], out["offsets"], out["perm_token"],
-                    out["slot_row"], out["perm_w"], out["x_perm"], stream)
+                    out["slot_row"], out["perm_w"], out["x_perm"], pws, stream)
     moe.moe_expert_ffn(s, out["x_perm"], out["offsets"], out["perm_w"], dev["w1"], dev["w3"], dev["w2"],
                        out["y_slot"], ws, stream)
     moe.moe_combine(s, out["y_slot"], out["slot_row"], out["y"], stream)

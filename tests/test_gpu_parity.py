@@ -329,3 +329,57 @@ def test_single_and_paired_token_tiles_agree():
         assert_status_ok()
     a, b = outs[0]["y_slot"].numpy(), outs[1]["y_slot"].numpy()
     assert np.max(np.abs(a - b)) <= 1e-3 * np.max(np.abs(a))
+
+
+def _permute_outputs(s, idx, w, x, ws):
+    T, d = x.shape
+    c = "cuda"
+    out = dict(counts=torch.full((8,), -5, dtype=torch.int32, device=c),
+               offsets=torch.full((9,), -5, dtype=torch.int32, device=c),
+               perm_token=torch.full((2 * T,), -5, dtype=torch.int32, device=c),
+               slot_row=torch.full((T, 2), -5, dtype=torch.int32, device=c),
+               perm_w=torch.full((2 * T,), -5.0, device=c),
+               x_perm=torch.zeros((2 * T, d), dtype=x.dtype, device=c))
+    moe.moe_permute(s, idx, w, x, out["counts"], out["offsets"], out["perm_token"], out["slot_row"],
+                    out["perm_w"], out["x_perm"], ws)
+    torch.cuda.synchronize()
+    return out
+
+
+@pytest.mark.parametrize("T,dtype,bad", [(2048, "bf16", False), (5000, "bf16", False), (4500, "f32", False),
+                                         (9000, "bf16", True)])
+def test_many_cta_grouping_equals_single_cta(T, dtype, bad):
+    """Per-chunk counts + ranks on many CTAs give the unique stable order of the one-CTA kernel."""
+    d = 256 if dtype == "bf16" else 37  # 37 fp32 = 148-byte rows: the separate row gather
+    L = make_layer(T, d, 128, 8, dtype, seed=T)
+    x = L.x.cuda()
+    s = moe.make_shape(T, d, 128, moe.MOE_BF16 if dtype == "bf16" else moe.MOE_F32)
+    rng = np.random.default_rng(T)
+    sel = np.stack([rng.choice(8, size=2, replace=False) for _ in range(T)]).astype(np.int32)
+    # skew: expert 3 takes many slots, expert 6 none
+    sel[: T // 3, 0] = 3
+    sel[: T // 3, 1] = np.where(sel[: T // 3, 1] == 3, 5, sel[: T // 3, 1])
+    sel[sel == 6] = 7
+    sel[sel[:, 0] == sel[:, 1], 1] = 0
+    sel[sel[:, 0] == sel[:, 1], 1] = 1
+    if bad:
+        sel[T // 2, 1] = 11
+    idx = torch.from_numpy(sel).cuda()
+    w = torch.rand((T, 2), device="cuda")
+    ws = torch.empty(moe.moe_permute_workspace_bytes(s), dtype=torch.uint8, device="cuda")
+    one = _permute_outputs(s, idx, w, x, None)
+    code_one, _ = moe.moe_get_device_status()
+    many = _permute_outputs(s, idx, w, x, ws)
+    code_many, _ = moe.moe_get_device_status()
+    for k in one:
+        assert torch.equal(one[k], many[k]), k
+    if bad:
+        assert code_one == code_many == moe.MOE_ERR_DEVICE_CHECK
+        assert int(many["slot_row"][T // 2, 1]) == -1
+    else:
+        assert code_one == code_many == moe.MOE_OK
+        assert int(many["counts"][6]) == 0
+        ref = oracle.permute(sel.astype(np.int64), w.cpu().numpy(), 8)
+        for k in ("counts", "offsets", "perm_token", "slot_row"):
+            assert np.array_equal(many[k].cpu().numpy().astype(np.int64), ref[k]), k
+        assert torch.equal(many["x_perm"].cpu(), L.x[torch.from_numpy(ref["perm_token"])])
