@@ -170,6 +170,50 @@ def _dist_env():
     return rank, world, local
 
 
+class Ranks:
+    """The replicas of a multi-GPU run: one process per GPU, no exchange on the data path.
+
+    Only two collectives exist, both outside the layer: a barrier around each
+    timed region and the max over ranks of the measured times (the slowest
+    replica sets the job's time). With one rank both are local no-ops.
+    """
+
+    def __init__(self, rank: int, world: int, local: int, backend: str = "nccl"):
+        self.rank, self.world, self.backend = rank, world, backend
+        self.dist = None
+        if world > 1:
+            import torch
+            import torch.distributed as dist
+            kw = {"device_id": torch.device("cuda", local)} if backend == "nccl" else {}
+            dist.init_process_group(backend, rank=rank, world_size=world, **kw)
+            self.dist = dist
+
+    def _device(self):
+        return "cuda" if self.backend == "nccl" else "cpu"
+
+    def barrier(self) -> None:
+        if self.dist is not None:
+            self.dist.barrier()
+
+    def max(self, values: list[float]) -> list[float]:
+        if self.dist is None:
+            return [float(v) for v in values]
+        import torch
+        t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=self._device())
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return [float(v) for v in t.cpu().tolist()]
+
+    def close(self) -> None:
+        if self.dist is not None:
+            self.dist.destroy_process_group()
+            self.dist = None
+
+
+def throughput(tokens_per_rank: int, world: int, ms_max: float) -> float:
+    """Whole-job tokens/s: the tokens of every replica over the slowest replica's step time."""
+    return round(tokens_per_rank * world / (ms_max * 1e-3), 1)
+
+
 def _algorithmic(cfg: dict, counts) -> dict:
     """Work of one step from the per-expert row counts (the router's decision)."""
     T, d, F = cfg["T"], cfg["d"], cfg["ffn"]
@@ -191,14 +235,10 @@ def run_ours(args, rank, world, local) -> dict | None:
     torch.cuda.set_device(local)
     moe.moe_set_knob(moe.MOE_KNOB_PDL, args.pdl)
     moe.moe_set_knob(moe.MOE_KNOB_TILE_CTAS, args.tile_ctas)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    ranks = Ranks(rank, world, local, backend="nccl")
 
     def barrier():
-        if dist is not None:
-            dist.barrier()
+        ranks.barrier()
         torch.cuda.synchronize()
 
     k = args.config
@@ -272,14 +312,10 @@ def run_ours(args, rank, world, local) -> dict | None:
     moe.moe_route_top2(shape, x, wg, idx, gw)
     counts = torch.bincount(idx.flatten().long(), minlength=8).cpu().tolist()
 
-    if dist is not None:
-        t = torch.tensor([ms, e2e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, e2e_ms = float(t[0]), float(t[1])
+    ms, e2e_ms = ranks.max([ms, e2e_ms])
 
     work = _algorithmic(cfg, counts)
     peaks = _peaks()
-    tokens = cfg["T"] * world
     launches_per_step = sum(v[0] for v in kern.values()) / max(1, args.steps)
     streaming = cfg["T"] <= 64
     if streaming:
@@ -304,7 +340,7 @@ def run_ours(args, rank, world, local) -> dict | None:
                 "traffic": _profile_traffic(dom, cfg["name"])}
     step_s = ms * 1e-3
     line = {
-        "metric": METRIC, "value": round(tokens / step_s, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "metric": METRIC, "value": throughput(cfg["T"], world, ms), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded Mixtral-shape tensors, random init)",
         "config": {"workload": cfg["name"], "T": cfg["T"], "d": cfg["d"], "ffn": cfg["ffn"], "E": cfg["E"], "k": 2,
@@ -321,13 +357,12 @@ def run_ours(args, rank, world, local) -> dict | None:
         "roofline": roof,
         "kernels_ms_per_step": {n: round(v[1] / max(1, args.steps), 5) for n, v in kern.items()},
         "gpu_launches": int(round(launches_per_step * args.steps)),
-        "e2e": {"value": round(tokens / (e2e_ms * 1e-3), 1), "unit": UNIT,
+        "e2e": {"value": throughput(cfg["T"], world, e2e_ms), "unit": UNIT,
                 "h2d_bytes_per_step": int(L.x.numel() * L.x.element_size()),
                 "d2h_bytes_per_step": int(L.x.numel() * L.x.element_size()), "ms_per_step": round(e2e_ms, 5)},
         "clocks": sampler.summary(),
     }
-    if dist is not None:
-        dist.destroy_process_group()
+    ranks.close()
     return line if rank == 0 else None
 
 
