@@ -768,8 +768,23 @@ __global__ void __launch_bounds__(256)
     const int64_t n = R * F;
     const int64_t plane = R * F;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        // groups of four slices are loaded before they are added (in slice order)
         float u = 0.f, v = 0.f;
-        for (int s = 0; s < S; ++s) {
+        int s = 0;
+        for (; s + 4 <= S; s += 4) {
+            float pu[4], pv[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                pu[q] = part[(2 * (int64_t)(s + q)) * plane + i];
+                pv[q] = part[(2 * (int64_t)(s + q) + 1) * plane + i];
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                u += pu[q];
+                v += pv[q];
+            }
+        }
+        for (; s < S; ++s) {
             u += part[(2 * (int64_t)s) * plane + i];
             v += part[(2 * (int64_t)s + 1) * plane + i];
         }
@@ -813,8 +828,18 @@ __global__ void __launch_bounds__(256)
             const int r = slot_row[2 * t + j];
             float v = 0.f;
             if (r >= 0) {
+                // groups of eight slices are loaded before they are added (in slice order)
+                const float* p = part + (int64_t)r * d + c;
                 float acc = 0.f;
-                for (int s = 0; s < S; ++s) acc += part[(int64_t)s * plane + (int64_t)r * d + c];
+                int s = 0;
+                for (; s + 8 <= S; s += 8) {
+                    float pv[8];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) pv[q] = p[(int64_t)(s + q) * plane];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) acc += pv[q];
+                }
+                for (; s < S; ++s) acc += p[(int64_t)s * plane];
                 v = perm_w[r] * acc;
             }
             ab[j] = v;

@@ -340,8 +340,19 @@ moe_status run_permute(const moe_shape& s, const int32_t* idx, const float* w, c
                            static_cast<unsigned char*>(x_perm));
         }));
         if (rows16) return MOE_OK;
+    } else if (s.T > 0 && R <= kSmallPermuteMaxSlots && rows16) {
+        // small batch: every CTA ranks all slots, CTA 0 writes the grouping,
+        // the grid copies the rows
+        const int64_t chunks = R * (row_bytes / 16);
+        const int grid = (int)std::max<int64_t>(
+            1, std::min<int64_t>((chunks + 2 * kSmallPermuteThreads - 1) / (2 * kSmallPermuteThreads), sm_count()));
+        return launch("permute", st, [&] {
+            return klaunch(permute_small_kernel, grid, kSmallPermuteThreads, 0, st, idx, w, s.T, s.E, counts,
+                           offsets, perm_token, slot_row, perm_w, static_cast<const unsigned char*>(x), row_bytes,
+                           static_cast<unsigned char*>(x_perm));
+        });
     } else {
-        // small batch: one CTA; it also copies the rows when they are few
+        // one CTA; it also copies the rows when they are few
         const bool fused = s.T > 0 && rows16 && R * row_bytes <= kFusedGatherBytes;
         MOE_TRY(launch("permute", st, [&] {
             return klaunch(permute_kernel, 1, kPermuteThreads, 0, st, idx, w, s.T, s.E, counts, offsets, perm_token,

@@ -125,6 +125,104 @@ __global__ void __launch_bounds__(kPermuteThreads)
     }
 }
 
+// ---------------------------------------------------------------------------
+// Grouping of small batches (2T <= 512 slots) on several CTAs. Every CTA
+// ranks all the slots itself (16 warps, one slot per thread, warp ballots per
+// expert, integer counts: the same unique stable order as permute_kernel), CTA
+// 0 writes the grouping, and every CTA copies its share of the token rows into
+// x_perm. A single CTA copying all the rows waits on one memory round trip per
+// handful of rows; spread over the grid the copies are in flight together.
+// ---------------------------------------------------------------------------
+constexpr int kSmallPermuteThreads = 512;
+constexpr int kSmallPermuteMaxSlots = kSmallPermuteThreads;
+
+__global__ void __launch_bounds__(kSmallPermuteThreads)
+    permute_small_kernel(const int32_t* __restrict__ topk_idx, const float* __restrict__ topk_w, int64_t T_tokens,
+                         int E, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                         int32_t* __restrict__ perm_token, int32_t* __restrict__ slot_row,
+                         float* __restrict__ perm_w, const unsigned char* __restrict__ x, int64_t row_bytes,
+                         unsigned char* __restrict__ x_perm) {
+    constexpr int W = kSmallPermuteThreads / 32;
+    __shared__ int wcnt[W][kMaxExperts];
+    __shared__ int s_off[kMaxExperts + 1];
+    __shared__ int row_token[kSmallPermuteMaxSlots];
+    pdl_trigger();
+    pdl_wait();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int R = (int)(2 * T_tokens);
+    const bool lead = blockIdx.x == 0;
+    int e = -1;
+    if (tid < R) e = topk_idx[tid];
+    const bool valid = e >= 0 && e < E;
+    if (tid < R && !valid && lead) report_error(MOE_ERR_DEVICE_CHECK, K_PERMUTE, W_INDEX);
+    const unsigned lt = (1u << lane) - 1u;
+    int before = 0;
+#pragma unroll
+    for (int q = 0; q < kMaxExperts; ++q) {
+        const unsigned m = __ballot_sync(0xffffffffu, valid && e == q);
+        if (e == q) before = __popc(m & lt);
+        if (lane == 0) wcnt[warp][q] = __popc(m);
+    }
+    __syncthreads();
+    if (tid < kMaxExperts) {
+        // exclusive prefix over warps (in place); the total goes to s_off
+        int run = 0;
+        for (int w = 0; w < W; ++w) {
+            const int c = wcnt[w][tid];
+            wcnt[w][tid] = run;
+            run += c;
+        }
+        s_off[tid + 1] = run;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        s_off[0] = 0;
+        for (int q = 0; q < E; ++q) {
+            if (lead) counts[q] = s_off[q + 1];
+            s_off[q + 1] += s_off[q];
+        }
+        if (lead)
+            for (int q = 0; q <= E; ++q) offsets[q] = s_off[q];
+    }
+    __syncthreads();
+    if (tid < R) {
+        const int r = valid ? s_off[e] + wcnt[warp][e] + before : -1;
+        if (valid) row_token[r] = tid >> 1;
+        if (lead) {
+            slot_row[tid] = r;
+            if (valid) {
+                perm_token[r] = tid >> 1;
+                perm_w[r] = topk_w[tid];
+            }
+        }
+    }
+    __syncthreads();
+    // rows [0, s_off[E]) of x_perm, 16-byte chunks spread over the grid, four
+    // loads in flight per thread before their stores
+    const int64_t c16 = row_bytes / 16;
+    const int64_t n = (int64_t)s_off[E] * c16;
+    const int64_t stride = (int64_t)gridDim.x * kSmallPermuteThreads;
+    for (int64_t i0 = (int64_t)blockIdx.x * kSmallPermuteThreads + tid; i0 < n; i0 += 4 * stride) {
+        uint4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int64_t i = i0 + u * stride;
+            if (i < n) {
+                const int64_t r = i / c16, c = i - r * c16;
+                v[u] = reinterpret_cast<const uint4*>(x + (int64_t)row_token[r] * row_bytes)[c];
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int64_t i = i0 + u * stride;
+            if (i < n) {
+                const int64_t r = i / c16, c = i - r * c16;
+                reinterpret_cast<uint4*>(x_perm + r * row_bytes)[c] = v[u];
+            }
+        }
+    }
+}
+
 // x_perm[r] = x[perm_token[r]]: one row per warp-group, 16-byte copies when
 // the row size allows, 4-byte copies otherwise.
 __global__ void __launch_bounds__(256)

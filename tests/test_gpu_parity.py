@@ -383,3 +383,35 @@ def test_many_cta_grouping_equals_single_cta(T, dtype, bad):
         for k in ("counts", "offsets", "perm_token", "slot_row"):
             assert np.array_equal(many[k].cpu().numpy().astype(np.int64), ref[k]), k
         assert torch.equal(many["x_perm"].cpu(), L.x[torch.from_numpy(ref["perm_token"])])
+
+
+@pytest.mark.parametrize("T,bad", [(1, False), (7, False), (64, False), (256, False), (100, True)])
+def test_small_batch_grouping_matches_oracle(T, bad):
+    """Slots ranked on every CTA of the small-batch grouping: the oracle's unique stable order, bit for bit."""
+    d = 512
+    L = make_layer(T, d, 128, 8, "bf16", seed=400 + T)
+    x = L.x.cuda()
+    s = moe.make_shape(T, d, 128, moe.MOE_BF16)
+    rng = np.random.default_rng(T)
+    sel = np.stack([rng.choice(8, size=2, replace=False) for _ in range(T)]).astype(np.int32)
+    sel[sel == 6] = 7  # expert 6 empty
+    sel[sel[:, 0] == sel[:, 1], 1] = 0
+    sel[sel[:, 0] == sel[:, 1], 1] = 1
+    if bad:
+        sel[T // 3, 0] = -2
+    idx = torch.from_numpy(sel).cuda()
+    w = torch.rand((T, 2), device="cuda")
+    out = _permute_outputs(s, idx, w, x, None)
+    code, _ = moe.moe_get_device_status()
+    ok = (sel >= 0) & (sel < 8)
+    ref = oracle.permute(np.where(ok, sel, 0).astype(np.int64), w.cpu().numpy(), 8)
+    if bad:
+        assert code == moe.MOE_ERR_DEVICE_CHECK
+        assert int(out["slot_row"][T // 3, 0]) == -1
+        assert int(out["offsets"][8]) == 2 * T - 1
+        return
+    assert code == moe.MOE_OK
+    for k in ("counts", "offsets", "perm_token", "slot_row"):
+        assert np.array_equal(out[k].cpu().numpy().astype(np.int64), ref[k]), k
+    assert np.array_equal(out["perm_w"].cpu().numpy(), ref["perm_w"].astype(np.float32))
+    assert torch.equal(out["x_perm"].cpu(), L.x[torch.from_numpy(ref["perm_token"])])
