@@ -138,14 +138,16 @@ class ClockSampler:
                 "reasons": sorted(self.reasons - {"gpu_idle"}), "samples": len(self.samples)}
 
 
-KERNEL_SOURCES = ("ffn_tc.cuh", "common.cuh")
+CSRC = ROOT / "sparse_mixture_experts_53_b300" / "csrc"
 
 
 def _source_digest() -> str:
-    """Digest of the files that define the tensor-core kernels (ncu figures go stale when they change)."""
+    """Digest of the kernels and their launch code (ncu figures go stale when any of it changes)."""
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES:
-        h.update((ROOT / "sparse_mixture_experts_53_b300" / "csrc" / name).read_bytes())
+    for f in sorted(CSRC.iterdir()):
+        if f.suffix in (".cu", ".cuh"):
+            h.update(f.name.encode())
+            h.update(f.read_bytes())
     return h.hexdigest()[:16]
 
 
