@@ -17,3 +17,9 @@ from .moe_oracle import (  # noqa: F401
     aux_stats,
     mixtral_param_counts,
 )
+from .moe_backward import (  # noqa: F401
+    silu_grad,
+    topk_softmax_backward,
+    aux_score_grad,
+    layer_backward,
+)
