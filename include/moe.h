@@ -187,6 +187,57 @@ moe_status moe_layer_forward_noalloc(const moe_shape* s, const void* x, const vo
                                      const void* w1, const void* w3, const void* w2, void* y,
                                      void* stream);
 
+/* ---------------------------------------------------------------- training
+ * The pages train the router and the experts end to end and add the
+ * load-balancing term to the loss (tokentrails.org "Mixtral", step "Load
+ * balancing"; lecture, router walkthrough: the router is a learned linear
+ * layer). They print no backward pass; these calls give, for an upstream
+ * gradient dy, the gradients of
+ *     L = sum_t <dy_t, y_t> + aux_coef * L_aux
+ * by the chain rule through the forward definition: the top-2 choice and the
+ * routed counts f_i are piecewise constant (not differentiated), the two kept
+ * weights are the softmax of the two kept scores, L_aux reaches the scores
+ * through P_i (the full softmax), SiLU'(z) = s (1 + z (1 - s)).
+ * Training needs shape->dtype == MOE_BF16 and d, ffn multiples of 256. */
+
+/* Bytes of the state moe_layer_forward_train keeps for moe_layer_backward
+ * (0 on an unsupported shape): the forward workspace plus u = W1 x and
+ * v = W3 x of every slot row in bf16. */
+size_t moe_train_state_bytes(const moe_shape* s);
+
+/* Bytes of the workspace of moe_layer_backward (0 on an unsupported shape):
+ * transposed weights, per-slot gradients and token-transposed activations
+ * (about 4.7 GB of transposed weights plus 130 KB per token at the Mixtral
+ * shape). */
+size_t moe_backward_workspace_bytes(const moe_shape* s);
+
+/* Forward pass that keeps its intermediates for the backward pass.
+ *   Same arguments and results as moe_layer_forward (y bit-identical for the
+ *   same inputs), with the workspace replaced by
+ *   state / state_bytes: at least moe_train_state_bytes(s) bytes of device
+ *     memory, owned by the caller and passed unchanged to moe_layer_backward. */
+moe_status moe_layer_forward_train(const moe_shape* s, const void* x, const void* w_gate,
+                                   const void* w1, const void* w3, const void* w2, void* y,
+                                   float* aux_f, float* aux_P, float* aux_l_aux,
+                                   void* state, size_t state_bytes, void* stream);
+
+/* Backward pass for an upstream gradient dy [T][d] (bf16).
+ *   x, w_gate, w1, w3, w2   the forward's inputs (unchanged since the forward)
+ *   aux_coef                weight of L_aux in the loss (0 = none)
+ *   state / state_bytes     from moe_layer_forward_train on the same inputs
+ *   dx       [T][d]        bf16 out
+ *   dw_gate  [E][d]        float out
+ *   dw1, dw3 [E][ffn][d]   float out
+ *   dw2      [E][d][ffn]   float out
+ *   ws / ws_bytes          at least moe_backward_workspace_bytes(s) bytes
+ * Gradients are written, not accumulated; an expert no token selected gets
+ * zeros. All sums run in a fixed order: results are deterministic. */
+moe_status moe_layer_backward(const moe_shape* s, const void* x, const void* w_gate,
+                              const void* w1, const void* w3, const void* w2, const void* dy,
+                              float aux_coef, const void* state, size_t state_bytes, void* dx,
+                              float* dw_gate, float* dw1, float* dw3, float* dw2,
+                              void* ws, size_t ws_bytes, void* stream);
+
 /* Synchronises the current device, then reports and clears its status word.
  * *code receives MOE_OK or the first device-side error since the last read;
  * *detail (nullable) receives a kernel/where code for diagnostics. Returns

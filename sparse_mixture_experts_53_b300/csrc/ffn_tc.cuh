@@ -90,14 +90,25 @@ __device__ __forceinline__ void raise_abort(TcControl* c, int kernel, int where)
 
 struct TileArgs {
     const int32_t* offsets;  // [E+1]
-    const float* perm_w;     // [R] (down only)
-    void* out;               // up: H bf16 [R][ldo]; down: y_slot fp32 [R][ldo]
+    const float* perm_w;     // [R] (down only; nullptr = no scale)
+    void* out;               // up: H bf16 [R][ldo]; down: y_slot fp32 [R][ldo]; see the backward modes
     int E;
     int K;          // reduction length (d for up, ffn for down)
     int n_tiles_n;  // column tiles per expert
     int w_rows;     // rows of one expert in the weight maps (ffn for up, d for down)
     int ldo;        // output row stride in elements
     uint64_t timeout_ns;
+    // training forward (up): also keep u = W1 x and v = W3 x in bf16 [R][ldo] (nullable)
+    __nv_bfloat16* u_out;
+    __nv_bfloat16* v_out;
+    // backward of the SwiGLU (pair kernel, PM_BWD_DH): the kept u and v
+    const __nv_bfloat16* u_in;
+    const __nv_bfloat16* v_in;
+    // weight gradients (pair kernel, PM_WGRAD): rows >= split_rows go to out2
+    float* out2;
+    int m_tiles;           // 256-row tiles of the gradient per expert
+    int split_rows;        // rows of the first gradient matrix
+    int64_t out_estride;   // elements per expert in each gradient matrix
 };
 
 // Epilogue of one token tile for one thread (one row): reads the row's 256
@@ -127,10 +138,24 @@ __device__ __forceinline__ void tile_epilogue(uint32_t taddr, bool valid, int64_
                 uint4* dst = reinterpret_cast<uint4*>(out + j);
                 dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
                 dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                if (args.u_out != nullptr) {
+                    // training forward: keep u and v (bf16) for the backward pass
+                    const int64_t at = r * args.ldo + nt * kTileM + j;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) pk[i] = pack_bf16x2(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1]));
+                    uint4* du = reinterpret_cast<uint4*>(args.u_out + at);
+                    du[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    du[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+                    uint4* dv = reinterpret_cast<uint4*>(args.v_out + at);
+                    dv[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    dv[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                }
             }
         }
     } else {
-        const float pw = valid ? args.perm_w[r] : 0.f;
+        const float pw = valid ? (args.perm_w != nullptr ? args.perm_w[r] : 1.0f) : 0.f;
         float* out = reinterpret_cast<float*>(args.out) + r * args.ldo + nt * kTileN;
 #pragma unroll 1
         for (int j = 0; j < kTileN; j += 16) {
@@ -352,10 +377,107 @@ constexpr uint32_t kPairHalfBytes = 128 * kBK * 2;          // 16 KB: one CTA's 
 constexpr uint32_t kPairStageBytes = 2 * kPairHalfBytes;     // 32 KB per CTA and stage
 constexpr size_t kPairSmemBytes = 1024 + (size_t)kPairStages * kPairStageBytes + sizeof(TcControl);
 
-template <bool UP>
+// What a CTA-pair tile kernel computes (the tile loop, the TMA ring and the
+// MMA issue are shared; the operands' rows, the K range and the epilogue
+// differ):
+//   PM_UP      H = SiLU(X W1^T) * (X W3^T) per expert (forward)
+//   PM_DOWN    y_slot = perm_w * (H W2^T) per expert (forward)
+//   PM_BWD_DH  dh = dYs W2 per expert; the epilogue applies the SwiGLU
+//              backward with the kept u, v: du = dh v SiLU'(u), dv = dh SiLU(u),
+//              written side by side as dUV [R][2 ffn] (bf16)
+//   PM_BWD_DX  dXp = dUV [W1; W3] per expert, fp32 (B = the transposed
+//              weights, K = 2 ffn)
+//   PM_WGRAD   weight gradients, fp32: per expert, rows x columns = A^T B over
+//              the expert's tokens, with A and B token-transposed activations
+//              whose expert groups start at multiples of 64 tokens (K range
+//              per expert, zero padded); an expert with no tokens gets zeros
+enum PairMode : int { PM_UP = 0, PM_DOWN = 1, PM_BWD_DH = 2, PM_BWD_DX = 3, PM_WGRAD = 4 };
+
+// Start of expert e's K range in the token-transposed layout: groups padded
+// to multiples of 64 tokens, in expert order.
+__device__ __forceinline__ int wgrad_kofs(const int* cnt, int e) {
+    int k = 0;
+    for (int q = 0; q < e; ++q) k += (cnt[q] + kBK - 1) / kBK * kBK;
+    return k;
+}
+
+// Epilogue of one row of a PM_BWD_DH tile: 256 columns f of dh, the kept u
+// and v of the same row and columns, du and dv out in bf16.
+__device__ __forceinline__ void bwd_dh_epilogue(uint32_t taddr, bool valid, int64_t r, int nt, const TileArgs& args) {
+    const int F = args.w_rows;
+    const int64_t col0 = (int64_t)nt * kTileN;
+    const __nv_bfloat16* urow = args.u_in + r * F + col0;
+    const __nv_bfloat16* vrow = args.v_in + r * F + col0;
+    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(args.out) + r * args.ldo + col0;
+#pragma unroll 1
+    for (int j = 0; j < kTileN; j += 16) {
+        uint32_t a[16];
+        tmem_ld16(taddr + j, a);
+        uint4 uraw[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+        uint4 vraw[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+        if (valid) {
+            uraw[0] = reinterpret_cast<const uint4*>(urow + j)[0];
+            uraw[1] = reinterpret_cast<const uint4*>(urow + j)[1];
+            vraw[0] = reinterpret_cast<const uint4*>(vrow + j)[0];
+            vraw[1] = reinterpret_cast<const uint4*>(vrow + j)[1];
+        }
+        tmem_wait_ld();
+        const __nv_bfloat16* uu = reinterpret_cast<const __nv_bfloat16*>(uraw);
+        const __nv_bfloat16* vv = reinterpret_cast<const __nv_bfloat16*>(vraw);
+        uint32_t pdu[8], pdv[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            float du2[2], dv2[2];
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const float dh = __uint_as_float(a[2 * i + q]);
+                const float u = __bfloat162float(uu[2 * i + q]);
+                const float v = __bfloat162float(vv[2 * i + q]);
+                const float sg = 1.0f / (1.0f + expf(-u));
+                du2[q] = dh * v * (sg * (1.0f + u * (1.0f - sg)));
+                dv2[q] = dh * (u * sg);
+            }
+            pdu[i] = pack_bf16x2(du2[0], du2[1]);
+            pdv[i] = pack_bf16x2(dv2[0], dv2[1]);
+        }
+        if (valid) {
+            uint4* d0 = reinterpret_cast<uint4*>(out + j);
+            d0[0] = make_uint4(pdu[0], pdu[1], pdu[2], pdu[3]);
+            d0[1] = make_uint4(pdu[4], pdu[5], pdu[6], pdu[7]);
+            uint4* d1 = reinterpret_cast<uint4*>(out + F + j);
+            d1[0] = make_uint4(pdv[0], pdv[1], pdv[2], pdv[3]);
+            d1[1] = make_uint4(pdv[4], pdv[5], pdv[6], pdv[7]);
+        }
+    }
+}
+
+// Epilogue of one row of a PM_WGRAD tile: 256 fp32 columns of the gradient
+// (zeros when the expert had no tokens, i.e. no MMA wrote the accumulator).
+__device__ __forceinline__ void wgrad_epilogue(uint32_t taddr, bool any_k, int e, int row, int nt,
+                                               const TileArgs& args) {
+    float* base = row < args.split_rows ? reinterpret_cast<float*>(args.out) : args.out2;
+    const int rr = row < args.split_rows ? row : row - args.split_rows;
+    float* out = base + (int64_t)e * args.out_estride + (int64_t)rr * args.ldo + (int64_t)nt * kTileN;
+#pragma unroll 1
+    for (int j = 0; j < kTileN; j += 16) {
+        uint32_t a[16];
+        tmem_ld16(taddr + j, a);
+        tmem_wait_ld();
+        float4* dst = reinterpret_cast<float4*>(out + j);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            dst[i] = any_k ? make_float4(__uint_as_float(a[4 * i]), __uint_as_float(a[4 * i + 1]),
+                                         __uint_as_float(a[4 * i + 2]), __uint_as_float(a[4 * i + 3]))
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+}
+
+template <int MODE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
     tile_pair_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b0,
                           const __grid_constant__ CUtensorMap map_b1, const TileArgs args) {
+    constexpr bool UP = MODE == PM_UP;
+    constexpr bool WG = MODE == PM_WGRAD;
     extern __shared__ unsigned char tc_smem_raw[];
     unsigned char* smem = align1024(tc_smem_raw);
     TcControl* ctl = reinterpret_cast<TcControl*>(smem + (size_t)kPairStages * kPairStageBytes);
@@ -399,7 +521,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
         for (int e = 0; e < args.E; ++e) {
             const int c = ctl->off[e + 1] - ctl->off[e];
             ctl->cnt[e] = c;
-            ctl->mt[e] = (c + kPairM - 1) / kPairM;
+            // token modes: 256-token row tiles; weight gradients: fixed row tiles, every expert
+            ctl->mt[e] = WG ? args.m_tiles : (c + kPairM - 1) / kPairM;
             ctl->base[e] = tiles;
             tiles += ctl->mt[e] * args.n_tiles_n;
         }
@@ -423,10 +546,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
         nt = rem / ctl->mt[e];
         mt = rem - nt * ctl->mt[e];
     };
+    // K steps of a tile: fixed, or the expert's padded token count
+    auto ksteps = [&](int e) { return WG ? (ctl->cnt[e] + kBK - 1) / kBK : KB; };
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer (both CTAs)
         if (lane == 0) {
+            // token rows are re-read for every column tile: keep them in L2;
+            // a weight tile is shared by the pairs working on the expert's
+            // row tiles at the same time: normal priority (and both operands
+            // of the weight gradients, which together exceed L2)
             const uint64_t pol_act = policy_evict_last();
             const uint64_t pol_w = policy_evict_normal();
             const CUtensorMap* map_b = (UP && rank == 1) ? &map_b1 : &map_b0;
@@ -436,9 +565,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
             for (int tile = pair; ok && tile < n_work; tile += n_pairs) {
                 int e, nt, mt;
                 decode(tile, e, nt, mt);
-                const int arow = ctl->off[e] + mt * kPairM + 128 * (int)rank;
-                const int brow = UP ? e * args.w_rows + nt * kTileM : e * args.w_rows + nt * kTileN + 128 * (int)rank;
-                for (int kb = 0; kb < KB; ++kb) {
+                int arow, brow, kx0 = 0;
+                if (WG) {
+                    arow = mt * kPairM + 128 * (int)rank;
+                    brow = nt * kTileN + 128 * (int)rank;
+                    kx0 = wgrad_kofs(ctl->cnt, e);
+                } else {
+                    arow = ctl->off[e] + mt * kPairM + 128 * (int)rank;
+                    brow = UP ? e * args.w_rows + nt * kTileM : e * args.w_rows + nt * kTileN + 128 * (int)rank;
+                }
+                const int nk = ksteps(e);
+                for (int kb = 0; kb < nk; ++kb) {
                     if (!mbar_wait(smem_u32(&ctl->empty[s]), ph ^ 1, tmo, abort_flag)) {
                         raise_abort(ctl, kid, W_PRODUCER);
                         ok = false;
@@ -448,8 +585,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
                     const uint32_t fb = mapa_shared(fb_local, 0);  // the leader's barrier counts both CTAs
                     if (leader) mbar_arrive_expect_tx(fb_local, 2 * kPairStageBytes);
                     const uint32_t sa = smem_u32(smem + (size_t)s * kPairStageBytes);
-                    tma_load_2d_pair(sa, &map_a, fb, kb * kBK, arow, pol_act);
-                    tma_load_2d_pair(sa + kPairHalfBytes, map_b, fb, kb * kBK, brow, pol_w);
+                    tma_load_2d_pair(sa, &map_a, fb, kx0 + kb * kBK, arow, WG ? pol_w : pol_act);
+                    tma_load_2d_pair(sa + kPairHalfBytes, map_b, fb, kx0 + kb * kBK, brow, pol_w);
                     issued_mask |= 1u << s;
                     issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
                     if (++s == kPairStages) { s = 0; ph ^= 1; }
@@ -470,6 +607,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
             bool ok = true, any = false;
             int it = 0;
             for (int tile = pair; ok && tile < n_work; tile += n_pairs, ++it) {
+                int e, nt, mt;
+                decode(tile, e, nt, mt);
+                const int nk = ksteps(e);
                 const int b = it & 1;
                 const uint32_t aph = (it >> 1) & 1;
                 if (!mbar_wait_cluster(smem_u32(&ctl->tempty[b]), aph ^ 1, tmo, abort_flag)) {
@@ -479,7 +619,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + b * kTileAccCols;
-                for (int kb = 0; kb < KB; ++kb) {
+                for (int kb = 0; kb < nk; ++kb) {
                     if (!mbar_wait(smem_u32(&ctl->full[s]), ph, tmo, abort_flag)) {
                         raise_abort(ctl, kid, W_MMA);
                         ok = false;
@@ -523,10 +663,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
             }
             tc_fence_after();
             const uint32_t taddr = tmem_base + b * kTileAccCols + ((uint32_t)(sub * 32) << 16);
-            const int grow = mt * kPairM + row_in_tile;
-            const bool valid = grow < ctl->cnt[e];
-            const int64_t r = ctl->off[e] + grow;
-            tile_epilogue<UP>(taddr, valid, r, nt, args);
+            if (WG) {
+                wgrad_epilogue(taddr, ksteps(e) > 0, e, mt * kPairM + row_in_tile, nt, args);
+            } else {
+                const int grow = mt * kPairM + row_in_tile;
+                const bool valid = grow < ctl->cnt[e];
+                const int64_t r = ctl->off[e] + grow;
+                if (MODE == PM_BWD_DH) bwd_dh_epilogue(taddr, valid, r, nt, args);
+                else tile_epilogue<UP>(taddr, valid, r, nt, args);
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(tempty_leader[b]);
@@ -760,9 +905,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 }
 
 // H[r][f] = bf16( SiLU(sum_s U_s[r][f]) * sum_s V_s[r][f] ), partials [S][2][R][F]
+// u_out, v_out (nullable, training forward): the summed u and v in bf16.
 __global__ void __launch_bounds__(256)
     reduce_swiglu_kernel(const float* __restrict__ part, int S, int64_t R, int F,
-                         __nv_bfloat16* __restrict__ H) {
+                         __nv_bfloat16* __restrict__ H, __nv_bfloat16* __restrict__ u_out,
+                         __nv_bfloat16* __restrict__ v_out) {
     pdl_trigger();
     pdl_wait();
     const int64_t n = R * F;
@@ -789,6 +936,10 @@ __global__ void __launch_bounds__(256)
             v += part[(2 * (int64_t)s + 1) * plane + i];
         }
         H[i] = __float2bfloat16_rn(silu_f32(u) * v);
+        if (u_out != nullptr) {
+            u_out[i] = __float2bfloat16_rn(u);
+            v_out[i] = __float2bfloat16_rn(v);
+        }
     }
 }
 

@@ -17,6 +17,7 @@
 #include "common.cuh"
 #include "ffn_f32.cuh"
 #include "ffn_tc.cuh"
+#include "bwd.cuh"
 #include "permute.cuh"
 #include "router.cuh"
 
@@ -46,11 +47,11 @@ struct HostState {
     bool timing = false;
     bool pdl = true;           // programmatic dependent launch between the library's kernels
     int tile_ctas = 2;         // token tiles on CTA pairs (2) or single CTAs (1)
-    int pair_cap[kMaxDevices][2] = {{0}};  // resident CTA pairs per kernel (0 = not queried)
+    int pair_cap[kMaxDevices][5] = {{0}};  // resident CTA pairs per kernel (0 = not queried)
     std::vector<TimingRecord> records;
     std::vector<cudaEvent_t> pool;
     int sms[kMaxDevices] = {0};
-    bool attr_set[kMaxDevices][8] = {{false}};
+    bool attr_set[kMaxDevices][12] = {{false}};
 };
 HostState g;
 
@@ -409,7 +410,7 @@ int pair_grid(int64_t pairs_upper, int cap) {
 moe_status run_ffn(const moe_shape& s, const void* x_perm, const int32_t* offsets, const float* perm_w,
                    const void* w1, const void* w3, const void* w2, float* y_slot, unsigned char* ws,
                    const FfnLayout& L, cudaStream_t st, const int32_t* slot_row = nullptr, void* y = nullptr,
-                   bool* combined = nullptr) {
+                   bool* combined = nullptr, __nv_bfloat16* u_out = nullptr, __nv_bfloat16* v_out = nullptr) {
     if (s.T == 0) return MOE_OK;
     const int64_t R = 2 * s.T;
     const int d = s.d, F = s.ffn, E = s.E;
@@ -429,19 +430,19 @@ moe_status run_ffn(const moe_shape& s, const void* x_perm, const int32_t* offset
     __nv_bfloat16* H = reinterpret_cast<__nv_bfloat16*>(ws + L.h);
     if (L.path == 1 && g.tile_ctas == 2) {
         // CTA pairs: each CTA stages 128 token rows and 128 weight rows per stage
-        const int cap_up = ensure_smem(tile_pair_gemm_kernel<true>, 6, kPairSmemBytes)
-                               ? pair_capacity(tile_pair_gemm_kernel<true>, kPairSmemBytes, 0) : -1;
-        const int cap_down = ensure_smem(tile_pair_gemm_kernel<false>, 7, kPairSmemBytes)
-                                 ? pair_capacity(tile_pair_gemm_kernel<false>, kPairSmemBytes, 1) : -1;
+        const int cap_up = ensure_smem(tile_pair_gemm_kernel<PM_UP>, 6, kPairSmemBytes)
+                               ? pair_capacity(tile_pair_gemm_kernel<PM_UP>, kPairSmemBytes, 0) : -1;
+        const int cap_down = ensure_smem(tile_pair_gemm_kernel<PM_DOWN>, 7, kPairSmemBytes)
+                                 ? pair_capacity(tile_pair_gemm_kernel<PM_DOWN>, kPairSmemBytes, 1) : -1;
         if (cap_up > 0 && cap_down > 0) {
             CUtensorMap ma, mb0, mb1;
             if (!make_map(&ma, x_perm, d, R, 128) || !make_map(&mb0, w1, d, (uint64_t)E * F, 128) ||
                 !make_map(&mb1, w3, d, (uint64_t)E * F, 128))
                 return MOE_ERR_CUDA;
-            TileArgs up{offsets, perm_w, H, E, d, F / kTileM, F, F, g.timeout_ns};
+            TileArgs up{offsets, perm_w, H, E, d, F / kTileM, F, F, g.timeout_ns, u_out, v_out};
             const int64_t pairs_up = ((R + kPairM - 1) / kPairM + E) * (F / kTileM);
             MOE_TRY(launch("tile_up_swiglu", st, [&] {
-                return klaunch(tile_pair_gemm_kernel<true>, pair_grid(pairs_up, cap_up), kTcThreads, kPairSmemBytes,
+                return klaunch(tile_pair_gemm_kernel<PM_UP>, pair_grid(pairs_up, cap_up), kTcThreads, kPairSmemBytes,
                                st, ma, mb0, mb1, up);
             }));
             CUtensorMap mh, mw2;
@@ -449,7 +450,7 @@ moe_status run_ffn(const moe_shape& s, const void* x_perm, const int32_t* offset
             TileArgs down{offsets, perm_w, y_slot, E, F, d / kTileN, d, d, g.timeout_ns};
             const int64_t pairs_down = ((R + kPairM - 1) / kPairM + E) * (d / kTileN);
             return launch("tile_down_scale", st, [&] {
-                return klaunch(tile_pair_gemm_kernel<false>, pair_grid(pairs_down, cap_down), kTcThreads,
+                return klaunch(tile_pair_gemm_kernel<PM_DOWN>, pair_grid(pairs_down, cap_down), kTcThreads,
                                kPairSmemBytes, st, mh, mw2, mw2, down);
             });
         }
@@ -460,7 +461,7 @@ moe_status run_ffn(const moe_shape& s, const void* x_perm, const int32_t* offset
             !make_map(&mb1, w3, d, (uint64_t)E * F, kTileM))
             return MOE_ERR_CUDA;
         if (!ensure_smem(tile_gemm_kernel<true>, 2, kTileSmemBytes)) return MOE_ERR_CUDA;
-        TileArgs up{offsets, perm_w, H, E, d, F / kTileM, F, F, g.timeout_ns};
+        TileArgs up{offsets, perm_w, H, E, d, F / kTileM, F, F, g.timeout_ns, u_out, v_out};
         const int64_t tiles_up = ((R + kTileM - 1) / kTileM + E) * (F / kTileM);
         MOE_TRY(launch("tile_up_swiglu", st, [&] {
             return klaunch(tile_gemm_kernel<true>, tc_grid(tiles_up), kTcThreads, kTileSmemBytes, st, ma, mb0, mb1, up);
@@ -504,7 +505,7 @@ moe_status run_ffn(const moe_shape& s, const void* x_perm, const int32_t* offset
     }));
     const int rgrid = (int)std::min<int64_t>((R * F + 255) / 256, (int64_t)sm_count() * 8);
     MOE_TRY(launch("reduce_swiglu", st, [&] {
-        return klaunch(reduce_swiglu_kernel, rgrid, 256, 0, st, part_up, L.S_up, R, F, H);
+        return klaunch(reduce_swiglu_kernel, rgrid, 256, 0, st, part_up, L.S_up, R, F, H, u_out, v_out);
     }));
     CUtensorMap mw2, mh;
     if (!make_map(&mw2, w2, F, (uint64_t)E * d, 128) || !make_map(&mh, H, F, R, L.nb)) return MOE_ERR_CUDA;
@@ -564,6 +565,183 @@ moe_status run_aux(const moe_shape& s, const float* logits, const int32_t* count
     return launch("aux_stats", st, [&] {
         return klaunch(aux_stats_kernel, 1, kAuxThreads, 0, st, logits, counts, s.T, s.E, f, P, l_aux);
     });
+}
+
+// ------------------------------------------------------------- training
+// State kept by the training forward: the forward workspace (routing, grouping,
+// x_perm, H, y_slot, scores) plus u = W1 x and v = W3 x per row (bf16).
+struct TrainLayout {
+    FwdLayout f;
+    size_t u = 0, v = 0, total = 0;
+};
+
+TrainLayout train_layout(const moe_shape& s) {
+    TrainLayout L;
+    L.f = fwd_layout(s);
+    const size_t uv = align_up((size_t)(2 * s.T) * s.ffn * 2, kAlign);
+    L.u = L.f.total;
+    L.v = L.u + uv;
+    L.total = L.v + uv;
+    return L;
+}
+
+// Workspace of the backward pass.
+struct BwdLayout {
+    size_t dg, dl, dys, duv, dxp, w2t, w13t, dyst, ht, duvt, xpt, dwg, total;
+    int64_t rp;   // token columns of the token-transposed activations (padded groups)
+    int nchunks;  // token chunks of the router's weight gradient
+};
+
+BwdLayout bwd_layout(const moe_shape& s) {
+    BwdLayout L;
+    const size_t T = (size_t)s.T, R = 2 * T, E = (size_t)s.E, d = (size_t)s.d, F = (size_t)s.ffn;
+    L.rp = (int64_t)align_up(R + (size_t)kBK * E, kBK);
+    L.nchunks = (int)((T + kDwgChunk - 1) / kDwgChunk);
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off = align_up(off + bytes, kAlign);
+        return at;
+    };
+    L.dg = take(R * 4);
+    L.dl = take(T * E * 4);
+    L.dys = take(R * d * 2);
+    L.duv = take(R * 2 * F * 2);
+    L.dxp = take(R * d * 4);
+    L.w2t = take(E * F * d * 2);
+    L.w13t = take(E * d * 2 * F * 2);
+    L.dyst = take(d * (size_t)L.rp * 2);
+    L.ht = take(F * (size_t)L.rp * 2);
+    L.duvt = take(2 * F * (size_t)L.rp * 2);
+    L.xpt = take(d * (size_t)L.rp * 2);
+    L.dwg = take((size_t)std::max(L.nchunks, 1) * E * d * 4);
+    L.total = off;
+    return L;
+}
+
+bool train_supported(const moe_shape& s) { return s.dtype == MOE_BF16 && s.d % 256 == 0 && s.ffn % 256 == 0; }
+
+// One CTA-pair GEMM of the backward pass; MOE_ERR_UNSUPPORTED when no CTA pair fits.
+template <int MODE>
+moe_status launch_pair(const char* name, int slot, int cap_slot, const CUtensorMap& ma, const CUtensorMap& mb,
+                       const TileArgs& a, int64_t pairs_upper, cudaStream_t st) {
+    if (!ensure_smem(tile_pair_gemm_kernel<MODE>, slot, kPairSmemBytes)) return MOE_ERR_CUDA;
+    const int cap = pair_capacity(tile_pair_gemm_kernel<MODE>, kPairSmemBytes, cap_slot);
+    if (cap <= 0) return MOE_ERR_UNSUPPORTED;
+    return launch(name, st, [&] {
+        return klaunch(tile_pair_gemm_kernel<MODE>, pair_grid(pairs_upper, cap), kTcThreads, kPairSmemBytes, st, ma,
+                       mb, mb, a);
+    });
+}
+
+moe_status run_backward(const moe_shape& s, const __nv_bfloat16* x, const __nv_bfloat16* wg,
+                        const __nv_bfloat16* w1, const __nv_bfloat16* w3, const __nv_bfloat16* w2,
+                        const __nv_bfloat16* dy, float aux_coef, const unsigned char* state, __nv_bfloat16* dx,
+                        float* dwg, float* dw1, float* dw3, float* dw2, unsigned char* ws, cudaStream_t st) {
+    const TrainLayout TL = train_layout(s);
+    const BwdLayout B = bwd_layout(s);
+    const int64_t T = s.T, R = 2 * T;
+    const int d = s.d, F = s.ffn, E = s.E;
+    const int32_t* idx = reinterpret_cast<const int32_t*>(state + TL.f.idx);
+    const float* gw = reinterpret_cast<const float*>(state + TL.f.w);
+    const float* logits = reinterpret_cast<const float*>(state + TL.f.logits);
+    const int32_t* counts = reinterpret_cast<const int32_t*>(state + TL.f.counts);
+    const int32_t* offsets = reinterpret_cast<const int32_t*>(state + TL.f.offsets);
+    const int32_t* perm_token = reinterpret_cast<const int32_t*>(state + TL.f.perm_token);
+    const int32_t* slot_row = reinterpret_cast<const int32_t*>(state + TL.f.slot_row);
+    const float* perm_w = reinterpret_cast<const float*>(state + TL.f.perm_w);
+    const __nv_bfloat16* x_perm = reinterpret_cast<const __nv_bfloat16*>(state + TL.f.x_perm);
+    const float* y_slot = reinterpret_cast<const float*>(state + TL.f.y_slot);
+    const __nv_bfloat16* H = reinterpret_cast<const __nv_bfloat16*>(state + TL.f.ffn + TL.f.f.h);
+    const __nv_bfloat16* U = reinterpret_cast<const __nv_bfloat16*>(state + TL.u);
+    const __nv_bfloat16* V = reinterpret_cast<const __nv_bfloat16*>(state + TL.v);
+    float* dg = reinterpret_cast<float*>(ws + B.dg);
+    float* dl = reinterpret_cast<float*>(ws + B.dl);
+    __nv_bfloat16* dys = reinterpret_cast<__nv_bfloat16*>(ws + B.dys);
+    __nv_bfloat16* duv = reinterpret_cast<__nv_bfloat16*>(ws + B.duv);
+    float* dxp = reinterpret_cast<float*>(ws + B.dxp);
+    __nv_bfloat16* w2t = reinterpret_cast<__nv_bfloat16*>(ws + B.w2t);
+    __nv_bfloat16* w13t = reinterpret_cast<__nv_bfloat16*>(ws + B.w13t);
+    __nv_bfloat16* dyst = reinterpret_cast<__nv_bfloat16*>(ws + B.dyst);
+    __nv_bfloat16* ht = reinterpret_cast<__nv_bfloat16*>(ws + B.ht);
+    __nv_bfloat16* duvt = reinterpret_cast<__nv_bfloat16*>(ws + B.duvt);
+    __nv_bfloat16* xpt = reinterpret_cast<__nv_bfloat16*>(ws + B.xpt);
+    float* part = reinterpret_cast<float*>(ws + B.dwg);
+    const int sms = sm_count();
+
+    // transposed weights: W2^T [E][ffn][d] and [W1^T | W3^T] [E][d][2 ffn]
+    MOE_TRY(launch("bwd_transpose_w", st, [&] {
+        return klaunch(transpose_w_kernel, dim3(F / kTrTile, d / kTrTile, E), kTrThreads, 0, st, w2, d, F, w2t, d, 0);
+    }));
+    MOE_TRY(launch("bwd_transpose_w", st, [&] {
+        return klaunch(transpose_w_kernel, dim3(d / kTrTile, F / kTrTile, E), kTrThreads, 0, st, w1, F, d, w13t,
+                       2 * F, 0);
+    }));
+    MOE_TRY(launch("bwd_transpose_w", st, [&] {
+        return klaunch(transpose_w_kernel, dim3(d / kTrTile, F / kTrTile, E), kTrThreads, 0, st, w3, F, d, w13t,
+                       2 * F, F);
+    }));
+    // per slot: dYs = g dy, dg = <dy, E(x)>; per token: the scores' gradient
+    MOE_TRY(launch("bwd_slot", st, [&] {
+        return klaunch(bwd_slot_kernel, (int)std::max<int64_t>(1, std::min<int64_t>((R + 7) / 8, (int64_t)sms * 8)),
+                       256, 0, st, dy, y_slot, perm_token, perm_w, offsets, E, d, dys, dg);
+    }));
+    MOE_TRY(launch("bwd_router", st, [&] {
+        return klaunch(bwd_router_kernel, (int)std::min<int64_t>((T + 255) / 256, (int64_t)sms * 4), 256, 0, st, idx,
+                       gw, slot_row, dg, logits, counts, T, E, aux_coef, dl);
+    }));
+    // dh = dYs W2, then du, dv with the kept u, v
+    const int64_t token_tiles = (R + kPairM - 1) / kPairM + E;
+    CUtensorMap ma, mb;
+    if (!make_map(&ma, dys, d, R, 128) || !make_map(&mb, w2t, d, (uint64_t)E * F, 128)) return MOE_ERR_CUDA;
+    TileArgs a_dh{offsets, nullptr, duv, E, d, F / kTileN, F, 2 * F, g.timeout_ns};
+    a_dh.u_in = U;
+    a_dh.v_in = V;
+    MOE_TRY(launch_pair<PM_BWD_DH>("bwd_dh_swiglu", 8, 2, ma, mb, a_dh, token_tiles * (F / kTileN), st));
+    // dXp = [du dv] [W1; W3]
+    if (!make_map(&ma, duv, 2 * F, R, 128) || !make_map(&mb, w13t, 2 * F, (uint64_t)E * d, 128)) return MOE_ERR_CUDA;
+    TileArgs a_dx{offsets, nullptr, dxp, E, 2 * F, d / kTileN, d, d, g.timeout_ns};
+    MOE_TRY(launch_pair<PM_BWD_DX>("bwd_dx", 9, 3, ma, mb, a_dx, token_tiles * (d / kTileN), st));
+    // dx = both slots + the router's part
+    MOE_TRY(launch("bwd_combine", st, [&] {
+        return klaunch(bwd_combine_kernel, (int)std::min<int64_t>((T * (d / 4) + 255) / 256, (int64_t)sms * 8), 256, 0,
+                       st, dxp, slot_row, dl, wg, T, d, E, dx);
+    }));
+    // dW_g = dl^T x
+    MOE_TRY(launch("bwd_dwg", st, [&] {
+        return klaunch(dwg_partial_kernel, dim3(B.nchunks, (d + 255) / 256), 256, 0, st, dl, x, T, d, E, part);
+    }));
+    MOE_TRY(launch("bwd_dwg", st, [&] {
+        return klaunch(dwg_final_kernel, (int)std::min<int64_t>(((int64_t)E * d + 255) / 256, (int64_t)sms * 4), 256,
+                       0, st, part, B.nchunks, d, E, dwg);
+    }));
+    // token-transposed activations, each expert's tokens from a multiple of 64
+    auto tr = [&](const __nv_bfloat16* in, int cols, __nv_bfloat16* out) {
+        return launch("bwd_transpose_tok", st, [&] {
+            return klaunch(transpose_tok_kernel, dim3(cols / kTrTile, (unsigned)(B.rp / kTrTile)), kTrThreads, 0, st,
+                           in, offsets, E, cols, out, B.rp);
+        });
+    };
+    MOE_TRY(tr(dys, d, dyst));
+    MOE_TRY(tr(H, F, ht));
+    MOE_TRY(tr(duv, 2 * F, duvt));
+    MOE_TRY(tr(x_perm, d, xpt));
+    // dW2[e] = dYs_e^T H_e
+    if (!make_map(&ma, dyst, (uint64_t)B.rp, d, 128) || !make_map(&mb, ht, (uint64_t)B.rp, F, 128)) return MOE_ERR_CUDA;
+    TileArgs a_w2{offsets, nullptr, dw2, E, 0, F / kTileN, 0, F, g.timeout_ns};
+    a_w2.m_tiles = d / kPairM;
+    a_w2.split_rows = d;
+    a_w2.out_estride = (int64_t)d * F;
+    MOE_TRY(launch_pair<PM_WGRAD>("bwd_dw2", 10, 4, ma, mb, a_w2, (int64_t)E * (d / kPairM) * (F / kTileN), st));
+    // [dW1; dW3][e] = [du dv]_e^T Xp_e
+    if (!make_map(&ma, duvt, (uint64_t)B.rp, 2 * (uint64_t)F, 128) || !make_map(&mb, xpt, (uint64_t)B.rp, d, 128))
+        return MOE_ERR_CUDA;
+    TileArgs a_w13{offsets, nullptr, dw1, E, 0, d / kTileN, 0, d, g.timeout_ns};
+    a_w13.out2 = dw3;
+    a_w13.m_tiles = 2 * F / kPairM;
+    a_w13.split_rows = F;
+    a_w13.out_estride = (int64_t)F * d;
+    return launch_pair<PM_WGRAD>("bwd_dw13", 10, 4, ma, mb, a_w13, (int64_t)E * (2 * F / kPairM) * (d / kTileN), st);
 }
 
 // Scratch of moe_layer_forward_noalloc: a fixed array of static device memory,
@@ -721,6 +899,83 @@ moe_status moe_layer_forward_noalloc(const moe_shape* s, const void* x, const vo
     if (scratch == nullptr) return MOE_ERR_CUDA;
     return moe_layer_forward(s, x, w_gate, w1, w3, w2, y, nullptr, nullptr, nullptr, scratch, kNoAllocScratchBytes,
                              stream);
+}
+
+size_t moe_train_state_bytes(const moe_shape* s) {
+    if (check_shape(s) != MOE_OK || !train_supported(*s) || choose_path(*s) == 0) return 0;
+    return train_layout(*s).total;
+}
+
+size_t moe_backward_workspace_bytes(const moe_shape* s) {
+    if (check_shape(s) != MOE_OK || !train_supported(*s)) return 0;
+    return bwd_layout(*s).total;
+}
+
+moe_status moe_layer_forward_train(const moe_shape* s, const void* x, const void* w_gate, const void* w1,
+                                   const void* w3, const void* w2, void* y, float* aux_f, float* aux_P,
+                                   float* aux_l_aux, void* state, size_t state_bytes, void* stream) {
+    MOE_TRY(check_shape(s));
+    if (!train_supported(*s)) return MOE_ERR_UNSUPPORTED;
+    const bool aux = aux_f != nullptr && aux_P != nullptr && aux_l_aux != nullptr;
+    if ((aux_f != nullptr || aux_P != nullptr || aux_l_aux != nullptr) && !aux) return MOE_ERR_INVALID_ARG;
+    if (aux && (!ok_ptr(aux_f) || !ok_ptr(aux_P) || !ok_ptr(aux_l_aux))) return MOE_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (s->T == 0) return aux ? run_aux(*s, nullptr, nullptr, aux_f, aux_P, aux_l_aux, st) : MOE_OK;
+    if (!ok_ptr(x) || !ok_ptr(w_gate) || !ok_ptr(w1) || !ok_ptr(w3) || !ok_ptr(w2) || !ok_ptr(y) || !ok_ptr(state))
+        return MOE_ERR_INVALID_ARG;
+    if (choose_path(*s) == 0) return MOE_ERR_UNSUPPORTED;
+    const TrainLayout L = train_layout(*s);
+    if (state_bytes < L.total) return MOE_ERR_WORKSPACE;
+    unsigned char* w = static_cast<unsigned char*>(state);
+    int32_t* idx = reinterpret_cast<int32_t*>(w + L.f.idx);
+    float* gw = reinterpret_cast<float*>(w + L.f.w);
+    float* logits = reinterpret_cast<float*>(w + L.f.logits);
+    int32_t* counts = reinterpret_cast<int32_t*>(w + L.f.counts);
+    int32_t* offsets = reinterpret_cast<int32_t*>(w + L.f.offsets);
+    int32_t* perm_token = reinterpret_cast<int32_t*>(w + L.f.perm_token);
+    int32_t* slot_row = reinterpret_cast<int32_t*>(w + L.f.slot_row);
+    float* perm_w = reinterpret_cast<float*>(w + L.f.perm_w);
+    void* x_perm = w + L.f.x_perm;
+    float* y_slot = reinterpret_cast<float*>(w + L.f.y_slot);
+    MOE_TRY(run_router(*s, x, w_gate, idx, gw, logits, st));
+    MOE_TRY(run_permute(*s, idx, gw, x, counts, offsets, perm_token, slot_row, perm_w, x_perm, w + L.f.perm_ws,
+                        permute_ws_bytes(*s), st));
+    // y_slot stays in the state (the backward reads each expert's output), so
+    // the expert outputs are combined by the separate pass
+    MOE_TRY(run_ffn(*s, x_perm, offsets, perm_w, w1, w3, w2, y_slot, w + L.f.ffn, L.f.f, st, nullptr, nullptr,
+                    nullptr, reinterpret_cast<__nv_bfloat16*>(w + L.u), reinterpret_cast<__nv_bfloat16*>(w + L.v)));
+    MOE_TRY(run_combine(*s, y_slot, slot_row, y, st));
+    if (aux) MOE_TRY(run_aux(*s, logits, counts, aux_f, aux_P, aux_l_aux, st));
+    return MOE_OK;
+}
+
+moe_status moe_layer_backward(const moe_shape* s, const void* x, const void* w_gate, const void* w1, const void* w3,
+                              const void* w2, const void* dy, float aux_coef, const void* state, size_t state_bytes,
+                              void* dx, float* dw_gate, float* dw1, float* dw3, float* dw2, void* ws, size_t ws_bytes,
+                              void* stream) {
+    MOE_TRY(check_shape(s));
+    if (!train_supported(*s)) return MOE_ERR_UNSUPPORTED;
+    if (!ok_ptr(dw_gate) || !ok_ptr(dw1) || !ok_ptr(dw3) || !ok_ptr(dw2)) return MOE_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (s->T == 0) {
+        // no tokens: every gradient is zero
+        const size_t we = (size_t)s->E * s->ffn * s->d * sizeof(float);
+        if (cudaMemsetAsync(dw_gate, 0, (size_t)s->E * s->d * sizeof(float), st) != cudaSuccess ||
+            cudaMemsetAsync(dw1, 0, we, st) != cudaSuccess || cudaMemsetAsync(dw3, 0, we, st) != cudaSuccess ||
+            cudaMemsetAsync(dw2, 0, we, st) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        return MOE_OK;
+    }
+    if (!ok_ptr(x) || !ok_ptr(w_gate) || !ok_ptr(w1) || !ok_ptr(w3) || !ok_ptr(w2) || !ok_ptr(dy) ||
+        !ok_ptr(state) || !ok_ptr(dx) || !ok_ptr(ws))
+        return MOE_ERR_INVALID_ARG;
+    if (choose_path(*s) == 0) return MOE_ERR_UNSUPPORTED;
+    if (state_bytes < train_layout(*s).total || ws_bytes < bwd_layout(*s).total) return MOE_ERR_WORKSPACE;
+    return run_backward(*s, static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(w_gate),
+                        static_cast<const __nv_bfloat16*>(w1), static_cast<const __nv_bfloat16*>(w3),
+                        static_cast<const __nv_bfloat16*>(w2), static_cast<const __nv_bfloat16*>(dy), aux_coef,
+                        static_cast<const unsigned char*>(state), static_cast<__nv_bfloat16*>(dx), dw_gate, dw1, dw3,
+                        dw2, static_cast<unsigned char*>(ws), st);
 }
 
 moe_status moe_get_device_status(int32_t* code, int32_t* detail) {

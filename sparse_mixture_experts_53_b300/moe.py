@@ -38,7 +38,8 @@ EXPORTED = (
     "moe_permute_workspace_bytes",
     "moe_route_top2", "moe_permute", "moe_expert_ffn", "moe_combine", "moe_aux_stats",
     "moe_layer_forward", "moe_layer_forward_noalloc", "moe_get_device_status", "moe_set_wait_timeout_ns", "moe_set_knob",
-    "moe_timing_enable", "moe_timing_read",
+    "moe_timing_enable", "moe_timing_read", "moe_train_state_bytes", "moe_backward_workspace_bytes",
+    "moe_layer_forward_train", "moe_layer_backward",
 )
 
 
@@ -80,6 +81,11 @@ def _load() -> ctypes.CDLL:
         "moe_set_knob": ([ctypes.c_int32, ctypes.c_int64], I),
         "moe_timing_enable": ([ctypes.c_int32], I),
         "moe_timing_read": ([ctypes.c_char_p, ctypes.c_size_t], I),
+        "moe_train_state_bytes": ([S], ctypes.c_size_t),
+        "moe_backward_workspace_bytes": ([S], ctypes.c_size_t),
+        "moe_layer_forward_train": ([S, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P], I),
+        "moe_layer_backward": ([S, P, P, P, P, P, P, ctypes.c_float, P, ctypes.c_size_t, P, P, P, P, P, P,
+                                ctypes.c_size_t, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -193,6 +199,30 @@ def moe_layer_forward_noalloc(shape, x, w_gate, w1, w3, w2, y, stream=None):
         ctypes.byref(shape), _ptr(x), _ptr(w_gate), _ptr(w1), _ptr(w3), _ptr(w2), _ptr(y), _stream(stream)))
 
 
+def moe_train_state_bytes(shape: moe_shape) -> int:
+    return int(lib.moe_train_state_bytes(ctypes.byref(shape)))
+
+
+def moe_backward_workspace_bytes(shape: moe_shape) -> int:
+    return int(lib.moe_backward_workspace_bytes(ctypes.byref(shape)))
+
+
+def moe_layer_forward_train(shape, x, w_gate, w1, w3, w2, y, state, aux=None, stream=None):
+    """moe_layer_forward that keeps its intermediates in `state` (moe_train_state_bytes bytes)."""
+    f, P, l = aux if aux is not None else (None, None, None)
+    _check("moe_layer_forward_train", lib.moe_layer_forward_train(
+        ctypes.byref(shape), _ptr(x), _ptr(w_gate), _ptr(w1), _ptr(w3), _ptr(w2), _ptr(y), _ptr(f), _ptr(P),
+        _ptr(l), _ptr(state), state.numel() * state.element_size(), _stream(stream)))
+
+
+def moe_layer_backward(shape, x, w_gate, w1, w3, w2, dy, aux_coef, state, dx, dw_gate, dw1, dw3, dw2, ws,
+                       stream=None):
+    _check("moe_layer_backward", lib.moe_layer_backward(
+        ctypes.byref(shape), _ptr(x), _ptr(w_gate), _ptr(w1), _ptr(w3), _ptr(w2), _ptr(dy), float(aux_coef),
+        _ptr(state), state.numel() * state.element_size(), _ptr(dx), _ptr(dw_gate), _ptr(dw1), _ptr(dw3),
+        _ptr(dw2), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
 def moe_get_device_status() -> tuple[int, int]:
     code = ctypes.c_int32(0)
     detail = ctypes.c_int32(0)
@@ -242,3 +272,41 @@ def layer_forward(x, w_gate, w1, w3, w2, aux: bool = False, ws=None, out=None, s
                  torch.empty(1, dtype=torch.float32, device=x.device))
     moe_layer_forward(shape, x, w_gate, w1, w3, w2, y, ws, stats, stream)
     return (y, stats) if aux else y
+
+
+def _bytes(n: int, device) -> torch.Tensor:
+    return torch.empty(max(int(n), 16), dtype=torch.uint8, device=device)
+
+
+def layer_forward_train(x, w_gate, w1, w3, w2, aux: bool = False, stream=None):
+    """Training forward: returns (y, state[, stats]); the state feeds layer_backward."""
+    shape = shape_of(x, w1)
+    n = moe_train_state_bytes(shape)
+    if n == 0 and shape.T > 0:
+        raise MoEError("moe_train_state_bytes", MOE_ERR_UNSUPPORTED)
+    state = _bytes(n, x.device)
+    y = torch.empty_like(x)
+    stats = None
+    if aux:
+        E = w1.shape[0]
+        stats = tuple(torch.empty(m, dtype=torch.float32, device=x.device) for m in (E, E, 1))
+    moe_layer_forward_train(shape, x, w_gate, w1, w3, w2, y, state, stats, stream)
+    return (y, state, stats) if aux else (y, state)
+
+
+def layer_backward(x, w_gate, w1, w3, w2, dy, state, aux_coef: float = 0.0, ws=None, stream=None):
+    """Gradients (dx, dw_gate, dw1, dw3, dw2) for the upstream gradient dy; weight gradients in float32."""
+    shape = shape_of(x, w1)
+    if ws is None:
+        n = moe_backward_workspace_bytes(shape)
+        if n == 0:
+            raise MoEError("moe_backward_workspace_bytes", MOE_ERR_UNSUPPORTED)
+        ws = _bytes(n, x.device)
+    f32 = dict(dtype=torch.float32, device=x.device)
+    dx = torch.empty_like(x)
+    dw_gate = torch.empty(w_gate.shape, **f32)
+    dw1 = torch.empty(w1.shape, **f32)
+    dw3 = torch.empty(w3.shape, **f32)
+    dw2 = torch.empty(w2.shape, **f32)
+    moe_layer_backward(shape, x, w_gate, w1, w3, w2, dy, aux_coef, state, dx, dw_gate, dw1, dw3, dw2, ws, stream)
+    return dx, dw_gate, dw1, dw3, dw2
