@@ -369,6 +369,89 @@ def run_ours(args, rank, world, local) -> dict | None:
     return line if rank == 0 else None
 
 
+TRAIN_GEMM_FLOPS = {  # multiples of R*d*ffn (R = 2T slot rows) per launch
+    "tile_up_swiglu": 4, "tile_down_scale": 2, "bwd_dh_swiglu": 2, "bwd_dx": 4, "bwd_dw2": 2, "bwd_dw13": 4,
+}
+
+
+def run_training(args) -> dict:
+    """One training step of the layer: forward that keeps its state, then the backward pass."""
+    import torch
+
+    from moe_inputs import CONFIGS, make_config
+    from sparse_mixture_experts_53_b300 import moe
+
+    torch.cuda.set_device(0)
+    moe.moe_set_knob(moe.MOE_KNOB_PDL, args.pdl)
+    k = args.config
+    cfg = CONFIGS[k]
+    L = make_config(k)
+    x = L.x.cuda()
+    wg, w1, w3, w2 = L.w_gate.cuda(), L.w1.cuda(), L.w3.cuda(), L.w2.cuda()
+    dy = torch.randn(x.shape, generator=torch.Generator().manual_seed(7)).to(torch.bfloat16).cuda()
+    shape = moe.shape_of(x, w1)
+    state = torch.empty(moe.moe_train_state_bytes(shape), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(moe.moe_backward_workspace_bytes(shape), dtype=torch.uint8, device="cuda")
+    y = torch.empty_like(x)
+    dx = torch.empty_like(x)
+    f32 = dict(dtype=torch.float32, device="cuda")
+    dwg, dw1, dw3, dw2 = (torch.empty(t.shape, **f32) for t in (wg, w1, w3, w2))
+    aux_coef = 0.01 if cfg["aux"] else 0.0
+    stream = torch.cuda.current_stream()
+
+    def step():
+        moe.moe_layer_forward_train(shape, x, wg, w1, w3, w2, y, state, None, stream)
+        moe.moe_layer_backward(shape, x, wg, w1, w3, w2, dy, aux_coef, state, dx, dwg, dw1, dw3, dw2, ws, stream)
+
+    for _ in range(args.warmup):
+        step()
+    code, detail = moe.moe_get_device_status()
+    if code != moe.MOE_OK:
+        raise RuntimeError(f"device status after warm-up: {moe.status_string(code)} ({detail})")
+    sampler = ClockSampler(0)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with sampler:
+        a.record(stream)
+        for _ in range(args.steps):
+            step()
+        b.record(stream)
+        torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / args.steps
+    moe.moe_timing_enable(True)
+    for _ in range(args.steps):
+        step()
+    torch.cuda.synchronize()
+    kern = moe.moe_timing_read()
+    moe.moe_timing_enable(False)
+    code, detail = moe.moe_get_device_status()
+    if code != moe.MOE_OK:
+        raise RuntimeError(f"device status after timing: {moe.status_string(code)} ({detail})")
+    T, d, F = cfg["T"], cfg["d"], cfg["ffn"]
+    R = 2 * T
+    peaks = _peaks()
+    per = {n: (v[1] / v[0]) for n, v in kern.items()}
+    gemms = {n: per[n] for n in TRAIN_GEMM_FLOPS if n in per}
+    dom = max(gemms, key=gemms.get)
+    achieved = TRAIN_GEMM_FLOPS[dom] * R * d * F / (per[dom] * 1e-3) / 1e12
+    flops = 18 * R * d * F
+    return {
+        "metric": "MoE-layer training tokens/s (forward + backward) at Mixtral shape (bf16)", "pass": "forward+backward",
+        "value": round(T / (ms * 1e-3), 1), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "dtype": "bf16",
+        "data": "synthetic (seeded Mixtral-shape tensors, random init)",
+        "config": {"workload": cfg["name"], "T": T, "d": d, "ffn": F, "E": cfg["E"], "k": 2, "aux_coef": aux_coef},
+        "step": {"tflops": round(flops / (ms * 1e-3) / 1e12, 2),
+                 "frac_bf16": round(flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4)},
+        "roofline": {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
+                     "peak_source": peaks["source"] + " (burst)", "launch_ms": round(per[dom], 5)},
+        "kernels_ms_per_step": {n: round(v[1] / max(1, args.steps), 5) for n, v in kern.items()},
+        "gpu_launches": int(sum(v[0] for v in kern.values())),
+        "clocks": sampler.summary(),
+    }
+
+
 def cpu_baseline(k: int, max_tokens: int | None = None, budget_s: float = 20.0) -> dict:
     """The fp64 oracle, as it stands, on a bounded sample of the workload's tokens."""
     import oracle
@@ -438,12 +521,19 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--pdl", type=int, default=1, choices=[0, 1],
                     help="programmatic dependent launch between the library's kernels")
+    ap.add_argument("--train", action="store_true",
+                    help="time a training step (forward that keeps its state + backward) instead of the forward")
     ap.add_argument("--tile-ctas", type=int, default=2, choices=[1, 2],
                     help="token tiles on CTA pairs (2) or single CTAs (1)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     rank, world, local = _dist_env()
+    if args.train:
+        if args.impl != "ours" or world != 1:
+            raise SystemExit("--train times this library's training step on one GPU")
+        print(json.dumps(run_training(args)), flush=True)
+        return
     if args.impl == "reference":
         line = run_reference(args, rank, world)
         if line is not None:

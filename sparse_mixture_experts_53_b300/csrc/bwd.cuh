@@ -22,103 +22,48 @@
 
 namespace moe {
 
-constexpr int kTrTile = 64;        // transpose tile (elements per side)
-constexpr int kTrThreads = 256;
-
-// out[b][c][col_off + r] = in[b][r][c] for r < rows, c < cols (bf16); rows and
-// cols are multiples of 64. Batched over experts (blockIdx.z).
-__global__ void __launch_bounds__(kTrThreads)
-    transpose_w_kernel(const __nv_bfloat16* __restrict__ in, int rows, int cols, __nv_bfloat16* __restrict__ out,
-                       int ld_out, int col_off) {
-    __shared__ __nv_bfloat16 tile[kTrTile][kTrTile + 8];
-    pdl_trigger();
-    pdl_wait();
-    const int r0 = blockIdx.y * kTrTile, c0 = blockIdx.x * kTrTile;
-    const __nv_bfloat16* src = in + (int64_t)blockIdx.z * rows * cols;
-    __nv_bfloat16* dst = out + (int64_t)blockIdx.z * cols * ld_out;
-    // load: 64 rows x 8 chunks of 8 elements
-    for (int i = threadIdx.x; i < kTrTile * 8; i += kTrThreads) {
-        const int rr = i >> 3, cc = (i & 7) * 8;
-        const uint4 v = *reinterpret_cast<const uint4*>(src + (int64_t)(r0 + rr) * cols + c0 + cc);
-        const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&v);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) tile[rr][cc + q] = e[q];
-    }
-    __syncthreads();
-    for (int i = threadIdx.x; i < kTrTile * 8; i += kTrThreads) {
-        const int cc = i >> 3, rr = (i & 7) * 8;
-        __align__(16) __nv_bfloat16 e[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) e[q] = tile[rr + q][cc];
-        *reinterpret_cast<uint4*>(dst + (int64_t)(c0 + cc) * ld_out + col_off + r0 + rr) =
-            *reinterpret_cast<const uint4*>(e);
-    }
-}
-
-// Token transpose of an activation in expert-contiguous row order:
-// out[c][j] = in[r][c] with j = kofs[e] + (r - offsets[e]), where expert e's
-// group starts at kofs[e] = sum over q < e of cnt[q] rounded up to 64; the
-// columns of a group past its cnt[e] tokens are zero. A 64-column tile of the
-// output lies inside one group. cols is a multiple of 64.
-__global__ void __launch_bounds__(kTrThreads)
-    transpose_tok_kernel(const __nv_bfloat16* __restrict__ in, const int32_t* __restrict__ offsets, int E, int cols,
-                         __nv_bfloat16* __restrict__ out, int64_t ld_out) {
-    __shared__ __nv_bfloat16 tile[kTrTile][kTrTile + 8];
-    __shared__ int grp[3];  // expert, first token row, tokens
-    pdl_trigger();
-    pdl_wait();
-    const int64_t j0 = (int64_t)blockIdx.y * kTrTile;
-    const int c0 = blockIdx.x * kTrTile;
-    if (threadIdx.x == 0) {
-        int k = 0, e = -1, r0 = 0, n = 0;
-        for (int q = 0; q < E; ++q) {
-            const int c = offsets[q + 1] - offsets[q];
-            const int kp = (c + kBK - 1) / kBK * kBK;
-            if (j0 >= k && j0 < k + kp) { e = q; r0 = offsets[q] + (int)(j0 - k); n = c - (int)(j0 - k); }
-            k += kp;
-        }
-        grp[0] = e; grp[1] = r0; grp[2] = n;
-    }
-    __syncthreads();
-    if (grp[0] < 0) return;  // past the last group: never read
-    const int r0 = grp[1], n = grp[2];
-    for (int i = threadIdx.x; i < kTrTile * 8; i += kTrThreads) {
-        const int rr = i >> 3, cc = (i & 7) * 8;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (rr < n) v = *reinterpret_cast<const uint4*>(in + (int64_t)(r0 + rr) * cols + c0 + cc);
-        const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&v);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) tile[rr][cc + q] = e[q];
-    }
-    __syncthreads();
-    for (int i = threadIdx.x; i < kTrTile * 8; i += kTrThreads) {
-        const int cc = i >> 3, rr = (i & 7) * 8;
-        __align__(16) __nv_bfloat16 e[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) e[q] = tile[rr + q][cc];
-        *reinterpret_cast<uint4*>(out + (int64_t)(c0 + cc) * ld_out + j0 + rr) = *reinterpret_cast<const uint4*>(e);
-    }
-}
-
-// Per slot row r (one warp each): dYs[r] = perm_w[r] * dy[token], and
-// dg[r] = <dy[token], y_slot[r]> / perm_w[r], i.e. <dy, E_e(x)>. Each lane sums
-// its own 8-element chunks in order, then a butterfly adds the lanes.
+// Rows of dYs and dUV are in the padded group order the backward GEMMs read:
+// expert e's rows start at koff[e] = sum over q < e of its count rounded up to
+// 64, and the rows between groups are zero. One warp per padded row pr:
+//   a row of expert e's group (k = pr - koff[e] < count): r = offsets[e] + k,
+//     dYs[pr] = perm_w[r] * dy[token], dg[r] = <dy[token], y_slot[r]> / perm_w[r]
+//     (= <dy, E_e(x)>); each lane sums its own 8-element chunks in order, then
+//     a butterfly adds the lanes;
+//   a pad row: dYs[pr] = 0 and dUV[pr] = 0.
 __global__ void __launch_bounds__(256)
     bwd_slot_kernel(const __nv_bfloat16* __restrict__ dy, const float* __restrict__ y_slot,
                     const int32_t* __restrict__ perm_token, const float* __restrict__ perm_w,
-                    const int32_t* __restrict__ offsets, int E, int d, __nv_bfloat16* __restrict__ dys,
-                    float* __restrict__ dg) {
+                    const int32_t* __restrict__ offsets, int E, int d, int F, int64_t padded_rows,
+                    __nv_bfloat16* __restrict__ dys, __nv_bfloat16* __restrict__ duv, float* __restrict__ dg) {
+    __shared__ int koff[kMaxExperts + 1];
+    __shared__ int off[kMaxExperts + 1];
     pdl_trigger();
     pdl_wait();
+    if (threadIdx.x == 0) {
+        koff[0] = 0;
+        for (int e = 0; e <= E; ++e) off[e] = offsets[e];
+        for (int e = 0; e < E; ++e) koff[e + 1] = koff[e] + (off[e + 1] - off[e] + 63) / 64 * 64;
+    }
+    __syncthreads();
     const int lane = threadIdx.x & 31;
-    const int64_t rows = offsets[E];
-    for (int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows;
-         r += ((int64_t)gridDim.x * blockDim.x) >> 5) {
+    const int64_t used = koff[E] < padded_rows ? koff[E] : padded_rows;
+    for (int64_t pr = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; pr < used;
+         pr += ((int64_t)gridDim.x * blockDim.x) >> 5) {
+        int e = 0;
+        while (e < E - 1 && pr >= koff[e + 1]) ++e;
+        const int64_t k = pr - koff[e];
+        __nv_bfloat16* out = dys + pr * d;
+        if (k >= off[e + 1] - off[e]) {
+            const uint4 z = make_uint4(0, 0, 0, 0);
+            for (int c = lane * 8; c < d; c += 32 * 8) *reinterpret_cast<uint4*>(out + c) = z;
+            for (int c = lane * 8; c < 2 * F; c += 32 * 8) *reinterpret_cast<uint4*>(duv + pr * 2 * F + c) = z;
+            continue;
+        }
+        const int64_t r = off[e] + k;
         const int64_t t = perm_token[r];
         const float w = perm_w[r];
         const __nv_bfloat16* dyr = dy + t * d;
         const float* ys = y_slot + r * d;
-        __nv_bfloat16* out = dys + r * d;
         float acc = 0.f;
         for (int c = lane * 8; c < d; c += 32 * 8) {
             const uint4 raw = *reinterpret_cast<const uint4*>(dyr + c);

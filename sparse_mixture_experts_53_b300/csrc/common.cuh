@@ -179,11 +179,22 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
            (static_cast<uint64_t>(1024u >> 4) << 32) | (1ull << 46) | (2ull << 61);
 }
 
+// Shared-memory descriptor of an MN-major tile in the 128-byte swizzle TMA
+// writes for a box of 64 MN elements (128 bytes) x K rows: a swizzle atom is 64
+// MN elements x 8 K rows (1 KB); atoms follow each other along K every 1 KB
+// (stride byte offset) and a 64-element MN block is `mn_block_bytes` after the
+// previous one (leading byte offset). A K step of 16 advances 2 KB.
+__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t saddr, uint32_t mn_block_bytes) {
+    return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(mn_block_bytes >> 4) << 16) |
+           (static_cast<uint64_t>(1024u >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+
 // Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1),
-// A and B bf16 (bits 7-9 = 1, bits 10-12 = 1), both K-major (bits 15, 16 = 0),
+// A and B bf16 (bits 7-9 = 1, bits 10-12 = 1), A / B MN-major (bit 15 / 16),
 // N >> 3 in bits 17-22, M >> 4 in bits 24-28.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, bool a_mn = false, bool b_mn = false) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+           ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, one CTA, M x N x 16.

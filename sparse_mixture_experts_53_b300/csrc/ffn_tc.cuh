@@ -62,6 +62,7 @@ struct TcControl {
     int mt[kMaxExperts];
     int base[kMaxExperts + 1];
     int act[kMaxExperts];
+    int koff[kMaxExperts + 1];  // expert groups padded to multiples of 64 rows
 };
 
 constexpr size_t kTileSmemBytes = 1024 + (size_t)kTileStages * kTileStageBytes + sizeof(TcControl);
@@ -378,37 +379,35 @@ constexpr uint32_t kPairStageBytes = 2 * kPairHalfBytes;     // 32 KB per CTA an
 constexpr size_t kPairSmemBytes = 1024 + (size_t)kPairStages * kPairStageBytes + sizeof(TcControl);
 
 // What a CTA-pair tile kernel computes (the tile loop, the TMA ring and the
-// MMA issue are shared; the operands' rows, the K range and the epilogue
-// differ):
+// MMA issue are shared; the operands' rows, their major-ness, the K range and
+// the epilogue differ):
 //   PM_UP      H = SiLU(X W1^T) * (X W3^T) per expert (forward)
 //   PM_DOWN    y_slot = perm_w * (H W2^T) per expert (forward)
-//   PM_BWD_DH  dh = dYs W2 per expert; the epilogue applies the SwiGLU
-//              backward with the kept u, v: du = dh v SiLU'(u), dv = dh SiLU(u),
-//              written side by side as dUV [R][2 ffn] (bf16)
-//   PM_BWD_DX  dXp = dUV [W1; W3] per expert, fp32 (B = the transposed
-//              weights, K = 2 ffn)
-//   PM_WGRAD   weight gradients, fp32: per expert, rows x columns = A^T B over
-//              the expert's tokens, with A and B token-transposed activations
-//              whose expert groups start at multiples of 64 tokens (K range
-//              per expert, zero padded); an expert with no tokens gets zeros
+//   PM_BWD_DH  dh = dYs W2 per expert, W2 read as stored ([d][ffn]: MN-major
+//              B); the epilogue applies the SwiGLU backward with the kept u,
+//              v: du = dh v SiLU'(u), dv = dh SiLU(u), written side by side
+//              as dUV [.][2 ffn] (bf16)
+//   PM_BWD_DX  dXp = dUV [W1; W3] per expert, fp32, W1 and W3 read as stored
+//              ([ffn][d]: MN-major B), K = 2 ffn
+//   PM_WGRAD   weight gradients, fp32: per expert, A^T B over the expert's
+//              tokens, both operands read as stored (token rows: MN-major);
+//              A is a backward activation whose expert groups start at
+//              multiples of 64 rows with zero rows between them, so a K step
+//              that runs past the group adds nothing; an expert with no tokens
+//              gets zeros
+// dYs and dUV (the A operands of the backward modes) use that padded row
+// order; x_perm, H and the outputs y_slot, dXp use the plain one.
 enum PairMode : int { PM_UP = 0, PM_DOWN = 1, PM_BWD_DH = 2, PM_BWD_DX = 3, PM_WGRAD = 4 };
-
-// Start of expert e's K range in the token-transposed layout: groups padded
-// to multiples of 64 tokens, in expert order.
-__device__ __forceinline__ int wgrad_kofs(const int* cnt, int e) {
-    int k = 0;
-    for (int q = 0; q < e; ++q) k += (cnt[q] + kBK - 1) / kBK * kBK;
-    return k;
-}
 
 // Epilogue of one row of a PM_BWD_DH tile: 256 columns f of dh, the kept u
 // and v of the same row and columns, du and dv out in bf16.
-__device__ __forceinline__ void bwd_dh_epilogue(uint32_t taddr, bool valid, int64_t r, int nt, const TileArgs& args) {
-    const int F = args.w_rows;
+__device__ __forceinline__ void bwd_dh_epilogue(uint32_t taddr, bool valid, int64_t r, int64_t pr, int nt,
+                                                const TileArgs& args) {
+    const int F = args.ldo / 2;
     const int64_t col0 = (int64_t)nt * kTileN;
     const __nv_bfloat16* urow = args.u_in + r * F + col0;
     const __nv_bfloat16* vrow = args.v_in + r * F + col0;
-    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(args.out) + r * args.ldo + col0;
+    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(args.out) + pr * args.ldo + col0;
 #pragma unroll 1
     for (int j = 0; j < kTileN; j += 16) {
         uint32_t a[16];
@@ -478,6 +477,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
                           const __grid_constant__ CUtensorMap map_b1, const TileArgs args) {
     constexpr bool UP = MODE == PM_UP;
     constexpr bool WG = MODE == PM_WGRAD;
+    constexpr bool A_MN = WG;                      // A read as stored with K = token rows
+    constexpr bool B_MN = MODE >= PM_BWD_DH;       // B read as stored (weights, or token rows)
+    constexpr bool A_PAD = MODE >= PM_BWD_DH;      // A rows in the padded group order
     extern __shared__ unsigned char tc_smem_raw[];
     unsigned char* smem = align1024(tc_smem_raw);
     TcControl* ctl = reinterpret_cast<TcControl*>(smem + (size_t)kPairStages * kPairStageBytes);
@@ -528,6 +530,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
         }
         ctl->base[args.E] = tiles;
         ctl->n_work = tiles;
+        ctl->koff[0] = 0;
+        for (int e = 0; e < args.E; ++e) ctl->koff[e + 1] = ctl->koff[e] + (ctl->cnt[e] + kBK - 1) / kBK * kBK;
     }
     // both CTAs' barriers are initialised and both halves of tensor memory are
     // allocated before any CTA signals the other
@@ -547,7 +551,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
         mt = rem - nt * ctl->mt[e];
     };
     // K steps of a tile: fixed, or the expert's padded token count
-    auto ksteps = [&](int e) { return WG ? (ctl->cnt[e] + kBK - 1) / kBK : KB; };
+    auto ksteps = [&](int e) { return WG ? (ctl->koff[e + 1] - ctl->koff[e]) / kBK : KB; };
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer (both CTAs)
@@ -565,15 +569,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
             for (int tile = pair; ok && tile < n_work; tile += n_pairs) {
                 int e, nt, mt;
                 decode(tile, e, nt, mt);
-                int arow, brow, kx0 = 0;
-                if (WG) {
-                    arow = mt * kPairM + 128 * (int)rank;
-                    brow = nt * kTileN + 128 * (int)rank;
-                    kx0 = wgrad_kofs(ctl->cnt, e);
-                } else {
-                    arow = ctl->off[e] + mt * kPairM + 128 * (int)rank;
-                    brow = UP ? e * args.w_rows + nt * kTileM : e * args.w_rows + nt * kTileN + 128 * (int)rank;
-                }
+                // this CTA's 128 rows (K-major) or 128 columns (MN-major) of each operand
+                const int a0 = WG ? mt * kPairM + 128 * (int)rank
+                                  : (A_PAD ? ctl->koff[e] : ctl->off[e]) + mt * kPairM + 128 * (int)rank;
+                const int b0 = UP ? e * args.w_rows + nt * kTileM
+                                  : (B_MN ? nt * kTileN + 128 * (int)rank
+                                          : e * args.w_rows + nt * kTileN + 128 * (int)rank);
                 const int nk = ksteps(e);
                 for (int kb = 0; kb < nk; ++kb) {
                     if (!mbar_wait(smem_u32(&ctl->empty[s]), ph ^ 1, tmo, abort_flag)) {
@@ -585,8 +586,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
                     const uint32_t fb = mapa_shared(fb_local, 0);  // the leader's barrier counts both CTAs
                     if (leader) mbar_arrive_expect_tx(fb_local, 2 * kPairStageBytes);
                     const uint32_t sa = smem_u32(smem + (size_t)s * kPairStageBytes);
-                    tma_load_2d_pair(sa, &map_a, fb, kx0 + kb * kBK, arow, WG ? pol_w : pol_act);
-                    tma_load_2d_pair(sa + kPairHalfBytes, map_b, fb, kx0 + kb * kBK, brow, pol_w);
+                    const uint32_t sb = sa + kPairHalfBytes;
+                    const int kx = kb * kBK;
+                    if (A_MN) {
+                        // two boxes of 64 columns x 64 token rows of the padded activation
+                        const int ky = ctl->koff[e] + kx;
+                        tma_load_2d_pair(sa, &map_a, fb, a0, ky, pol_w);
+                        tma_load_2d_pair(sa + kPairHalfBytes / 2, &map_a, fb, a0 + 64, ky, pol_w);
+                    } else {
+                        tma_load_2d_pair(sa, &map_a, fb, kx, a0, pol_act);
+                    }
+                    if (B_MN) {
+                        // two boxes of 64 columns x 64 K rows, read as stored
+                        const CUtensorMap* mb = &map_b0;
+                        int ky;
+                        if (WG) {
+                            ky = ctl->off[e] + kx;                    // token rows of x_perm or H
+                        } else if (MODE == PM_BWD_DX) {
+                            mb = kx < args.w_rows ? &map_b0 : &map_b1;  // rows of W1, then of W3
+                            ky = e * args.w_rows + (kx < args.w_rows ? kx : kx - args.w_rows);
+                        } else {
+                            ky = e * args.w_rows + kx;                // rows of W2
+                        }
+                        tma_load_2d_pair(sb, mb, fb, b0, ky, pol_w);
+                        tma_load_2d_pair(sb + kPairHalfBytes / 2, mb, fb, b0 + 64, ky, pol_w);
+                    } else {
+                        tma_load_2d_pair(sb, map_b, fb, kx, b0, pol_w);
+                    }
                     issued_mask |= 1u << s;
                     issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
                     if (++s == kPairStages) { s = 0; ph ^= 1; }
@@ -602,7 +628,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer (even CTA only)
         if (lane == 0 && leader) {
-            constexpr uint32_t idesc = idesc_bf16_f32(kPairM, kTileN);
+            constexpr uint32_t idesc = idesc_bf16_f32(kPairM, kTileN, A_MN, B_MN);
+            // descriptor start advance per K step of 16, in 16-byte units:
+            // 32 bytes inside a K-major swizzle row, two 1 KB atoms MN-major
+            constexpr uint64_t a_step = A_MN ? 128 : 2;
+            constexpr uint64_t b_step = B_MN ? 128 : 2;
             uint32_t s = 0, ph = 0;
             bool ok = true, any = false;
             int it = 0;
@@ -627,11 +657,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
                     }
                     tc_fence_after();
                     const uint32_t sa = smem_u32(smem + (size_t)s * kPairStageBytes);
-                    const uint64_t adesc = sw128_kmajor_desc(sa);
-                    const uint64_t bdesc = sw128_kmajor_desc(sa + kPairHalfBytes);
+                    const uint32_t sb = sa + kPairHalfBytes;
+                    const uint64_t adesc = A_MN ? sw128_mnmajor_desc(sa, kPairHalfBytes / 2) : sw128_kmajor_desc(sa);
+                    const uint64_t bdesc = B_MN ? sw128_mnmajor_desc(sb, kPairHalfBytes / 2) : sw128_kmajor_desc(sb);
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk)
-                        mma_bf16_pair(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (kb | kk) != 0);
+                        mma_bf16_pair(d_tmem, adesc + a_step * kk, bdesc + b_step * kk, idesc, (kb | kk) != 0);
                     any = true;
                     mma_commit_pair(smem_u32(&ctl->empty[s]), 0x3);
                     if (++s == kPairStages) { s = 0; ph ^= 1; }
@@ -669,7 +700,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
                 const int grow = mt * kPairM + row_in_tile;
                 const bool valid = grow < ctl->cnt[e];
                 const int64_t r = ctl->off[e] + grow;
-                if (MODE == PM_BWD_DH) bwd_dh_epilogue(taddr, valid, r, nt, args);
+                if (MODE == PM_BWD_DH) bwd_dh_epilogue(taddr, valid, r, (int64_t)ctl->koff[e] + grow, nt, args);
                 else tile_epilogue<UP>(taddr, valid, r, nt, args);
             }
             tc_fence_before();

@@ -585,10 +585,11 @@ TrainLayout train_layout(const moe_shape& s) {
     return L;
 }
 
-// Workspace of the backward pass.
+// Workspace of the backward pass. dYs and dUV rows are in the padded group
+// order (each expert's rows from a multiple of 64, zero rows between groups).
 struct BwdLayout {
-    size_t dg, dl, dys, duv, dxp, w2t, w13t, dyst, ht, duvt, xpt, dwg, total;
-    int64_t rp;   // token columns of the token-transposed activations (padded groups)
+    size_t dg, dl, dys, duv, dxp, dwg, total;
+    int64_t rp;   // padded rows: 2T + 64 E, rounded up to 64
     int nchunks;  // token chunks of the router's weight gradient
 };
 
@@ -605,15 +606,9 @@ BwdLayout bwd_layout(const moe_shape& s) {
     };
     L.dg = take(R * 4);
     L.dl = take(T * E * 4);
-    L.dys = take(R * d * 2);
-    L.duv = take(R * 2 * F * 2);
+    L.dys = take((size_t)L.rp * d * 2);
+    L.duv = take((size_t)L.rp * 2 * F * 2);
     L.dxp = take(R * d * 4);
-    L.w2t = take(E * F * d * 2);
-    L.w13t = take(E * d * 2 * F * 2);
-    L.dyst = take(d * (size_t)L.rp * 2);
-    L.ht = take(F * (size_t)L.rp * 2);
-    L.duvt = take(2 * F * (size_t)L.rp * 2);
-    L.xpt = take(d * (size_t)L.rp * 2);
     L.dwg = take((size_t)std::max(L.nchunks, 1) * E * d * 4);
     L.total = off;
     return L;
@@ -623,14 +618,14 @@ bool train_supported(const moe_shape& s) { return s.dtype == MOE_BF16 && s.d % 2
 
 // One CTA-pair GEMM of the backward pass; MOE_ERR_UNSUPPORTED when no CTA pair fits.
 template <int MODE>
-moe_status launch_pair(const char* name, int slot, int cap_slot, const CUtensorMap& ma, const CUtensorMap& mb,
-                       const TileArgs& a, int64_t pairs_upper, cudaStream_t st) {
+moe_status launch_pair(const char* name, int slot, int cap_slot, const CUtensorMap& ma, const CUtensorMap& mb0,
+                       const CUtensorMap& mb1, const TileArgs& a, int64_t pairs_upper, cudaStream_t st) {
     if (!ensure_smem(tile_pair_gemm_kernel<MODE>, slot, kPairSmemBytes)) return MOE_ERR_CUDA;
     const int cap = pair_capacity(tile_pair_gemm_kernel<MODE>, kPairSmemBytes, cap_slot);
     if (cap <= 0) return MOE_ERR_UNSUPPORTED;
     return launch(name, st, [&] {
         return klaunch(tile_pair_gemm_kernel<MODE>, pair_grid(pairs_upper, cap), kTcThreads, kPairSmemBytes, st, ma,
-                       mb, mb, a);
+                       mb0, mb1, a);
     });
 }
 
@@ -660,48 +655,34 @@ moe_status run_backward(const moe_shape& s, const __nv_bfloat16* x, const __nv_b
     __nv_bfloat16* dys = reinterpret_cast<__nv_bfloat16*>(ws + B.dys);
     __nv_bfloat16* duv = reinterpret_cast<__nv_bfloat16*>(ws + B.duv);
     float* dxp = reinterpret_cast<float*>(ws + B.dxp);
-    __nv_bfloat16* w2t = reinterpret_cast<__nv_bfloat16*>(ws + B.w2t);
-    __nv_bfloat16* w13t = reinterpret_cast<__nv_bfloat16*>(ws + B.w13t);
-    __nv_bfloat16* dyst = reinterpret_cast<__nv_bfloat16*>(ws + B.dyst);
-    __nv_bfloat16* ht = reinterpret_cast<__nv_bfloat16*>(ws + B.ht);
-    __nv_bfloat16* duvt = reinterpret_cast<__nv_bfloat16*>(ws + B.duvt);
-    __nv_bfloat16* xpt = reinterpret_cast<__nv_bfloat16*>(ws + B.xpt);
     float* part = reinterpret_cast<float*>(ws + B.dwg);
     const int sms = sm_count();
 
-    // transposed weights: W2^T [E][ffn][d] and [W1^T | W3^T] [E][d][2 ffn]
-    MOE_TRY(launch("bwd_transpose_w", st, [&] {
-        return klaunch(transpose_w_kernel, dim3(F / kTrTile, d / kTrTile, E), kTrThreads, 0, st, w2, d, F, w2t, d, 0);
-    }));
-    MOE_TRY(launch("bwd_transpose_w", st, [&] {
-        return klaunch(transpose_w_kernel, dim3(d / kTrTile, F / kTrTile, E), kTrThreads, 0, st, w1, F, d, w13t,
-                       2 * F, 0);
-    }));
-    MOE_TRY(launch("bwd_transpose_w", st, [&] {
-        return klaunch(transpose_w_kernel, dim3(d / kTrTile, F / kTrTile, E), kTrThreads, 0, st, w3, F, d, w13t,
-                       2 * F, F);
-    }));
-    // per slot: dYs = g dy, dg = <dy, E(x)>; per token: the scores' gradient
+    // per slot: dYs = g dy (padded order, pad rows of dYs and dUV zeroed),
+    // dg = <dy, E(x)>; per token: the scores' gradient
     MOE_TRY(launch("bwd_slot", st, [&] {
-        return klaunch(bwd_slot_kernel, (int)std::max<int64_t>(1, std::min<int64_t>((R + 7) / 8, (int64_t)sms * 8)),
-                       256, 0, st, dy, y_slot, perm_token, perm_w, offsets, E, d, dys, dg);
+        return klaunch(bwd_slot_kernel, (int)std::max<int64_t>(1, std::min<int64_t>((B.rp + 7) / 8, (int64_t)sms * 8)),
+                       256, 0, st, dy, y_slot, perm_token, perm_w, offsets, E, d, F, B.rp, dys, duv, dg);
     }));
     MOE_TRY(launch("bwd_router", st, [&] {
         return klaunch(bwd_router_kernel, (int)std::min<int64_t>((T + 255) / 256, (int64_t)sms * 4), 256, 0, st, idx,
                        gw, slot_row, dg, logits, counts, T, E, aux_coef, dl);
     }));
-    // dh = dYs W2, then du, dv with the kept u, v
+    // dh = dYs W2 (W2 read as stored), then du, dv with the kept u, v
     const int64_t token_tiles = (R + kPairM - 1) / kPairM + E;
-    CUtensorMap ma, mb;
-    if (!make_map(&ma, dys, d, R, 128) || !make_map(&mb, w2t, d, (uint64_t)E * F, 128)) return MOE_ERR_CUDA;
-    TileArgs a_dh{offsets, nullptr, duv, E, d, F / kTileN, F, 2 * F, g.timeout_ns};
+    CUtensorMap ma, mb0, mb1;
+    if (!make_map(&ma, dys, d, (uint64_t)B.rp, 128) || !make_map(&mb0, w2, F, (uint64_t)E * d, 64))
+        return MOE_ERR_CUDA;
+    TileArgs a_dh{offsets, nullptr, duv, E, d, F / kTileN, d, 2 * F, g.timeout_ns};
     a_dh.u_in = U;
     a_dh.v_in = V;
-    MOE_TRY(launch_pair<PM_BWD_DH>("bwd_dh_swiglu", 8, 2, ma, mb, a_dh, token_tiles * (F / kTileN), st));
-    // dXp = [du dv] [W1; W3]
-    if (!make_map(&ma, duv, 2 * F, R, 128) || !make_map(&mb, w13t, 2 * F, (uint64_t)E * d, 128)) return MOE_ERR_CUDA;
-    TileArgs a_dx{offsets, nullptr, dxp, E, 2 * F, d / kTileN, d, d, g.timeout_ns};
-    MOE_TRY(launch_pair<PM_BWD_DX>("bwd_dx", 9, 3, ma, mb, a_dx, token_tiles * (d / kTileN), st));
+    MOE_TRY(launch_pair<PM_BWD_DH>("bwd_dh_swiglu", 8, 2, ma, mb0, mb0, a_dh, token_tiles * (F / kTileN), st));
+    // dXp = [du dv] [W1; W3] (W1, W3 read as stored)
+    if (!make_map(&ma, duv, 2 * F, (uint64_t)B.rp, 128) || !make_map(&mb0, w1, d, (uint64_t)E * F, 64) ||
+        !make_map(&mb1, w3, d, (uint64_t)E * F, 64))
+        return MOE_ERR_CUDA;
+    TileArgs a_dx{offsets, nullptr, dxp, E, 2 * F, d / kTileN, F, d, g.timeout_ns};
+    MOE_TRY(launch_pair<PM_BWD_DX>("bwd_dx", 9, 3, ma, mb0, mb1, a_dx, token_tiles * (d / kTileN), st));
     // dx = both slots + the router's part
     MOE_TRY(launch("bwd_combine", st, [&] {
         return klaunch(bwd_combine_kernel, (int)std::min<int64_t>((T * (d / 4) + 255) / 256, (int64_t)sms * 8), 256, 0,
@@ -715,33 +696,23 @@ moe_status run_backward(const moe_shape& s, const __nv_bfloat16* x, const __nv_b
         return klaunch(dwg_final_kernel, (int)std::min<int64_t>(((int64_t)E * d + 255) / 256, (int64_t)sms * 4), 256,
                        0, st, part, B.nchunks, d, E, dwg);
     }));
-    // token-transposed activations, each expert's tokens from a multiple of 64
-    auto tr = [&](const __nv_bfloat16* in, int cols, __nv_bfloat16* out) {
-        return launch("bwd_transpose_tok", st, [&] {
-            return klaunch(transpose_tok_kernel, dim3(cols / kTrTile, (unsigned)(B.rp / kTrTile)), kTrThreads, 0, st,
-                           in, offsets, E, cols, out, B.rp);
-        });
-    };
-    MOE_TRY(tr(dys, d, dyst));
-    MOE_TRY(tr(H, F, ht));
-    MOE_TRY(tr(duv, 2 * F, duvt));
-    MOE_TRY(tr(x_perm, d, xpt));
-    // dW2[e] = dYs_e^T H_e
-    if (!make_map(&ma, dyst, (uint64_t)B.rp, d, 128) || !make_map(&mb, ht, (uint64_t)B.rp, F, 128)) return MOE_ERR_CUDA;
+    // dW2[e] = dYs_e^T H_e, both read as stored (token rows)
+    if (!make_map(&ma, dys, d, (uint64_t)B.rp, 64) || !make_map(&mb0, H, F, R, 64)) return MOE_ERR_CUDA;
     TileArgs a_w2{offsets, nullptr, dw2, E, 0, F / kTileN, 0, F, g.timeout_ns};
     a_w2.m_tiles = d / kPairM;
     a_w2.split_rows = d;
     a_w2.out_estride = (int64_t)d * F;
-    MOE_TRY(launch_pair<PM_WGRAD>("bwd_dw2", 10, 4, ma, mb, a_w2, (int64_t)E * (d / kPairM) * (F / kTileN), st));
+    MOE_TRY(launch_pair<PM_WGRAD>("bwd_dw2", 10, 4, ma, mb0, mb0, a_w2, (int64_t)E * (d / kPairM) * (F / kTileN), st));
     // [dW1; dW3][e] = [du dv]_e^T Xp_e
-    if (!make_map(&ma, duvt, (uint64_t)B.rp, 2 * (uint64_t)F, 128) || !make_map(&mb, xpt, (uint64_t)B.rp, d, 128))
+    if (!make_map(&ma, duv, 2 * (uint64_t)F, (uint64_t)B.rp, 64) || !make_map(&mb0, x_perm, d, R, 64))
         return MOE_ERR_CUDA;
     TileArgs a_w13{offsets, nullptr, dw1, E, 0, d / kTileN, 0, d, g.timeout_ns};
     a_w13.out2 = dw3;
     a_w13.m_tiles = 2 * F / kPairM;
     a_w13.split_rows = F;
     a_w13.out_estride = (int64_t)F * d;
-    return launch_pair<PM_WGRAD>("bwd_dw13", 10, 4, ma, mb, a_w13, (int64_t)E * (2 * F / kPairM) * (d / kTileN), st);
+    return launch_pair<PM_WGRAD>("bwd_dw13", 10, 4, ma, mb0, mb0, a_w13,
+                                 (int64_t)E * (2 * F / kPairM) * (d / kTileN), st);
 }
 
 // Scratch of moe_layer_forward_noalloc: a fixed array of static device memory,

@@ -3,7 +3,7 @@
 The oracle's gradients are pinned to central finite differences of the forward
 definition (test_oracle_backward_pins.py). The GPU keeps u, v, h, g*dy and
 du, dv in bf16 between its contractions (fp32 accumulation), so each gradient
-is held to max|err| <= 3e-2 * max|ref| (BWD_TOL); indices are exact and an
+is held to max|err| <= 2e-2 * max|ref| (BWD_TOL; measured 1.5e-3 to 4.2e-3); indices are exact and an
 expert with no tokens must get exactly zero.
 """
 import numpy as np
@@ -18,7 +18,7 @@ from gpu_harness import TOL, assert_status_ok, upload
 
 pytestmark = pytest.mark.gpu
 
-BWD_TOL = 3e-2
+BWD_TOL = 2e-2
 NAMES = ("dx", "dw_gate", "dw1", "dw3", "dw2")
 
 
