@@ -206,9 +206,9 @@ moe_status moe_layer_forward_noalloc(const moe_shape* s, const void* x, const vo
 size_t moe_train_state_bytes(const moe_shape* s);
 
 /* Bytes of the workspace of moe_layer_backward (0 on an unsupported shape):
- * transposed weights, per-slot gradients and token-transposed activations
- * (about 4.7 GB of transposed weights plus 130 KB per token at the Mixtral
- * shape). */
+ * the per-slot gradients g*dy, [du dv] and dx before the combine (about 160 KB
+ * per token at the Mixtral shape) and the router's partial sums. No weight is
+ * copied: the backward GEMMs read W1, W3, W2 as stored. */
 size_t moe_backward_workspace_bytes(const moe_shape* s);
 
 /* Forward pass that keeps its intermediates for the backward pass.
