@@ -88,7 +88,10 @@ const char* moe_status_string(moe_status s);
  * shape). Covers routing arrays, x_perm, the hidden activations and y_slot. */
 size_t moe_workspace_bytes(const moe_shape* s);
 
-/* Workspace bytes needed by moe_expert_ffn for this shape (0 on a bad shape). */
+/* Workspace bytes needed by moe_expert_ffn for this shape (0 on a bad shape).
+ * moe_expert_ffn and this call accept any s->E from 1 to 8 (a rank of an
+ * expert-parallel layer holds a share of the experts); the other calls need
+ * E = 8, k = 2. */
 size_t moe_ffn_workspace_bytes(const moe_shape* s);
 
 /* Router (lecture router walkthrough; flashpapers "How It Works";
@@ -136,7 +139,10 @@ size_t moe_permute_workspace_bytes(const moe_shape* s);
  *   ws / ws_bytes: workspace of at least moe_ffn_workspace_bytes(s) bytes.
  * The bf16 path accumulates in fp32 and rounds SiLU(u)*v to bf16 before the
  * W2 product. Experts with no rows read none of their weights. The row counts
- * stay on the device: the host never waits for them. */
+ * stay on the device: the host never waits for them. Each expert may hold at
+ * most T rows (true of any top-2 routing, where a token picks two different
+ * experts); a larger group latches MOE_ERR_DEVICE_CHECK on the decode-sized
+ * path (T <= 64), which then skips the experts' work. */
 moe_status moe_expert_ffn(const moe_shape* s, const void* x_perm, const int32_t* offsets,
                           const float* perm_w, const void* w1, const void* w3, const void* w2,
                           float* y_slot, void* ws, size_t ws_bytes, void* stream);
@@ -186,6 +192,14 @@ moe_status moe_layer_forward(const moe_shape* s, const void* x, const void* w_ga
 moe_status moe_layer_forward_noalloc(const moe_shape* s, const void* x, const void* w_gate,
                                      const void* w1, const void* w3, const void* w2, void* y,
                                      void* stream);
+
+/* Row gather (library plumbing for expert parallelism; the pages have no
+ * counterpart): dst[r] = src[index[r]] for r < rows, rows of row_bytes bytes
+ * (a multiple of 16). An index outside [0, src_rows) writes a row of zeros and
+ * latches MOE_ERR_DEVICE_CHECK. src, index, dst: device memory, 16-byte
+ * aligned; src and dst must not overlap. */
+moe_status moe_gather_rows(const void* src, int64_t src_rows, const int32_t* index, int64_t rows,
+                           int64_t row_bytes, void* dst, void* stream);
 
 /* ---------------------------------------------------------------- training
  * The pages train the router and the experts end to end and add the

@@ -185,6 +185,16 @@ moe_status check_shape(const moe_shape* s) {
     return MOE_OK;
 }
 
+// The expert FFN alone runs any number of experts from 1 to 8 (an
+// expert-parallel rank holds a share of them); k does not enter it.
+moe_status check_ffn_shape(const moe_shape* s) {
+    if (s == nullptr || s->E < 1 || s->E > kMaxExperts) return s == nullptr ? MOE_ERR_INVALID_ARG : MOE_ERR_UNSUPPORTED;
+    moe_shape t = *s;
+    t.E = 8;
+    t.k = 2;
+    return check_shape(&t);
+}
+
 bool ok_ptr(const void* p) { return p != nullptr && aligned16(p); }
 
 size_t esize(const moe_shape& s) { return s.dtype == MOE_BF16 ? 2 : 4; }
@@ -764,7 +774,7 @@ size_t moe_workspace_bytes(const moe_shape* s) {
 }
 
 size_t moe_ffn_workspace_bytes(const moe_shape* s) {
-    if (check_shape(s) != MOE_OK) return 0;
+    if (check_ffn_shape(s) != MOE_OK) return 0;
     if (s->dtype == MOE_BF16 && choose_path(*s) == 0) return 0;
     return ffn_layout(*s).total;
 }
@@ -799,7 +809,7 @@ moe_status moe_permute(const moe_shape* s, const int32_t* topk_idx, const float*
 moe_status moe_expert_ffn(const moe_shape* s, const void* x_perm, const int32_t* offsets, const float* perm_w,
                           const void* w1, const void* w3, const void* w2, float* y_slot, void* ws, size_t ws_bytes,
                           void* stream) {
-    MOE_TRY(check_shape(s));
+    MOE_TRY(check_ffn_shape(s));
     if (s->T == 0) return MOE_OK;
     if (!ok_ptr(x_perm) || !ok_ptr(offsets) || !ok_ptr(perm_w) || !ok_ptr(w1) || !ok_ptr(w3) || !ok_ptr(w2) ||
         !ok_ptr(y_slot) || !ok_ptr(ws))
@@ -870,6 +880,20 @@ moe_status moe_layer_forward_noalloc(const moe_shape* s, const void* x, const vo
     if (scratch == nullptr) return MOE_ERR_CUDA;
     return moe_layer_forward(s, x, w_gate, w1, w3, w2, y, nullptr, nullptr, nullptr, scratch, kNoAllocScratchBytes,
                              stream);
+}
+
+moe_status moe_gather_rows(const void* src, int64_t src_rows, const int32_t* index, int64_t rows, int64_t row_bytes,
+                           void* dst, void* stream) {
+    if (rows < 0 || src_rows < 0 || row_bytes <= 0 || row_bytes % 16 != 0) return MOE_ERR_INVALID_ARG;
+    if (rows == 0) return MOE_OK;
+    if (!ok_ptr(src) || !ok_ptr(index) || !ok_ptr(dst)) return MOE_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int64_t chunks = rows * (row_bytes / 16);
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((chunks + 1023) / 1024, (int64_t)sm_count() * 8));
+    return launch("gather_rows", st, [&] {
+        return klaunch(gather_index_kernel, grid, 256, 0, st, static_cast<const unsigned char*>(src), src_rows, index,
+                       rows, row_bytes, static_cast<unsigned char*>(dst));
+    });
 }
 
 size_t moe_train_state_bytes(const moe_shape* s) {

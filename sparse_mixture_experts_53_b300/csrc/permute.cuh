@@ -433,4 +433,42 @@ __global__ void __launch_bounds__(kPlaceThreads)
     }
 }
 
+// dst[r] = src[index[r]] for r < rows, 16-byte copies, four in flight per
+// thread; an index outside [0, src_rows) gives a row of zeros and latches
+// MOE_ERR_DEVICE_CHECK. Used to move rows between the ranks' buffers of an
+// expert-parallel layer laid out in one allocation, and to regroup them.
+__global__ void __launch_bounds__(256)
+    gather_index_kernel(const unsigned char* __restrict__ src, int64_t src_rows, const int32_t* __restrict__ index,
+                        int64_t rows, int64_t row_bytes, unsigned char* __restrict__ dst) {
+    pdl_trigger();
+    pdl_wait();
+    const int64_t c16 = row_bytes / 16;
+    const int64_t n = rows * c16;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    bool bad = false;
+    for (int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i0 < n; i0 += 4 * stride) {
+        uint4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int64_t i = i0 + u * stride;
+            v[u] = make_uint4(0, 0, 0, 0);
+            if (i < n) {
+                const int64_t r = i / c16, c = i - r * c16;
+                const int64_t s = index[r];
+                if (s >= 0 && s < src_rows) v[u] = reinterpret_cast<const uint4*>(src + s * row_bytes)[c];
+                else bad = true;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int64_t i = i0 + u * stride;
+            if (i < n) {
+                const int64_t r = i / c16, c = i - r * c16;
+                reinterpret_cast<uint4*>(dst + r * row_bytes)[c] = v[u];
+            }
+        }
+    }
+    if (bad) report_error(MOE_ERR_DEVICE_CHECK, K_GATHER, W_INDEX);
+}
+
 }  // namespace moe

@@ -39,7 +39,7 @@ EXPORTED = (
     "moe_route_top2", "moe_permute", "moe_expert_ffn", "moe_combine", "moe_aux_stats",
     "moe_layer_forward", "moe_layer_forward_noalloc", "moe_get_device_status", "moe_set_wait_timeout_ns", "moe_set_knob",
     "moe_timing_enable", "moe_timing_read", "moe_train_state_bytes", "moe_backward_workspace_bytes",
-    "moe_layer_forward_train", "moe_layer_backward",
+    "moe_layer_forward_train", "moe_layer_backward", "moe_gather_rows",
 )
 
 
@@ -81,6 +81,7 @@ def _load() -> ctypes.CDLL:
         "moe_set_knob": ([ctypes.c_int32, ctypes.c_int64], I),
         "moe_timing_enable": ([ctypes.c_int32], I),
         "moe_timing_read": ([ctypes.c_char_p, ctypes.c_size_t], I),
+        "moe_gather_rows": ([P, ctypes.c_int64, P, ctypes.c_int64, ctypes.c_int64, P, P], I),
         "moe_train_state_bytes": ([S], ctypes.c_size_t),
         "moe_backward_workspace_bytes": ([S], ctypes.c_size_t),
         "moe_layer_forward_train": ([S, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P], I),
@@ -197,6 +198,14 @@ def moe_layer_forward_noalloc(shape, x, w_gate, w1, w3, w2, y, stream=None):
     """moe_layer_forward on the library's fixed static scratch (no workspace, no allocation)."""
     _check("moe_layer_forward_noalloc", lib.moe_layer_forward_noalloc(
         ctypes.byref(shape), _ptr(x), _ptr(w_gate), _ptr(w1), _ptr(w3), _ptr(w2), _ptr(y), _stream(stream)))
+
+
+def moe_gather_rows(src, index, dst, stream=None):
+    """dst[r] = src[index[r]] (rows of src's trailing dimensions); index is int32 on the device."""
+    rows = index.numel()
+    row_bytes = dst[0].numel() * dst.element_size() if rows else 16
+    _check("moe_gather_rows", lib.moe_gather_rows(_ptr(src), src.shape[0], _ptr(index), rows, row_bytes, _ptr(dst),
+                                                  _stream(stream)))
 
 
 def moe_train_state_bytes(shape: moe_shape) -> int:
