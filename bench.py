@@ -452,6 +452,45 @@ def run_training(args) -> dict:
     }
 
 
+def run_ep(args) -> dict:
+    """Expert parallelism emulated on one GPU: the workload's tokens split over N ranks, each rank's
+    expert FFNs timed, for the contiguous and the load-balanced expert placement."""
+    import numpy as np
+    import torch
+
+    from moe_inputs import CONFIGS, make_config
+    from sparse_mixture_experts_53_b300 import ep
+
+    torch.cuda.set_device(0)
+    N = args.ep
+    cfg = CONFIGS[args.config]
+    L = make_config(args.config)
+    T = cfg["T"]
+    if T % N:
+        raise SystemExit("the workload's tokens must split evenly over the ranks")
+    xs = [L.x[s * T // N:(s + 1) * T // N].cuda() for s in range(N)]
+    wg, w1, w3, w2 = L.w_gate.cuda(), L.w1.cuda(), L.w3.cuda(), L.w2.cuda()
+    out = {}
+    load = None
+    for name in ("contiguous", "balanced"):
+        owner = ep.contiguous_owners(8, N) if name == "contiguous" else ep.balanced_owners(load, N)
+        for _ in range(max(1, args.warmup // 3)):
+            ep.emulate(xs, wg, w1, w3, w2, owner)
+        runs = [ep.emulate(xs, wg, w1, w3, w2, owner, time_experts=True) for _ in range(3)]
+        p = runs[-1][1]
+        ms = np.median(np.array([r[2] for r in runs]), axis=0)
+        load = p.counts.sum(0)
+        out[name] = {"owner": p.owner.tolist(), "rows_per_rank": p.rows_per_rank.tolist(),
+                     "expert_ms_per_rank": [round(float(v), 4) for v in ms],
+                     "max_over_mean": round(float(ms.max() / ms.mean()), 3),
+                     "tokens_per_s_if_ranks_in_parallel": round(T / (ms.max() * 1e-3), 1)}
+    return {"metric": "expert-parallel emulation: per-rank expert FFN time", "ep_ranks": N,
+            "config": {"workload": cfg["name"], "T": T, "tokens_per_rank": T // N},
+            "expert_load": [int(v) for v in load], "placements": out,
+            "note": "ranks run one after another on one GPU; a rank's time is its own experts' FFN on the rows "
+                    "it received, the quantity the slowest rank of a real expert-parallel step is bound by"}
+
+
 def cpu_baseline(k: int, max_tokens: int | None = None, budget_s: float = 20.0) -> dict:
     """The fp64 oracle, as it stands, on a bounded sample of the workload's tokens."""
     import oracle
@@ -521,6 +560,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--pdl", type=int, default=1, choices=[0, 1],
                     help="programmatic dependent launch between the library's kernels")
+    ap.add_argument("--ep", type=int, default=0,
+                    help="emulate N expert-parallel ranks on one GPU and time each rank's experts")
     ap.add_argument("--train", action="store_true",
                     help="time a training step (forward that keeps its state + backward) instead of the forward")
     ap.add_argument("--tile-ctas", type=int, default=2, choices=[1, 2],
@@ -529,6 +570,9 @@ def main():
     if args.warmup < 3:
         args.warmup = 3
     rank, world, local = _dist_env()
+    if args.ep:
+        print(json.dumps(run_ep(args)), flush=True)
+        return
     if args.train:
         if args.impl != "ours" or world != 1:
             raise SystemExit("--train times this library's training step on one GPU")
