@@ -290,20 +290,45 @@ def run_ours(args, rank, world, local) -> dict | None:
     kern = moe.moe_timing_read()
     moe.moe_timing_enable(False)
 
-    # ---- end to end through the public call, host buffers: copy x in, y out
+    # ---- end to end through the public call with host buffers: every step copies its tokens in from
+    # pinned host memory and reads its output back. Input and output copies run on their own streams
+    # (both directions of the link at once) with two device buffers each way, so step i+1's input copy
+    # and step i's output copy overlap neighbouring steps' kernels, as a serving loop would run them.
     x_host = L.x.pin_memory()
-    y_host = torch.empty_like(L.x).pin_memory()
-    for _ in range(2):
-        x.copy_(x_host, non_blocking=True)
-        step()
-        y_host.copy_(y, non_blocking=True)
+    y_host = [torch.empty_like(L.x).pin_memory() for _ in range(2)]
+    xb = [torch.empty_like(x) for _ in range(2)]
+    yb = [torch.empty_like(x) for _ in range(2)]
+    cin, cout = torch.cuda.Stream(), torch.cuda.Stream()
+    h2d = [torch.cuda.Event() for _ in range(2)]
+    comp = [torch.cuda.Event() for _ in range(2)]
+    d2h = [torch.cuda.Event() for _ in range(2)]
+
+    def e2e_steps(n):
+        for i in range(n):
+            b = i & 1
+            with torch.cuda.stream(cin):
+                if i >= 2:
+                    cin.wait_event(comp[b])  # xb[b] is free once step i-2 has run
+                xb[b].copy_(x_host, non_blocking=True)
+                h2d[b].record(cin)
+            stream.wait_event(h2d[b])
+            if i >= 2:
+                stream.wait_event(d2h[b])  # yb[b] has been read back
+            moe.moe_layer_forward(shape, xb[b], wg, w1, w3, w2, yb[b], ws, stats, stream)
+            comp[b].record(stream)
+            with torch.cuda.stream(cout):
+                cout.wait_event(comp[b])
+                y_host[b].copy_(yb[b], non_blocking=True)
+                d2h[b].record(cout)
+        stream.wait_stream(cout)
+
+    e2e_steps(3)
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
-        x.copy_(x_host, non_blocking=True)
-        step()
-        y_host.copy_(y, non_blocking=True)
+    cin.wait_stream(stream)
+    cout.wait_stream(stream)
+    e2e_steps(args.steps)
     e1.record(stream)
     barrier()
     e2e_ms = e0.elapsed_time(e1) / args.steps
@@ -362,7 +387,8 @@ def run_ours(args, rank, world, local) -> dict | None:
         "gpu_launches": int(round(launches_per_step * args.steps)),
         "e2e": {"value": throughput(cfg["T"], world, e2e_ms), "unit": UNIT,
                 "h2d_bytes_per_step": int(L.x.numel() * L.x.element_size()),
-                "d2h_bytes_per_step": int(L.x.numel() * L.x.element_size()), "ms_per_step": round(e2e_ms, 5)},
+                "d2h_bytes_per_step": int(L.x.numel() * L.x.element_size()), "ms_per_step": round(e2e_ms, 5),
+                "copies": "pinned host buffers; input and output copies on two streams overlap neighbouring steps"},
         "clocks": sampler.summary(),
     }
     ranks.close()

@@ -400,29 +400,34 @@ constexpr size_t kPairSmemBytes = 1024 + (size_t)kPairStages * kPairStageBytes +
 enum PairMode : int { PM_UP = 0, PM_DOWN = 1, PM_BWD_DH = 2, PM_BWD_DX = 3, PM_WGRAD = 4 };
 
 // Epilogue of one row of a PM_BWD_DH tile: 256 columns f of dh, the kept u
-// and v of the same row and columns, du and dv out in bf16.
+// and v of the same row and columns, du and dv out in bf16. The u, v loads of
+// the next 16 columns are issued before the current ones are used, so their
+// latency overlaps the tensor-memory load and the arithmetic.
 __device__ __forceinline__ void bwd_dh_epilogue(uint32_t taddr, bool valid, int64_t r, int64_t pr, int nt,
                                                 const TileArgs& args) {
     const int F = args.ldo / 2;
     const int64_t col0 = (int64_t)nt * kTileN;
-    const __nv_bfloat16* urow = args.u_in + r * F + col0;
-    const __nv_bfloat16* vrow = args.v_in + r * F + col0;
+    const uint4* urow = reinterpret_cast<const uint4*>(args.u_in + r * F + col0);
+    const uint4* vrow = reinterpret_cast<const uint4*>(args.v_in + r * F + col0);
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(args.out) + pr * args.ldo + col0;
+    const uint4 zero = make_uint4(0, 0, 0, 0);
+    uint4 un[2] = {zero, zero}, vn[2] = {zero, zero};
+    if (valid) {
+        un[0] = urow[0]; un[1] = urow[1];
+        vn[0] = vrow[0]; vn[1] = vrow[1];
+    }
 #pragma unroll 1
     for (int j = 0; j < kTileN; j += 16) {
+        const uint4 uc[2] = {un[0], un[1]}, vc[2] = {vn[0], vn[1]};
+        if (valid && j + 16 < kTileN) {
+            un[0] = urow[(j + 16) / 8]; un[1] = urow[(j + 16) / 8 + 1];
+            vn[0] = vrow[(j + 16) / 8]; vn[1] = vrow[(j + 16) / 8 + 1];
+        }
         uint32_t a[16];
         tmem_ld16(taddr + j, a);
-        uint4 uraw[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
-        uint4 vraw[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
-        if (valid) {
-            uraw[0] = reinterpret_cast<const uint4*>(urow + j)[0];
-            uraw[1] = reinterpret_cast<const uint4*>(urow + j)[1];
-            vraw[0] = reinterpret_cast<const uint4*>(vrow + j)[0];
-            vraw[1] = reinterpret_cast<const uint4*>(vrow + j)[1];
-        }
         tmem_wait_ld();
-        const __nv_bfloat16* uu = reinterpret_cast<const __nv_bfloat16*>(uraw);
-        const __nv_bfloat16* vv = reinterpret_cast<const __nv_bfloat16*>(vraw);
+        const __nv_bfloat16* uu = reinterpret_cast<const __nv_bfloat16*>(uc);
+        const __nv_bfloat16* vv = reinterpret_cast<const __nv_bfloat16*>(vc);
         uint32_t pdu[8], pdv[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -432,7 +437,7 @@ __device__ __forceinline__ void bwd_dh_epilogue(uint32_t taddr, bool valid, int6
                 const float dh = __uint_as_float(a[2 * i + q]);
                 const float u = __bfloat162float(uu[2 * i + q]);
                 const float v = __bfloat162float(vv[2 * i + q]);
-                const float sg = 1.0f / (1.0f + expf(-u));
+                const float sg = __fdividef(1.0f, 1.0f + __expf(-u));
                 du2[q] = dh * v * (sg * (1.0f + u * (1.0f - sg)));
                 dv2[q] = dh * (u * sg);
             }
