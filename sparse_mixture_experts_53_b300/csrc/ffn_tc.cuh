@@ -455,24 +455,35 @@ __device__ __forceinline__ void bwd_dh_epilogue(uint32_t taddr, bool valid, int6
     }
 }
 
-// Epilogue of one row of a PM_WGRAD tile: 256 fp32 columns of the gradient
-// (zeros when the expert had no tokens, i.e. no MMA wrote the accumulator).
-__device__ __forceinline__ void wgrad_epilogue(uint32_t taddr, bool any_k, int e, int row, int nt,
-                                               const TileArgs& args) {
-    float* base = row < args.split_rows ? reinterpret_cast<float*>(args.out) : args.out2;
-    const int rr = row < args.split_rows ? row : row - args.split_rows;
-    float* out = base + (int64_t)e * args.out_estride + (int64_t)rr * args.ldo + (int64_t)nt * kTileN;
+// Epilogue of a PM_WGRAD tile for one warp (32 rows of the gradient, 256
+// fp32 columns; zeros when the expert had no tokens, i.e. no MMA wrote the
+// accumulator). Each 32-column block goes through the warp's 32 x 33 staging
+// array in shared memory, so every store writes 32 consecutive floats of one
+// row (one 128-byte line) instead of 16 bytes of 32 different rows.
+constexpr int kWgradStageFloats = 32 * 33;
+constexpr size_t kWgradStageBytes = 4 * kWgradStageFloats * sizeof(float);
+
+__device__ __forceinline__ void wgrad_epilogue(uint32_t taddr, bool any_k, int e, int row0, int nt, int lane,
+                                               float* stage, const TileArgs& args) {
+    // the warp's rows lie in one gradient matrix (split_rows is a multiple of 256)
+    float* base = row0 < args.split_rows ? reinterpret_cast<float*>(args.out) : args.out2;
+    const int r0 = row0 < args.split_rows ? row0 : row0 - args.split_rows;
+    float* out = base + (int64_t)e * args.out_estride + (int64_t)r0 * args.ldo + (int64_t)nt * kTileN + lane;
 #pragma unroll 1
-    for (int j = 0; j < kTileN; j += 16) {
-        uint32_t a[16];
+    for (int j = 0; j < kTileN; j += 32) {
+        uint32_t a[16], b[16];
         tmem_ld16(taddr + j, a);
+        tmem_ld16(taddr + j + 16, b);
         tmem_wait_ld();
-        float4* dst = reinterpret_cast<float4*>(out + j);
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-            dst[i] = any_k ? make_float4(__uint_as_float(a[4 * i]), __uint_as_float(a[4 * i + 1]),
-                                         __uint_as_float(a[4 * i + 2]), __uint_as_float(a[4 * i + 3]))
-                           : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int c = 0; c < 16; ++c) {
+            stage[lane * 33 + c] = any_k ? __uint_as_float(a[c]) : 0.f;
+            stage[lane * 33 + 16 + c] = any_k ? __uint_as_float(b[c]) : 0.f;
+        }
+        __syncwarp();
+#pragma unroll 4
+        for (int rr = 0; rr < 32; ++rr) out[(int64_t)rr * args.ldo + j] = stage[rr * 33 + lane];
+        __syncwarp();
     }
 }
 
@@ -700,7 +711,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
             tc_fence_after();
             const uint32_t taddr = tmem_base + b * kTileAccCols + ((uint32_t)(sub * 32) << 16);
             if (WG) {
-                wgrad_epilogue(taddr, ksteps(e) > 0, e, mt * kPairM + row_in_tile, nt, args);
+                float* stage = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(ctl) +
+                                                        ((sizeof(TcControl) + 15) & ~size_t(15))) +
+                               sub * kWgradStageFloats;
+                wgrad_epilogue(taddr, ksteps(e) > 0, e, mt * kPairM + row_in_tile - lane, nt, lane, stage, args);
             } else {
                 const int grow = mt * kPairM + row_in_tile;
                 const bool valid = grow < ctl->cnt[e];

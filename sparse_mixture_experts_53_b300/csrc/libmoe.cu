@@ -630,12 +630,14 @@ bool train_supported(const moe_shape& s) { return s.dtype == MOE_BF16 && s.d % 2
 template <int MODE>
 moe_status launch_pair(const char* name, int slot, int cap_slot, const CUtensorMap& ma, const CUtensorMap& mb0,
                        const CUtensorMap& mb1, const TileArgs& a, int64_t pairs_upper, cudaStream_t st) {
-    if (!ensure_smem(tile_pair_gemm_kernel<MODE>, slot, kPairSmemBytes)) return MOE_ERR_CUDA;
-    const int cap = pair_capacity(tile_pair_gemm_kernel<MODE>, kPairSmemBytes, cap_slot);
+    // the weight-gradient epilogue stages its stores in 4 warps' arrays after the control block
+    const size_t smem = kPairSmemBytes + (MODE == PM_WGRAD ? 16 + kWgradStageBytes : 0);
+    if (!ensure_smem(tile_pair_gemm_kernel<MODE>, slot, smem)) return MOE_ERR_CUDA;
+    const int cap = pair_capacity(tile_pair_gemm_kernel<MODE>, smem, cap_slot);
     if (cap <= 0) return MOE_ERR_UNSUPPORTED;
     return launch(name, st, [&] {
-        return klaunch(tile_pair_gemm_kernel<MODE>, pair_grid(pairs_upper, cap), kTcThreads, kPairSmemBytes, st, ma,
-                       mb0, mb1, a);
+        return klaunch(tile_pair_gemm_kernel<MODE>, pair_grid(pairs_upper, cap), kTcThreads, smem, st, ma, mb0, mb1,
+                       a);
     });
 }
 
