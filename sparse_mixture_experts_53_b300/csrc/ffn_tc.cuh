@@ -118,12 +118,15 @@ struct TileArgs {
 //   down: perm_w[r] * acc in fp32.
 // Every thread of the warp must call it (tcgen05.ld is warp-collective);
 // `valid` only predicates the stores.
+// [j_begin, j_end): the columns this thread handles (up: of the 128 u, v
+// pairs; down: of the 256 columns), multiples of 16.
 template <bool UP>
-__device__ __forceinline__ void tile_epilogue(uint32_t taddr, bool valid, int64_t r, int nt, const TileArgs& args) {
+__device__ __forceinline__ void tile_epilogue(uint32_t taddr, bool valid, int64_t r, int nt, const TileArgs& args,
+                                              int j_begin = 0, int j_end = UP ? kTileM : kTileN) {
     if (UP) {
         __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(args.out) + r * args.ldo + nt * kTileM;
 #pragma unroll 1
-        for (int j = 0; j < kTileM; j += 16) {
+        for (int j = j_begin; j < j_end; j += 16) {
             uint32_t u[16], v[16];
             tmem_ld16(taddr + j, u);
             tmem_ld16(taddr + kTileM + j, v);
@@ -159,7 +162,7 @@ __device__ __forceinline__ void tile_epilogue(uint32_t taddr, bool valid, int64_
         const float pw = valid ? (args.perm_w != nullptr ? args.perm_w[r] : 1.0f) : 0.f;
         float* out = reinterpret_cast<float*>(args.out) + r * args.ldo + nt * kTileN;
 #pragma unroll 1
-        for (int j = 0; j < kTileN; j += 16) {
+        for (int j = j_begin; j < j_end; j += 16) {
             uint32_t a[16];
             tmem_ld16(taddr + j, a);
             tmem_wait_ld();
@@ -374,9 +377,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // ---------------------------------------------------------------------------
 constexpr int kPairM = 256;
 constexpr int kPairStages = 6;
+// CTA-pair kernels: warp 0 TMA, warp 1 MMA, warps 2-9 the epilogue (two warps
+// per tensor-memory lane quarter, each taking half of the tile's columns)
+constexpr int kPairThreads = 320;
+constexpr int kPairEpiWarps = 8;
 constexpr uint32_t kPairHalfBytes = 128 * kBK * 2;          // 16 KB: one CTA's half of A or of B
 constexpr uint32_t kPairStageBytes = 2 * kPairHalfBytes;     // 32 KB per CTA and stage
 constexpr size_t kPairSmemBytes = 1024 + (size_t)kPairStages * kPairStageBytes + sizeof(TcControl);
+// the weight-gradient epilogue's staging arrays, one per epilogue warp, after the control block
+constexpr size_t kWgradStageBytes = 16 + (size_t)kPairEpiWarps * 32 * 33 * sizeof(float);
+static_assert(kPairSmemBytes + kWgradStageBytes <= 227 * 1024, "CTA-pair kernel exceeds the shared memory of a CTA");
 
 // What a CTA-pair tile kernel computes (the tile loop, the TMA ring and the
 // MMA issue are shared; the operands' rows, their major-ness, the K range and
@@ -404,7 +414,7 @@ enum PairMode : int { PM_UP = 0, PM_DOWN = 1, PM_BWD_DH = 2, PM_BWD_DX = 3, PM_W
 // the next 16 columns are issued before the current ones are used, so their
 // latency overlaps the tensor-memory load and the arithmetic.
 __device__ __forceinline__ void bwd_dh_epilogue(uint32_t taddr, bool valid, int64_t r, int64_t pr, int nt,
-                                                const TileArgs& args) {
+                                                const TileArgs& args, int j_begin, int j_end) {
     const int F = args.ldo / 2;
     const int64_t col0 = (int64_t)nt * kTileN;
     const uint4* urow = reinterpret_cast<const uint4*>(args.u_in + r * F + col0);
@@ -413,13 +423,13 @@ __device__ __forceinline__ void bwd_dh_epilogue(uint32_t taddr, bool valid, int6
     const uint4 zero = make_uint4(0, 0, 0, 0);
     uint4 un[2] = {zero, zero}, vn[2] = {zero, zero};
     if (valid) {
-        un[0] = urow[0]; un[1] = urow[1];
-        vn[0] = vrow[0]; vn[1] = vrow[1];
+        un[0] = urow[j_begin / 8]; un[1] = urow[j_begin / 8 + 1];
+        vn[0] = vrow[j_begin / 8]; vn[1] = vrow[j_begin / 8 + 1];
     }
 #pragma unroll 1
-    for (int j = 0; j < kTileN; j += 16) {
+    for (int j = j_begin; j < j_end; j += 16) {
         const uint4 uc[2] = {un[0], un[1]}, vc[2] = {vn[0], vn[1]};
-        if (valid && j + 16 < kTileN) {
+        if (valid && j + 16 < j_end) {
             un[0] = urow[(j + 16) / 8]; un[1] = urow[(j + 16) / 8 + 1];
             vn[0] = vrow[(j + 16) / 8]; vn[1] = vrow[(j + 16) / 8 + 1];
         }
@@ -461,16 +471,15 @@ __device__ __forceinline__ void bwd_dh_epilogue(uint32_t taddr, bool valid, int6
 // array in shared memory, so every store writes 32 consecutive floats of one
 // row (one 128-byte line) instead of 16 bytes of 32 different rows.
 constexpr int kWgradStageFloats = 32 * 33;
-constexpr size_t kWgradStageBytes = 4 * kWgradStageFloats * sizeof(float);
 
 __device__ __forceinline__ void wgrad_epilogue(uint32_t taddr, bool any_k, int e, int row0, int nt, int lane,
-                                               float* stage, const TileArgs& args) {
+                                               float* stage, const TileArgs& args, int j_begin, int j_end) {
     // the warp's rows lie in one gradient matrix (split_rows is a multiple of 256)
     float* base = row0 < args.split_rows ? reinterpret_cast<float*>(args.out) : args.out2;
     const int r0 = row0 < args.split_rows ? row0 : row0 - args.split_rows;
     float* out = base + (int64_t)e * args.out_estride + (int64_t)r0 * args.ldo + (int64_t)nt * kTileN + lane;
 #pragma unroll 1
-    for (int j = 0; j < kTileN; j += 32) {
+    for (int j = j_begin; j < j_end; j += 32) {
         uint32_t a[16], b[16];
         tmem_ld16(taddr + j, a);
         tmem_ld16(taddr + j + 16, b);
@@ -488,7 +497,7 @@ __device__ __forceinline__ void wgrad_epilogue(uint32_t taddr, bool any_k, int e
 }
 
 template <int MODE>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     tile_pair_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b0,
                           const __grid_constant__ CUtensorMap map_b1, const TileArgs args) {
     constexpr bool UP = MODE == PM_UP;
@@ -516,7 +525,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&ctl->tfull[b]), 1);
-            mbar_init(smem_u32(&ctl->tempty[b]), 8);  // 4 epilogue warps in each CTA
+            mbar_init(smem_u32(&ctl->tempty[b]), 2 * kPairEpiWarps);  // the epilogue warps of both CTAs
         }
         mbar_init(smem_u32(&ctl->drain), 1);
         ctl->abort_flag = 0;
@@ -693,9 +702,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------ epilogue (warps 2-5, both CTAs)
-        const int sub = warp & 3;
+        // ------------------------------------------------ epilogue (warps 2-9, both CTAs)
+        const int sub = warp & 3;                 // tensor-memory lanes 32 sub .. 32 sub + 31
+        const int half = (warp - 2) >> 2;         // which half of the tile's columns
         const int row_in_tile = 128 * (int)rank + sub * 32 + lane;
+        constexpr int ncols = UP ? kTileM : kTileN;  // up: u, v pairs
+        const int j_begin = half * (ncols / 2), j_end = j_begin + ncols / 2;
         uint32_t tempty_leader[2];
         for (int b = 0; b < 2; ++b) tempty_leader[b] = mapa_shared(smem_u32(&ctl->tempty[b]), 0);
         int it = 0;
@@ -713,14 +725,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
             if (WG) {
                 float* stage = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(ctl) +
                                                         ((sizeof(TcControl) + 15) & ~size_t(15))) +
-                               sub * kWgradStageFloats;
-                wgrad_epilogue(taddr, ksteps(e) > 0, e, mt * kPairM + row_in_tile - lane, nt, lane, stage, args);
+                               (warp - 2) * kWgradStageFloats;
+                wgrad_epilogue(taddr, ksteps(e) > 0, e, mt * kPairM + row_in_tile - lane, nt, lane, stage, args,
+                               j_begin, j_end);
             } else {
                 const int grow = mt * kPairM + row_in_tile;
                 const bool valid = grow < ctl->cnt[e];
                 const int64_t r = ctl->off[e] + grow;
-                if (MODE == PM_BWD_DH) bwd_dh_epilogue(taddr, valid, r, (int64_t)ctl->koff[e] + grow, nt, args);
-                else tile_epilogue<UP>(taddr, valid, r, nt, args);
+                if (MODE == PM_BWD_DH)
+                    bwd_dh_epilogue(taddr, valid, r, (int64_t)ctl->koff[e] + grow, nt, args, j_begin, j_end);
+                else
+                    tile_epilogue<UP>(taddr, valid, r, nt, args, j_begin, j_end);
             }
             tc_fence_before();
             __syncwarp();

@@ -395,7 +395,7 @@ int pair_capacity(K kernel, size_t smem, int slot) {
     if (cap == 0) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(2 * (sm_count() / 2));
-        cfg.blockDim = dim3(kTcThreads);
+        cfg.blockDim = dim3(kPairThreads);
         cfg.dynamicSmemBytes = smem;
         int n = 0;
         if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n <= 0) {
@@ -452,7 +452,7 @@ moe_status run_ffn(const moe_shape& s, const void* x_perm, const int32_t* offset
             TileArgs up{offsets, perm_w, H, E, d, F / kTileM, F, F, g.timeout_ns, u_out, v_out};
             const int64_t pairs_up = ((R + kPairM - 1) / kPairM + E) * (F / kTileM);
             MOE_TRY(launch("tile_up_swiglu", st, [&] {
-                return klaunch(tile_pair_gemm_kernel<PM_UP>, pair_grid(pairs_up, cap_up), kTcThreads, kPairSmemBytes,
+                return klaunch(tile_pair_gemm_kernel<PM_UP>, pair_grid(pairs_up, cap_up), kPairThreads, kPairSmemBytes,
                                st, ma, mb0, mb1, up);
             }));
             CUtensorMap mh, mw2;
@@ -460,7 +460,7 @@ moe_status run_ffn(const moe_shape& s, const void* x_perm, const int32_t* offset
             TileArgs down{offsets, perm_w, y_slot, E, F, d / kTileN, d, d, g.timeout_ns};
             const int64_t pairs_down = ((R + kPairM - 1) / kPairM + E) * (d / kTileN);
             return launch("tile_down_scale", st, [&] {
-                return klaunch(tile_pair_gemm_kernel<PM_DOWN>, pair_grid(pairs_down, cap_down), kTcThreads,
+                return klaunch(tile_pair_gemm_kernel<PM_DOWN>, pair_grid(pairs_down, cap_down), kPairThreads,
                                kPairSmemBytes, st, mh, mw2, mw2, down);
             });
         }
@@ -631,12 +631,12 @@ template <int MODE>
 moe_status launch_pair(const char* name, int slot, int cap_slot, const CUtensorMap& ma, const CUtensorMap& mb0,
                        const CUtensorMap& mb1, const TileArgs& a, int64_t pairs_upper, cudaStream_t st) {
     // the weight-gradient epilogue stages its stores in 4 warps' arrays after the control block
-    const size_t smem = kPairSmemBytes + (MODE == PM_WGRAD ? 16 + kWgradStageBytes : 0);
+    const size_t smem = kPairSmemBytes + (MODE == PM_WGRAD ? kWgradStageBytes : 0);
     if (!ensure_smem(tile_pair_gemm_kernel<MODE>, slot, smem)) return MOE_ERR_CUDA;
     const int cap = pair_capacity(tile_pair_gemm_kernel<MODE>, smem, cap_slot);
     if (cap <= 0) return MOE_ERR_UNSUPPORTED;
     return launch(name, st, [&] {
-        return klaunch(tile_pair_gemm_kernel<MODE>, pair_grid(pairs_upper, cap), kTcThreads, smem, st, ma, mb0, mb1,
+        return klaunch(tile_pair_gemm_kernel<MODE>, pair_grid(pairs_upper, cap), kPairThreads, smem, st, ma, mb0, mb1,
                        a);
     });
 }
