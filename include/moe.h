@@ -258,6 +258,13 @@ moe_status moe_layer_backward(const moe_shape* s, const void* x, const void* w_g
  * MOE_ERR_CUDA if the device itself reports an error. */
 moe_status moe_get_device_status(int32_t* code, int32_t* detail);
 
+/* Self-test of the device-side timeout path (no counterpart on the pages):
+ * one CTA waits on an mbarrier that nothing arrives on, with the same bounded
+ * wait as the tensor-core kernels. After timeout_ns (1 ns .. 10 s) the wait
+ * gives up, *gave_up (device int32) is set to 1 and MOE_ERR_TIMEOUT is latched
+ * in the status word, as a real stall would; the device stays usable. */
+moe_status moe_selftest_wait_timeout(uint64_t timeout_ns, int32_t* gave_up, void* stream);
+
 /* Upper bound, in nanoseconds, on every device-side wait of the tensor-core
  * kernels (default 2e9). A wait that runs out latches MOE_ERR_TIMEOUT and the
  * kernel returns early after its in-flight copies and MMAs have landed. */

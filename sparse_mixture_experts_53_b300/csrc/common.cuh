@@ -348,4 +348,31 @@ __device__ __forceinline__ float to_f32<float>(float v) { return v; }
 template <>
 __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
 
+// ---------------------------------------------------------------------------
+// Self-test of the bounded waits: thread 0 waits, with the same helper as the
+// tensor-core kernels, on an mbarrier that no thread arrives on. The wait
+// gives up after timeout_ns and the kernel latches MOE_ERR_TIMEOUT, so a host
+// can check the timeout path end to end without faulting the device.
+// ---------------------------------------------------------------------------
+constexpr int K_SELFTEST = 12;
+
+__global__ void wait_selftest_kernel(uint64_t timeout_ns, int* gave_up) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const bool ok = mbar_wait(smem_u32(&bar), 0, timeout_ns, &abort_flag);
+        if (!ok) report_error(MOE_ERR_TIMEOUT, K_SELFTEST, W_MMA);
+        *gave_up = ok ? 0 : 1;
+        // complete the barrier's phase so the CTA leaves it with nothing pending
+        mbar_arrive(smem_u32(&bar));
+    }
+    __syncthreads();
+}
+
 }  // namespace moe

@@ -975,6 +975,13 @@ moe_status moe_layer_backward(const moe_shape* s, const void* x, const void* w_g
                         dw2, static_cast<unsigned char*>(ws), st);
 }
 
+moe_status moe_selftest_wait_timeout(uint64_t timeout_ns, int32_t* gave_up, void* stream) {
+    if (timeout_ns == 0 || timeout_ns > 10000000000ull || !ok_ptr(gave_up)) return MOE_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    wait_selftest_kernel<<<1, 32, 0, st>>>(timeout_ns, gave_up);
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
 moe_status moe_get_device_status(int32_t* code, int32_t* detail) {
     if (code == nullptr) return MOE_ERR_INVALID_ARG;
     if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;

@@ -39,7 +39,7 @@ EXPORTED = (
     "moe_route_top2", "moe_permute", "moe_expert_ffn", "moe_combine", "moe_aux_stats",
     "moe_layer_forward", "moe_layer_forward_noalloc", "moe_get_device_status", "moe_set_wait_timeout_ns", "moe_set_knob",
     "moe_timing_enable", "moe_timing_read", "moe_train_state_bytes", "moe_backward_workspace_bytes",
-    "moe_layer_forward_train", "moe_layer_backward", "moe_gather_rows",
+    "moe_layer_forward_train", "moe_layer_backward", "moe_gather_rows", "moe_selftest_wait_timeout",
 )
 
 
@@ -82,6 +82,7 @@ def _load() -> ctypes.CDLL:
         "moe_timing_enable": ([ctypes.c_int32], I),
         "moe_timing_read": ([ctypes.c_char_p, ctypes.c_size_t], I),
         "moe_gather_rows": ([P, ctypes.c_int64, P, ctypes.c_int64, ctypes.c_int64, P, P], I),
+        "moe_selftest_wait_timeout": ([ctypes.c_uint64, P, P], I),
         "moe_train_state_bytes": ([S], ctypes.c_size_t),
         "moe_backward_workspace_bytes": ([S], ctypes.c_size_t),
         "moe_layer_forward_train": ([S, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P], I),
@@ -230,6 +231,11 @@ def moe_layer_backward(shape, x, w_gate, w1, w3, w2, dy, aux_coef, state, dx, dw
         ctypes.byref(shape), _ptr(x), _ptr(w_gate), _ptr(w1), _ptr(w3), _ptr(w2), _ptr(dy), float(aux_coef),
         _ptr(state), state.numel() * state.element_size(), _ptr(dx), _ptr(dw_gate), _ptr(dw1), _ptr(dw3),
         _ptr(dw2), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def moe_selftest_wait_timeout(timeout_ns: int, gave_up, stream=None):
+    _check("moe_selftest_wait_timeout", lib.moe_selftest_wait_timeout(int(timeout_ns), _ptr(gave_up),
+                                                                      _stream(stream)))
 
 
 def moe_get_device_status() -> tuple[int, int]:

@@ -415,3 +415,18 @@ def test_small_batch_grouping_matches_oracle(T, bad):
         assert np.array_equal(out[k].cpu().numpy().astype(np.int64), ref[k]), k
     assert np.array_equal(out["perm_w"].cpu().numpy(), ref["perm_w"].astype(np.float32))
     assert torch.equal(out["x_perm"].cpu(), L.x[torch.from_numpy(ref["perm_token"])])
+
+
+def test_device_wait_timeout_is_reported_and_the_device_stays_usable():
+    """A wait on a barrier nothing arrives on gives up after its limit and latches MOE_ERR_TIMEOUT."""
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    moe.moe_selftest_wait_timeout(20_000_000, flag)  # 20 ms
+    code, detail = moe.moe_get_device_status()
+    assert code == moe.MOE_ERR_TIMEOUT and detail == 1202
+    assert int(flag) == 1
+    assert_status_ok()  # the read cleared the word
+    # and the device still runs the layer
+    L = _margin_layer(40, 256, 256, "bf16", seed=4)
+    got = run_staged(L)
+    assert_status_ok()
+    check_y(L, got["y"])
