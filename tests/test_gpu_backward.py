@@ -24,11 +24,11 @@ NAMES = ("dx", "dw_gate", "dw1", "dw3", "dw2")
 
 @pytest.fixture(autouse=True)
 def _reset_knobs():
-    for k, v in ((moe.MOE_KNOB_FFN_PATH, 0), (moe.MOE_KNOB_GRID, 0), (moe.MOE_KNOB_TILE_CTAS, 2)):
+    for k, v in ((moe.MOE_KNOB_FFN_PATH, 0), (moe.MOE_KNOB_GRID, 0), (moe.MOE_KNOB_TILE_CTAS, 0)):
         moe.moe_set_knob(k, v)
     moe.moe_get_device_status()
     yield
-    for k, v in ((moe.MOE_KNOB_FFN_PATH, 0), (moe.MOE_KNOB_GRID, 0), (moe.MOE_KNOB_TILE_CTAS, 2)):
+    for k, v in ((moe.MOE_KNOB_FFN_PATH, 0), (moe.MOE_KNOB_GRID, 0), (moe.MOE_KNOB_TILE_CTAS, 0)):
         moe.moe_set_knob(k, v)
 
 

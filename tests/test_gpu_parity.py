@@ -24,13 +24,13 @@ def _reset_knobs():
     moe.moe_set_knob(moe.MOE_KNOB_FFN_PATH, 0)
     moe.moe_set_knob(moe.MOE_KNOB_KSLICE, 0)
     moe.moe_set_knob(moe.MOE_KNOB_GRID, 0)
-    moe.moe_set_knob(moe.MOE_KNOB_TILE_CTAS, 2)
+    moe.moe_set_knob(moe.MOE_KNOB_TILE_CTAS, 0)
     moe.moe_get_device_status()
     yield
     moe.moe_set_knob(moe.MOE_KNOB_FFN_PATH, 0)
     moe.moe_set_knob(moe.MOE_KNOB_KSLICE, 0)
     moe.moe_set_knob(moe.MOE_KNOB_GRID, 0)
-    moe.moe_set_knob(moe.MOE_KNOB_TILE_CTAS, 2)
+    moe.moe_set_knob(moe.MOE_KNOB_TILE_CTAS, 0)
 
 
 def _margin_layer(T, d, ffn, dtype, seed, weights=None, E=8):
