@@ -254,7 +254,11 @@ moe_status moe_layer_backward(const moe_shape* s, const void* x, const void* w_g
 
 /* Synchronises the current device, then reports and clears its status word.
  * *code receives MOE_OK or the first device-side error since the last read;
- * *detail (nullable) receives a kernel/where code for diagnostics. Returns
+ * *detail (nullable) receives 100 * kernel + where for diagnostics, with
+ * kernel 1 router, 2 grouping, 3 row gather, 4 up tiles, 5 down tiles,
+ * 6 streaming up, 7 streaming down, 12 the wait self-test, 13 backward tiles,
+ * and where 1 TMA producer, 2 MMA issuer, 3 epilogue, 4 drain of in-flight
+ * work, 5 index check, 6 group larger than the kernel allows. Returns
  * MOE_ERR_CUDA if the device itself reports an error. */
 moe_status moe_get_device_status(int32_t* code, int32_t* detail);
 

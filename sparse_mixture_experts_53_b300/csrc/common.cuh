@@ -22,7 +22,8 @@ __device__ int g_status[4];
 
 enum KernelId : int {
     K_ROUTER = 1, K_PERMUTE = 2, K_GATHER = 3, K_TILE_UP = 4, K_TILE_DOWN = 5,
-    K_STREAM_UP = 6, K_STREAM_DOWN = 7, K_REDUCE = 8, K_COMBINE = 9, K_AUX = 10, K_F32_FFN = 11
+    K_STREAM_UP = 6, K_STREAM_DOWN = 7, K_REDUCE = 8, K_COMBINE = 9, K_AUX = 10, K_F32_FFN = 11,
+    K_SELFTEST = 12, K_TILE_BWD = 13
 };
 enum Where : int {
     W_PRODUCER = 1, W_MMA = 2, W_EPILOGUE = 3, W_DRAIN = 4, W_INDEX = 5, W_COUNT = 6
@@ -354,8 +355,6 @@ __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) { return
 // gives up after timeout_ns and the kernel latches MOE_ERR_TIMEOUT, so a host
 // can check the timeout path end to end without faulting the device.
 // ---------------------------------------------------------------------------
-constexpr int K_SELFTEST = 12;
-
 __global__ void wait_selftest_kernel(uint64_t timeout_ns, int* gave_up) {
     __shared__ uint64_t bar;
     __shared__ int abort_flag;

@@ -514,7 +514,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     const bool leader = rank == 0;
     const int pair = blockIdx.x >> 1;
     const int n_pairs = gridDim.x >> 1;
-    const int kid = UP ? K_TILE_UP : K_TILE_DOWN;
+    const int kid = UP ? K_TILE_UP : (MODE == PM_DOWN ? K_TILE_DOWN : K_TILE_BWD);
     const uint64_t tmo = args.timeout_ns;
     volatile int* abort_flag = &ctl->abort_flag;
 
