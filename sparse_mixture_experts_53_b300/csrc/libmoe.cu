@@ -300,7 +300,7 @@ moe_status run_router(const moe_shape& s, const void* x, const void* wg, int32_t
     const int use_smem = wbytes <= 200 * 1024 ? 1 : 0;
     const int V = (int)(16 / es);
     const int vec = (s.d % V == 0 && aligned16(x) && aligned16(wg)) ? 1 : 0;
-    const int64_t blocks = (s.T + kRouterWarps - 1) / kRouterWarps;
+    const int64_t blocks = (s.T + kRouterWarps * kRouterTokensPerWarp - 1) / (kRouterWarps * kRouterTokensPerWarp);
     // as many CTAs as fit at once (W_g staged in shared memory limits them)
     // (126 registers x 256 threads: two CTAs per SM)
     const int per_sm = use_smem ? (int)std::max<size_t>(1, std::min<size_t>(2, (200 * 1024) / std::max<size_t>(1, wbytes))) : 2;

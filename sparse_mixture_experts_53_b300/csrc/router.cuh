@@ -2,11 +2,12 @@
 // kept scores ("Mixtral of Experts" lecture, router walkthrough;
 // tokentrails.org "Mixtral", step "The router").
 //
-// One warp per token. W_g (E x d, 64 KB in bf16 at d = 4096) is staged once
-// per CTA in shared memory; each lane accumulates a fixed, strided share of
-// the d products for all E experts in fp32, then a butterfly of warp shuffles
-// leaves the E totals in every lane. The reduction order is fixed, so the
-// result does not depend on the grid.
+// Large batches: W_g (E x d, 64 KB in bf16 at d = 4096) is staged once per CTA
+// in shared memory and a warp scores four tokens at a time; each lane
+// accumulates a fixed, strided share of the d products of each token for all
+// E experts in fp32, then a butterfly of warp shuffles leaves the E totals in
+// every lane. Small batches split one token over a CTA. The reduction order
+// of a token's scores is fixed, so the result does not depend on the grid.
 #pragma once
 
 #include "common.cuh"
@@ -48,7 +49,8 @@ __device__ __forceinline__ void load_vec(const T* p, float (&v)[Vec16<T>::N]) {
     unpack_vec<T>(*reinterpret_cast<const uint4*>(p), v);
 }
 
-constexpr int kRouterGroup = 8;  // 16-byte chunks of a token row each lane loads before computing
+constexpr int kRouterGroup = 8;  // 16-byte chunks each thread loads before storing them (W_g staging)
+constexpr int kRouterTokensPerWarp = 4;  // tokens a warp scores together (large batches)
 
 // Top-2 selection and the two-way softmax from the E scores of one token.
 __device__ __forceinline__ void top2_softmax(const float (&acc)[kMaxExperts], int E, int32_t* idx, float* w) {
@@ -75,7 +77,7 @@ __device__ __forceinline__ void top2_softmax(const float (&acc)[kMaxExperts], in
 // dynamic shared memory); otherwise it is read through L1/L2.
 // vec: rows are 16-byte aligned and d is a multiple of the vector width.
 template <typename T>
-__global__ void __launch_bounds__(kRouterWarps * 32)
+__global__ void __launch_bounds__(kRouterWarps * 32, 2)
     router_top2_kernel(const T* __restrict__ x, const T* __restrict__ wg, int64_t T_tokens, int d,
                        int E, int use_smem, int vec, int32_t* __restrict__ topk_idx,
                        float* __restrict__ topk_w, float* __restrict__ logits) {
@@ -114,47 +116,82 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
     const int warp = threadIdx.x >> 5;
     constexpr int V = Vec16<T>::N;
 
-    for (int64_t t = (int64_t)blockIdx.x * kRouterWarps + warp; t < T_tokens;
-         t += (int64_t)gridDim.x * kRouterWarps) {
-        const T* xr = x + t * d;
-        float acc[kMaxExperts];
+    if (vec) {
+        // A warp scores kRouterTokensPerWarp consecutive tokens together, so
+        // each W_g chunk read from shared memory (and widened to fp32) serves
+        // all of them. Per token the sums are the single-token ones: lane
+        // chunks c = lane, lane + 32, ... in increasing order, then a butterfly.
+        constexpr int TPW = kRouterTokensPerWarp;
+        const int nchunks = d / V;
+        for (int64_t t0 = ((int64_t)blockIdx.x * kRouterWarps + warp) * TPW; t0 < T_tokens;
+             t0 += (int64_t)gridDim.x * kRouterWarps * TPW) {
+            float acc[TPW][kMaxExperts];
 #pragma unroll
-        for (int e = 0; e < kMaxExperts; ++e) acc[e] = 0.f;
-
-        int j0 = 0;
-        if (vec) {
-            // The lane's chunks are c = lane, lane + 32, ...; a group of them is
-            // loaded before any is used, so the row's loads overlap instead of
-            // waiting one by one. Chunks are still summed in increasing order.
-            const int nchunks = d / V;
-            for (int c0 = lane; c0 < nchunks; c0 += 32 * kRouterGroup) {
-                uint4 xg[kRouterGroup];
+            for (int k = 0; k < TPW; ++k)
 #pragma unroll
-                for (int u = 0; u < kRouterGroup; ++u) {
-                    const int c = c0 + 32 * u;
-                    if (c < nchunks) xg[u] = *reinterpret_cast<const uint4*>(xr + c * V);
-                }
+                for (int e = 0; e < kMaxExperts; ++e) acc[k][e] = 0.f;
+            for (int c0 = lane; c0 < nchunks; c0 += 64) {
+                uint4 xg[2][TPW];
 #pragma unroll
-                for (int u = 0; u < kRouterGroup; ++u) {
+                for (int u = 0; u < 2; ++u)
+#pragma unroll
+                    for (int k = 0; k < TPW; ++k) {
+                        const int c = c0 + 32 * u;
+                        xg[u][k] = (c < nchunks && t0 + k < T_tokens)
+                                       ? *reinterpret_cast<const uint4*>(x + (t0 + k) * d + c * V)
+                                       : make_uint4(0, 0, 0, 0);
+                    }
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
                     const int c = c0 + 32 * u;
                     if (c < nchunks) {
-                        float xv[V];
-                        unpack_vec<T>(xg[u], xv);
+                        float xv[TPW][V];
+#pragma unroll
+                        for (int k = 0; k < TPW; ++k) unpack_vec<T>(xg[u][k], xv[k]);
 #pragma unroll
                         for (int e = 0; e < kMaxExperts; ++e) {
                             if (e < E) {
                                 float wv[V];
                                 load_vec<T>(w + (int64_t)e * d + c * V, wv);
 #pragma unroll
-                                for (int i = 0; i < V; ++i) acc[e] = fmaf(xv[i], wv[i], acc[e]);
+                                for (int k = 0; k < TPW; ++k)
+#pragma unroll
+                                    for (int i = 0; i < V; ++i) acc[k][e] = fmaf(xv[k][i], wv[i], acc[k][e]);
                             }
                         }
                     }
                 }
             }
-            j0 = nchunks * V;
+#pragma unroll
+            for (int k = 0; k < TPW; ++k) {
+#pragma unroll
+                for (int e = 0; e < kMaxExperts; ++e) {
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) acc[k][e] += __shfl_xor_sync(0xffffffffu, acc[k][e], o);
+                }
+                const int64_t t = t0 + k;
+                if (t >= T_tokens) break;
+                if (logits != nullptr && lane < E) {
+                    float v = acc[k][0];
+#pragma unroll
+                    for (int e = 1; e < kMaxExperts; ++e)
+                        if (lane == e) v = acc[k][e];
+                    logits[t * E + lane] = v;
+                }
+                if (lane == 0) top2_softmax(acc[k], E, topk_idx + 2 * t, topk_w + 2 * t);
+            }
         }
-        for (int j = j0 + lane; j < d; j += 32) {
+        return;
+    }
+
+    // scalar path (rows not 16-byte aligned or d not a multiple of the vector width)
+    for (int64_t t = (int64_t)blockIdx.x * kRouterWarps + warp; t < T_tokens;
+         t += (int64_t)gridDim.x * kRouterWarps) {
+        const T* xr = x + t * d;
+        float acc[kMaxExperts];
+#pragma unroll
+        for (int e = 0; e < kMaxExperts; ++e) acc[e] = 0.f;
+        for (int j = lane; j < d; j += 32) {
             const float xv = to_f32<T>(xr[j]);
 #pragma unroll
             for (int e = 0; e < kMaxExperts; ++e)
