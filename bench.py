@@ -374,7 +374,8 @@ def run_ours(args, rank, world, local) -> dict | None:
         "config": {"workload": cfg["name"], "T": cfg["T"], "d": cfg["d"], "ffn": cfg["ffn"], "E": cfg["E"], "k": 2,
                    "aux_stats": aux, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "ffn_path": "weight-streaming (swap-AB)" if streaming else
-                   ("token tiles 256x256 on CTA pairs" if args.tile_ctas == 2 or (args.tile_ctas == 0 and cfg["T"] > 384)
+                   ("token tiles 256x256, two CTA pairs per cluster sharing the token tile" if args.tile_ctas == 4
+                    else "token tiles 256x256 on CTA pairs" if args.tile_ctas == 2 or (args.tile_ctas == 0 and cfg["T"] > 384)
                     else "token tiles 128x256"),
                    "pdl": bool(args.pdl),
                    "l2": "inputs larger than L2: each step reads %.2f GB of expert weights" % (work["weight_bytes"] / 1e9),
@@ -591,8 +592,8 @@ def main():
                     help="emulate N expert-parallel ranks on one GPU and time each rank's experts")
     ap.add_argument("--train", action="store_true",
                     help="time a training step (forward that keeps its state + backward) instead of the forward")
-    ap.add_argument("--tile-ctas", type=int, default=0, choices=[0, 1, 2],
-                    help="token tiles: automatic (0), single CTAs (1) or CTA pairs (2)")
+    ap.add_argument("--tile-ctas", type=int, default=0, choices=[0, 1, 2, 4],
+                    help="token tiles: automatic (0), single CTAs (1), CTA pairs (2), two pairs per cluster (4)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -289,8 +289,9 @@ moe_status moe_set_wait_timeout_ns(uint64_t ns);
  *   MOE_KNOB_TILE_CTAS  0 (default) = automatic: 128-token tiles on single
  *                       CTAs up to 384 tokens, 256-token tiles on CTA pairs
  *                       (one tcgen05 MMA spans two SMs) above; 1 = single
- *                       CTAs; 2 = CTA pairs. The single-CTA kernel also runs
- *                       when no CTA pair fits on the GPU.
+ *                       CTAs; 2 = CTA pairs; 4 = two CTA pairs per cluster
+ *                       sharing each token tile (loaded once, multicast). The
+ *                       single-CTA kernel also runs when no CTA pair fits.
  * Returns MOE_ERR_INVALID_ARG for an unknown knob or value. */
 enum { MOE_KNOB_FFN_PATH = 1, MOE_KNOB_KSLICE = 2, MOE_KNOB_GRID = 3, MOE_KNOB_PDL = 4, MOE_KNOB_TILE_CTAS = 5 };
 moe_status moe_set_knob(int32_t knob, int64_t value);

@@ -52,11 +52,11 @@ struct HostState {
     bool timing = false;
     bool pdl = true;           // programmatic dependent launch between the library's kernels
     int tile_ctas = 0;         // token tiles: 0 auto, 1 single CTAs, 2 CTA pairs
-    int pair_cap[kMaxDevices][5] = {{0}};  // resident CTA pairs per kernel (0 = not queried)
+    int pair_cap[kMaxDevices][8] = {{0}};  // resident clusters per pair kernel (0 = not queried)
     std::vector<TimingRecord> records;
     std::vector<cudaEvent_t> pool;
     int sms[kMaxDevices] = {0};
-    bool attr_set[kMaxDevices][12] = {{false}};
+    bool attr_set[kMaxDevices][16] = {{false}};
 };
 HostState g;
 
@@ -119,6 +119,27 @@ cudaError_t klaunch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = g.pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// As klaunch, for a kernel that runs in thread-block clusters of `cluster` CTAs.
+template <typename... KArgs, typename... Args>
+cudaError_t klaunch_cluster(void (*kernel)(KArgs...), int cluster, dim3 grid, dim3 block, size_t smem,
+                            cudaStream_t st, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = g.pdl ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
@@ -390,18 +411,25 @@ int tc_grid(int64_t work_upper) {
     return (int)std::max<int64_t>(1, std::min<int64_t>(work_upper, sms));
 }
 
-// CTA pairs of a cluster-of-2 kernel that fit on the GPU at once (queried once
-// per device); -1 if none fits.
+// Clusters of `cluster` CTAs (CTA pairs: 2) of a kernel that fit on the GPU
+// at once (queried once per device and slot); -1 if none fits.
 template <typename K>
-int pair_capacity(K kernel, size_t smem, int slot) {
+int pair_capacity(K kernel, size_t smem, int slot, int cluster = 2) {
     const int dev = current_device();
     if (dev < 0 || dev >= kMaxDevices) return -1;
     int& cap = g.pair_cap[dev][slot];
     if (cap == 0) {
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(2 * (sm_count() / 2));
+        cfg.gridDim = dim3(cluster * (sm_count() / cluster));
         cfg.blockDim = dim3(kPairThreads);
         cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)cluster;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
         int n = 0;
         if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n <= 0) {
             cudaGetLastError();
@@ -417,6 +445,46 @@ int pair_grid(int64_t pairs_upper, int cap) {
     int pairs = g.grid > 0 ? std::max(1, g.grid / 2) : cap;
     pairs = (int)std::max<int64_t>(1, std::min<int64_t>(pairs_upper, pairs));
     return 2 * pairs;
+}
+
+// Both expert GEMMs on CTA-pair token tiles, NP pairs per cluster.
+// MOE_ERR_UNSUPPORTED (nothing enqueued) when the kernels do not fit.
+template <int NP>
+moe_status run_pair_ffn(const moe_shape& s, const void* x_perm, const int32_t* offsets, const float* perm_w,
+                        const void* w1, const void* w3, const void* w2, float* y_slot, __nv_bfloat16* H,
+                        __nv_bfloat16* u_out, __nv_bfloat16* v_out, cudaStream_t st) {
+    const int64_t R = 2 * s.T;
+    const int d = s.d, F = s.ffn, E = s.E;
+    constexpr int CL = 2 * NP;
+    auto kup = tile_pair_gemm_kernel<PM_UP, NP>;
+    auto kdown = tile_pair_gemm_kernel<PM_DOWN, NP>;
+    const int slot = NP == 1 ? 6 : 12;
+    const int cap_slot = NP == 1 ? 0 : 5;  // the backward kernels use slots 2-4
+    const int cap_up = ensure_smem(kup, slot, kPairSmemBytes) ? pair_capacity(kup, kPairSmemBytes, cap_slot, CL) : -1;
+    const int cap_down =
+        ensure_smem(kdown, slot + 1, kPairSmemBytes) ? pair_capacity(kdown, kPairSmemBytes, cap_slot + 1, CL) : -1;
+    if (cap_up <= 0 || cap_down <= 0) {
+        cudaGetLastError();
+        return MOE_ERR_UNSUPPORTED;
+    }
+    CUtensorMap ma, mb0, mb1;
+    if (!make_map(&ma, x_perm, d, R, 128) || !make_map(&mb0, w1, d, (uint64_t)E * F, 128) ||
+        !make_map(&mb1, w3, d, (uint64_t)E * F, 128))
+        return MOE_ERR_CUDA;
+    TileArgs up{offsets, perm_w, H, E, d, F / kTileM, F, F, g.timeout_ns, u_out, v_out};
+    const int64_t units_up = ((R + kPairM - 1) / kPairM + E) * (F / kTileM / NP);
+    MOE_TRY(launch("tile_up_swiglu", st, [&] {
+        return klaunch_cluster(kup, CL, CL * (pair_grid(units_up, cap_up) / 2), kPairThreads, kPairSmemBytes, st, ma,
+                               mb0, mb1, up);
+    }));
+    CUtensorMap mh, mw2;
+    if (!make_map(&mh, H, F, R, 128) || !make_map(&mw2, w2, F, (uint64_t)E * d, 128)) return MOE_ERR_CUDA;
+    TileArgs down{offsets, perm_w, y_slot, E, F, d / kTileN, d, d, g.timeout_ns};
+    const int64_t units_down = ((R + kPairM - 1) / kPairM + E) * (d / kTileN / NP);
+    return launch("tile_down_scale", st, [&] {
+        return klaunch_cluster(kdown, CL, CL * (pair_grid(units_down, cap_down) / 2), kPairThreads, kPairSmemBytes, st,
+                               mh, mw2, mw2, down);
+    });
 }
 
 // With slot_row and y given (the whole-layer call), the weight-streaming path
@@ -444,32 +512,15 @@ moe_status run_ffn(const moe_shape& s, const void* x_perm, const int32_t* offset
     }
     __nv_bfloat16* H = reinterpret_cast<__nv_bfloat16*>(ws + L.h);
     const int tile_ctas = g.tile_ctas != 0 ? g.tile_ctas : (s.T <= kSingleCtaMaxTokens ? 1 : 2);
-    if (L.path == 1 && tile_ctas == 2) {
-        // CTA pairs: each CTA stages 128 token rows and 128 weight rows per stage
-        const int cap_up = ensure_smem(tile_pair_gemm_kernel<PM_UP>, 6, kPairSmemBytes)
-                               ? pair_capacity(tile_pair_gemm_kernel<PM_UP>, kPairSmemBytes, 0) : -1;
-        const int cap_down = ensure_smem(tile_pair_gemm_kernel<PM_DOWN>, 7, kPairSmemBytes)
-                                 ? pair_capacity(tile_pair_gemm_kernel<PM_DOWN>, kPairSmemBytes, 1) : -1;
-        if (cap_up > 0 && cap_down > 0) {
-            CUtensorMap ma, mb0, mb1;
-            if (!make_map(&ma, x_perm, d, R, 128) || !make_map(&mb0, w1, d, (uint64_t)E * F, 128) ||
-                !make_map(&mb1, w3, d, (uint64_t)E * F, 128))
-                return MOE_ERR_CUDA;
-            TileArgs up{offsets, perm_w, H, E, d, F / kTileM, F, F, g.timeout_ns, u_out, v_out};
-            const int64_t pairs_up = ((R + kPairM - 1) / kPairM + E) * (F / kTileM);
-            MOE_TRY(launch("tile_up_swiglu", st, [&] {
-                return klaunch(tile_pair_gemm_kernel<PM_UP>, pair_grid(pairs_up, cap_up), kPairThreads, kPairSmemBytes,
-                               st, ma, mb0, mb1, up);
-            }));
-            CUtensorMap mh, mw2;
-            if (!make_map(&mh, H, F, R, 128) || !make_map(&mw2, w2, F, (uint64_t)E * d, 128)) return MOE_ERR_CUDA;
-            TileArgs down{offsets, perm_w, y_slot, E, F, d / kTileN, d, d, g.timeout_ns};
-            const int64_t pairs_down = ((R + kPairM - 1) / kPairM + E) * (d / kTileN);
-            return launch("tile_down_scale", st, [&] {
-                return klaunch(tile_pair_gemm_kernel<PM_DOWN>, pair_grid(pairs_down, cap_down), kPairThreads,
-                               kPairSmemBytes, st, mh, mw2, mw2, down);
-            });
-        }
+    if (L.path == 1 && tile_ctas >= 2) {
+        // CTA pairs: each CTA stages 128 token rows and 128 weight rows per stage;
+        // tile_ctas == 4: two pairs per cluster share each token tile
+        const bool quad = tile_ctas == 4 && (F / kTileM) % 2 == 0 && (d / kTileN) % 2 == 0;
+        moe_status rc = MOE_ERR_UNSUPPORTED;
+        if (quad) rc = run_pair_ffn<2>(s, x_perm, offsets, perm_w, w1, w3, w2, y_slot, H, u_out, v_out, st);
+        if (rc == MOE_ERR_UNSUPPORTED)
+            rc = run_pair_ffn<1>(s, x_perm, offsets, perm_w, w1, w3, w2, y_slot, H, u_out, v_out, st);
+        if (rc != MOE_ERR_UNSUPPORTED) return rc;
     }
     if (L.path == 1) {
         CUtensorMap ma, mb0, mb1;
@@ -638,12 +689,12 @@ moe_status launch_pair(const char* name, int slot, int cap_slot, const CUtensorM
                        const CUtensorMap& mb1, const TileArgs& a, int64_t pairs_upper, cudaStream_t st) {
     // the weight-gradient epilogue stages its stores in 4 warps' arrays after the control block
     const size_t smem = kPairSmemBytes + (MODE == PM_WGRAD ? kWgradStageBytes : 0);
-    if (!ensure_smem(tile_pair_gemm_kernel<MODE>, slot, smem)) return MOE_ERR_CUDA;
-    const int cap = pair_capacity(tile_pair_gemm_kernel<MODE>, smem, cap_slot);
+    auto kern = tile_pair_gemm_kernel<MODE, 1>;
+    if (!ensure_smem(kern, slot, smem)) return MOE_ERR_CUDA;
+    const int cap = pair_capacity(kern, smem, cap_slot);
     if (cap <= 0) return MOE_ERR_UNSUPPORTED;
     return launch(name, st, [&] {
-        return klaunch(tile_pair_gemm_kernel<MODE>, pair_grid(pairs_upper, cap), kPairThreads, smem, st, ma, mb0, mb1,
-                       a);
+        return klaunch_cluster(kern, 2, pair_grid(pairs_upper, cap), kPairThreads, smem, st, ma, mb0, mb1, a);
     });
 }
 
@@ -1009,7 +1060,7 @@ moe_status moe_set_wait_timeout_ns(uint64_t ns) {
 moe_status moe_set_knob(int32_t knob, int64_t value) {
     switch (knob) {
         case MOE_KNOB_FFN_PATH:
-            if (value < 0 || value > 2) return MOE_ERR_INVALID_ARG;
+            if (value < 0 || value > 4 || value == 3) return MOE_ERR_INVALID_ARG;
             g.ffn_path = (int)value;
             return MOE_OK;
         case MOE_KNOB_KSLICE:
@@ -1025,7 +1076,7 @@ moe_status moe_set_knob(int32_t knob, int64_t value) {
             g.pdl = value != 0;
             return MOE_OK;
         case MOE_KNOB_TILE_CTAS:
-            if (value < 0 || value > 2) return MOE_ERR_INVALID_ARG;
+            if (value < 0 || value > 4 || value == 3) return MOE_ERR_INVALID_ARG;
             g.tile_ctas = (int)value;
             return MOE_OK;
     }

@@ -87,13 +87,15 @@ SMALL_BF16 = [
     (300, 512, 1024),
     (1000, 256, 384),
     (130, 768, 640),
+    (700, 1024, 768),
 ]
 
 
-@pytest.mark.parametrize("ctas", [2, 1])
+@pytest.mark.parametrize("ctas", [4, 2, 1])
 @pytest.mark.parametrize("T,d,ffn", SMALL_BF16)
 def test_bf16_token_tile_path(T, d, ffn, ctas):
-    """Token tiles on CTA pairs (256-token tiles, one MMA across two SMs) and on single CTAs."""
+    """Token tiles on CTA pairs (256-token tiles, one MMA across two SMs), on two pairs per cluster sharing
+    the token tile (4; shapes with an odd column-tile count fall back to one pair), and on single CTAs."""
     moe.moe_set_knob(moe.MOE_KNOB_FFN_PATH, 1)
     moe.moe_set_knob(moe.MOE_KNOB_TILE_CTAS, ctas)
     L = _margin_layer(T, d, ffn, "bf16", seed=7 + T)
@@ -138,7 +140,7 @@ def test_both_bf16_paths_agree(T):
 def test_small_grid_many_tiles_per_cta():
     """Few CTAs: each runs many tiles, cycling all stages and both accumulators."""
     moe.moe_set_knob(moe.MOE_KNOB_GRID, 3)
-    for path, T, ctas in ((1, 700, 2), (1, 700, 1), (2, 40, 1)):
+    for path, T, ctas in ((1, 700, 4), (1, 700, 2), (1, 700, 1), (2, 40, 1)):
         moe.moe_set_knob(moe.MOE_KNOB_FFN_PATH, path)
         moe.moe_set_knob(moe.MOE_KNOB_TILE_CTAS, ctas)
         L = _margin_layer(T, 256, 512, "bf16", seed=300 + T)
@@ -323,12 +325,15 @@ def test_single_and_paired_token_tiles_agree():
     dev = upload(L)
     moe.moe_set_knob(moe.MOE_KNOB_FFN_PATH, 1)
     outs = []
-    for ctas in (1, 2):
+    for ctas in (1, 2, 4):
         moe.moe_set_knob(moe.MOE_KNOB_TILE_CTAS, ctas)
         outs.append(run_staged(L, dev))
         assert_status_ok()
-    a, b = outs[0]["y_slot"].numpy(), outs[1]["y_slot"].numpy()
-    assert np.max(np.abs(a - b)) <= 1e-3 * np.max(np.abs(a))
+    a = outs[0]["y_slot"].numpy()
+    for o in outs[1:]:
+        assert np.max(np.abs(a - o["y_slot"].numpy())) <= 1e-3 * np.max(np.abs(a))
+    # one pair or two pairs sharing the token tile: the same MMAs, the same bits
+    assert torch.equal(outs[1]["y_slot"], outs[2]["y_slot"])
 
 
 def _permute_outputs(s, idx, w, x, ws):
