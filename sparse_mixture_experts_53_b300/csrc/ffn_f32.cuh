@@ -140,20 +140,35 @@ __global__ void __launch_bounds__(kAuxThreads)
     float acc[kMaxExperts];
 #pragma unroll
     for (int e = 0; e < kMaxExperts; ++e) acc[e] = 0.f;
-    for (int64_t t = threadIdx.x; t < T_tokens; t += kAuxThreads) {
-        const float* l = logits + t * E;
-        float m = l[0];
-        for (int e = 1; e < E; ++e) m = fmaxf(m, l[e]);
-        float p[kMaxExperts];
-        float s = 0.f;
+    // a thread's tokens t = tid, tid + 1024, ... in order; the score rows of
+    // four of them are loaded before any is used
+    constexpr int G = 4;
+    for (int64_t t0 = threadIdx.x; t0 < T_tokens; t0 += (int64_t)G * kAuxThreads) {
+        float lv[G][kMaxExperts];
 #pragma unroll
-        for (int e = 0; e < kMaxExperts; ++e) {
-            p[e] = e < E ? expf(l[e] - m) : 0.f;
-            s += p[e];
+        for (int g = 0; g < G; ++g) {
+            const int64_t t = t0 + (int64_t)g * kAuxThreads;
+#pragma unroll
+            for (int e = 0; e < kMaxExperts; ++e) lv[g][e] = (t < T_tokens && e < E) ? logits[t * E + e] : 0.f;
         }
-        const float inv = 1.0f / s;
 #pragma unroll
-        for (int e = 0; e < kMaxExperts; ++e) acc[e] += p[e] * inv;
+        for (int g = 0; g < G; ++g) {
+            if (t0 + (int64_t)g * kAuxThreads >= T_tokens) break;
+            float m = lv[g][0];
+#pragma unroll
+            for (int e = 1; e < kMaxExperts; ++e)
+                if (e < E) m = fmaxf(m, lv[g][e]);
+            float p[kMaxExperts];
+            float s = 0.f;
+#pragma unroll
+            for (int e = 0; e < kMaxExperts; ++e) {
+                p[e] = e < E ? expf(lv[g][e] - m) : 0.f;
+                s += p[e];
+            }
+            const float inv = 1.0f / s;
+#pragma unroll
+            for (int e = 0; e < kMaxExperts; ++e) acc[e] += p[e] * inv;
+        }
     }
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll

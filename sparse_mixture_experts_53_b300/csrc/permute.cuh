@@ -422,10 +422,22 @@ __global__ void __launch_bounds__(kPlaceThreads)
                 const int64_t t = sub + q;
                 const int ra = rows_s[q][0], rb = rows_s[q][1];
                 const uint4* src = reinterpret_cast<const uint4*>(x + t * row_bytes);
-                for (int64_t c = lane; c < c16; c += 32) {
-                    const uint4 v = src[c];
-                    if (ra >= 0) reinterpret_cast<uint4*>(x_perm + (int64_t)ra * row_bytes)[c] = v;
-                    if (rb >= 0) reinterpret_cast<uint4*>(x_perm + (int64_t)rb * row_bytes)[c] = v;
+                uint4* da = reinterpret_cast<uint4*>(x_perm + (int64_t)(ra >= 0 ? ra : 0) * row_bytes);
+                uint4* db = reinterpret_cast<uint4*>(x_perm + (int64_t)(rb >= 0 ? rb : 0) * row_bytes);
+                // four loads in flight per lane before their stores
+                for (int64_t c0 = lane; c0 < c16; c0 += 4 * 32) {
+                    uint4 v[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        if (c0 + 32 * u < c16) v[u] = src[c0 + 32 * u];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int64_t c = c0 + 32 * u;
+                        if (c < c16) {
+                            if (ra >= 0) da[c] = v[u];
+                            if (rb >= 0) db[c] = v[u];
+                        }
+                    }
                 }
             }
         }
