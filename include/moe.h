@@ -262,6 +262,11 @@ moe_status moe_layer_backward(const moe_shape* s, const void* x, const void* w_g
  * MOE_ERR_CUDA if the device itself reports an error. */
 moe_status moe_get_device_status(int32_t* code, int32_t* detail);
 
+/* Waits for `stream`, then reads and clears the device status word like
+ * moe_get_device_status, and returns the latched device error (MOE_OK if
+ * none, MOE_ERR_CUDA if the device itself failed). */
+moe_status moe_check_device_status(void* stream);
+
 /* Self-test of the device-side timeout path (no counterpart on the pages):
  * one CTA waits on an mbarrier that nothing arrives on, with the same bounded
  * wait as the tensor-core kernels. After timeout_ns (1 ns .. 10 s) the wait

@@ -51,7 +51,7 @@ struct HostState {
     uint64_t timeout_ns = 2000000000ull;
     bool timing = false;
     bool pdl = true;           // programmatic dependent launch between the library's kernels
-    int tile_ctas = 0;         // token tiles: 0 auto, 1 single CTAs, 2 CTA pairs
+    int tile_ctas = 0;         // token tiles: 0 auto, 1 single CTAs, 2 CTA pairs, 4 two pairs per cluster
     int pair_cap[kMaxDevices][8] = {{0}};  // resident clusters per pair kernel (0 = not queried)
     std::vector<TimingRecord> records;
     std::vector<cudaEvent_t> pool;
@@ -1049,6 +1049,13 @@ moe_status moe_get_device_status(int32_t* code, int32_t* detail) {
     *code = h[0];
     if (detail != nullptr) *detail = h[1] * 100 + h[2];
     return MOE_OK;
+}
+
+moe_status moe_check_device_status(void* stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MOE_ERR_CUDA;
+    int32_t code = MOE_OK;
+    const moe_status rc = moe_get_device_status(&code, nullptr);
+    return rc != MOE_OK ? rc : static_cast<moe_status>(code);
 }
 
 moe_status moe_set_wait_timeout_ns(uint64_t ns) {

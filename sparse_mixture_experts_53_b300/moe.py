@@ -40,6 +40,7 @@ EXPORTED = (
     "moe_layer_forward", "moe_layer_forward_noalloc", "moe_get_device_status", "moe_set_wait_timeout_ns", "moe_set_knob",
     "moe_timing_enable", "moe_timing_read", "moe_train_state_bytes", "moe_backward_workspace_bytes",
     "moe_layer_forward_train", "moe_layer_backward", "moe_gather_rows", "moe_selftest_wait_timeout",
+    "moe_check_device_status",
 )
 
 
@@ -83,6 +84,7 @@ def _load() -> ctypes.CDLL:
         "moe_timing_read": ([ctypes.c_char_p, ctypes.c_size_t], I),
         "moe_gather_rows": ([P, ctypes.c_int64, P, ctypes.c_int64, ctypes.c_int64, P, P], I),
         "moe_selftest_wait_timeout": ([ctypes.c_uint64, P, P], I),
+        "moe_check_device_status": ([P], I),
         "moe_train_state_bytes": ([S], ctypes.c_size_t),
         "moe_backward_workspace_bytes": ([S], ctypes.c_size_t),
         "moe_layer_forward_train": ([S, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P], I),
@@ -236,6 +238,11 @@ def moe_layer_backward(shape, x, w_gate, w1, w3, w2, dy, aux_coef, state, dx, dw
 def moe_selftest_wait_timeout(timeout_ns: int, gave_up, stream=None):
     _check("moe_selftest_wait_timeout", lib.moe_selftest_wait_timeout(int(timeout_ns), _ptr(gave_up),
                                                                       _stream(stream)))
+
+
+def moe_check_device_status(stream=None) -> int:
+    """Waits for the stream and returns (and clears) the latched device error code."""
+    return int(lib.moe_check_device_status(_stream(stream)))
 
 
 def moe_get_device_status() -> tuple[int, int]:

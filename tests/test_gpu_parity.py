@@ -430,6 +430,9 @@ def test_device_wait_timeout_is_reported_and_the_device_stays_usable():
     assert code == moe.MOE_ERR_TIMEOUT and detail == 1202
     assert int(flag) == 1
     assert_status_ok()  # the read cleared the word
+    moe.moe_selftest_wait_timeout(5_000_000, flag)
+    assert moe.moe_check_device_status() == moe.MOE_ERR_TIMEOUT
+    assert moe.moe_check_device_status() == moe.MOE_OK
     # and the device still runs the layer
     L = _margin_layer(40, 256, 256, "bf16", seed=4)
     got = run_staged(L)
