@@ -5,6 +5,7 @@
 // the caller's stream.
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
 #include <utility>
@@ -59,6 +60,16 @@ struct HostState {
     bool attr_set[kMaxDevices][16] = {{false}};
 };
 HostState g;
+
+// NVTX range around an ABI call, so profilers show the library's calls on the
+// host timeline (the NVTX header is self-contained; it costs nothing when no
+// tool is attached).
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -840,6 +851,7 @@ size_t moe_ffn_workspace_bytes(const moe_shape* s) {
 
 moe_status moe_route_top2(const moe_shape* s, const void* x, const void* w_gate, int32_t* topk_idx, float* topk_w,
                           float* logits, void* stream) {
+    NvtxRange nvtx("moe_route_top2");
     MOE_TRY(check_shape(s));
     if (s->T > 0 && (!ok_ptr(x) || !ok_ptr(w_gate) || !ok_ptr(topk_idx) || !ok_ptr(topk_w) ||
                      (logits != nullptr && !aligned16(logits))))
@@ -855,6 +867,7 @@ size_t moe_permute_workspace_bytes(const moe_shape* s) {
 moe_status moe_permute(const moe_shape* s, const int32_t* topk_idx, const float* topk_w, const void* x,
                        int32_t* counts, int32_t* offsets, int32_t* perm_token, int32_t* slot_row, float* perm_w,
                        void* x_perm, void* ws, size_t ws_bytes, void* stream) {
+    NvtxRange nvtx("moe_permute");
     MOE_TRY(check_shape(s));
     if (!ok_ptr(counts) || !ok_ptr(offsets)) return MOE_ERR_INVALID_ARG;
     if (s->T > 0 && (!ok_ptr(topk_idx) || !ok_ptr(topk_w) || !ok_ptr(x) || !ok_ptr(perm_token) ||
@@ -868,6 +881,7 @@ moe_status moe_permute(const moe_shape* s, const int32_t* topk_idx, const float*
 moe_status moe_expert_ffn(const moe_shape* s, const void* x_perm, const int32_t* offsets, const float* perm_w,
                           const void* w1, const void* w3, const void* w2, float* y_slot, void* ws, size_t ws_bytes,
                           void* stream) {
+    NvtxRange nvtx("moe_expert_ffn");
     MOE_TRY(check_ffn_shape(s));
     if (s->T == 0) return MOE_OK;
     if (!ok_ptr(x_perm) || !ok_ptr(offsets) || !ok_ptr(perm_w) || !ok_ptr(w1) || !ok_ptr(w3) || !ok_ptr(w2) ||
@@ -881,6 +895,7 @@ moe_status moe_expert_ffn(const moe_shape* s, const void* x_perm, const int32_t*
 }
 
 moe_status moe_combine(const moe_shape* s, const float* y_slot, const int32_t* slot_row, void* y, void* stream) {
+    NvtxRange nvtx("moe_combine");
     MOE_TRY(check_shape(s));
     if (s->T > 0 && (!ok_ptr(y_slot) || !ok_ptr(slot_row) || !ok_ptr(y))) return MOE_ERR_INVALID_ARG;
     return run_combine(*s, y_slot, slot_row, y, static_cast<cudaStream_t>(stream));
@@ -888,6 +903,7 @@ moe_status moe_combine(const moe_shape* s, const float* y_slot, const int32_t* s
 
 moe_status moe_aux_stats(const moe_shape* s, const float* logits, const int32_t* counts, float* f, float* P,
                          float* l_aux, void* stream) {
+    NvtxRange nvtx("moe_aux_stats");
     MOE_TRY(check_shape(s));
     if (!ok_ptr(counts) || !ok_ptr(f) || !ok_ptr(P) || !ok_ptr(l_aux)) return MOE_ERR_INVALID_ARG;
     if (s->T > 0 && !ok_ptr(logits)) return MOE_ERR_INVALID_ARG;
@@ -897,6 +913,7 @@ moe_status moe_aux_stats(const moe_shape* s, const float* logits, const int32_t*
 moe_status moe_layer_forward(const moe_shape* s, const void* x, const void* w_gate, const void* w1, const void* w3,
                              const void* w2, void* y, float* aux_f, float* aux_P, float* aux_l_aux, void* ws,
                              size_t ws_bytes, void* stream) {
+    NvtxRange nvtx("moe_layer_forward");
     MOE_TRY(check_shape(s));
     const bool aux = aux_f != nullptr && aux_P != nullptr && aux_l_aux != nullptr;
     if ((aux_f != nullptr || aux_P != nullptr || aux_l_aux != nullptr) && !aux) return MOE_ERR_INVALID_ARG;
@@ -931,6 +948,7 @@ moe_status moe_layer_forward(const moe_shape* s, const void* x, const void* w_ga
 
 moe_status moe_layer_forward_noalloc(const moe_shape* s, const void* x, const void* w_gate, const void* w1,
                                      const void* w3, const void* w2, void* y, void* stream) {
+    NvtxRange nvtx("moe_layer_forward_noalloc");
     MOE_TRY(check_shape(s));
     if (s->T == 0) return MOE_OK;
     if (s->dtype == MOE_BF16 && choose_path(*s) == 0) return MOE_ERR_UNSUPPORTED;
@@ -943,6 +961,7 @@ moe_status moe_layer_forward_noalloc(const moe_shape* s, const void* x, const vo
 
 moe_status moe_gather_rows(const void* src, int64_t src_rows, const int32_t* index, int64_t rows, int64_t row_bytes,
                            void* dst, void* stream) {
+    NvtxRange nvtx("moe_gather_rows");
     if (rows < 0 || src_rows < 0 || row_bytes <= 0 || row_bytes % 16 != 0) return MOE_ERR_INVALID_ARG;
     if (rows == 0) return MOE_OK;
     if (!ok_ptr(src) || !ok_ptr(index) || !ok_ptr(dst)) return MOE_ERR_INVALID_ARG;
@@ -968,6 +987,7 @@ size_t moe_backward_workspace_bytes(const moe_shape* s) {
 moe_status moe_layer_forward_train(const moe_shape* s, const void* x, const void* w_gate, const void* w1,
                                    const void* w3, const void* w2, void* y, float* aux_f, float* aux_P,
                                    float* aux_l_aux, void* state, size_t state_bytes, void* stream) {
+    NvtxRange nvtx("moe_layer_forward_train");
     MOE_TRY(check_shape(s));
     if (!train_supported(*s)) return MOE_ERR_UNSUPPORTED;
     const bool aux = aux_f != nullptr && aux_P != nullptr && aux_l_aux != nullptr;
@@ -1007,6 +1027,7 @@ moe_status moe_layer_backward(const moe_shape* s, const void* x, const void* w_g
                               const void* w2, const void* dy, float aux_coef, const void* state, size_t state_bytes,
                               void* dx, float* dw_gate, float* dw1, float* dw3, float* dw2, void* ws, size_t ws_bytes,
                               void* stream) {
+    NvtxRange nvtx("moe_layer_backward");
     MOE_TRY(check_shape(s));
     if (!train_supported(*s)) return MOE_ERR_UNSUPPORTED;
     if (!ok_ptr(dw_gate) || !ok_ptr(dw1) || !ok_ptr(dw3) || !ok_ptr(dw2)) return MOE_ERR_INVALID_ARG;
