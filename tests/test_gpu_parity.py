@@ -300,6 +300,40 @@ def test_named_workload_full_size(k, mixtral_weights, mixtral_dev_weights):
         assert counts.min() == 0  # the skewed workload leaves one expert empty
 
 
+def test_largest_batch_mixtral_shape(mixtral_weights, mixtral_dev_weights):
+    """T = 65536 (four times the largest named workload, 131072 slot rows): routing and grouping bit for bit
+    on every token, y on sampled tokens, the load-balancing statistics."""
+    T, d = 65536, 4096
+    c = CONFIGS[3]
+    from moe_inputs import make_tokens
+    x, wg = make_tokens(T, d, 8, "bf16", seed=65536)
+    # redraw the rows with a near tie (fp64 gaps below 1e-3) from a seeded stream
+    g = torch.Generator().manual_seed(65536)
+    while True:
+        l = oracle.router_logits(to_f64(x), to_f64(wg))
+        srt = -np.sort(-l, axis=1)
+        bad = np.nonzero((srt[:, 0] - srt[:, 1] < 1e-3) | (srt[:, 1] - srt[:, 2] < 1e-3))[0]
+        if bad.size == 0:
+            break
+        x[torch.from_numpy(bad)] = torch.randn((bad.size, d), generator=g).to(torch.bfloat16)
+    w1, w3, w2 = mixtral_weights
+    L = make_layer(1, d, c["ffn"], 8, "bf16", seed=1, weights=mixtral_weights)
+    L.T, L.x, L.w_gate = T, x, wg
+    dev = {"x": x.cuda(), "w_gate": wg.cuda()}
+    dev["w1"], dev["w3"], dev["w2"] = mixtral_dev_weights
+    got = run_staged(L, dev)
+    assert_status_ok()
+    idx_ref, _, l_ref = check_router(L, got)
+    check_permutation(L, got, idx_ref)
+    y, (f, P, l_aux) = run_forward(L, dev, aux=True)
+    assert_status_ok()
+    assert torch.equal(y, got["y"])
+    check_y(L, y, _sample_tokens(idx_ref, T, 96, seed=65536))
+    aux = oracle.aux_stats(l_ref, idx_ref, 8)
+    np.testing.assert_allclose(f.numpy(), aux["f"], rtol=0, atol=1e-7)
+    np.testing.assert_allclose(P.numpy(), aux["P"], rtol=0, atol=2e-5)
+
+
 @pytest.mark.parametrize("T", [16, 300])
 def test_pdl_on_and_off_give_identical_results(T):
     """Programmatic dependent launch only overlaps launch set-up: results are bit-identical."""
