@@ -482,7 +482,8 @@ def run_training(args) -> dict:
 
 def run_ep(args) -> dict:
     """Expert parallelism emulated on one GPU: the workload's tokens split over N ranks, each rank's
-    expert FFNs timed, for the contiguous and the load-balanced expert placement."""
+    expert FFNs timed, for the contiguous, the load-balanced and the replicated expert placement
+    (one more expert's weights per rank, given to copies of the hot experts)."""
     import numpy as np
     import torch
 
@@ -500,15 +501,20 @@ def run_ep(args) -> dict:
     wg, w1, w3, w2 = L.w_gate.cuda(), L.w1.cuda(), L.w3.cuda(), L.w2.cuda()
     out = {}
     load = None
-    for name in ("contiguous", "balanced"):
-        owner = ep.contiguous_owners(8, N) if name == "contiguous" else ep.balanced_owners(load, N)
+    for name in ("contiguous", "balanced", "replicated"):
+        if name == "contiguous":
+            owner = ep.contiguous_owners(8, N)
+        elif name == "balanced":
+            owner = ep.balanced_owners(load, N)
+        else:  # room for one more expert's weights per rank: copies of the hot experts
+            owner = ep.replicated_placement(load, N, 8 // N + 1)
         for _ in range(max(1, args.warmup // 3)):
             ep.emulate(xs, wg, w1, w3, w2, owner)
         runs = [ep.emulate(xs, wg, w1, w3, w2, owner, time_experts=True) for _ in range(3)]
         p = runs[-1][1]
         ms = np.median(np.array([r[2] for r in runs]), axis=0)
         load = p.counts.sum(0)
-        out[name] = {"owner": p.owner.tolist(), "rows_per_rank": p.rows_per_rank.tolist(),
+        out[name] = {"placement": p.placement, "rows_per_rank": p.rows_per_rank.tolist(),
                      "expert_ms_per_rank": [round(float(v), 4) for v in ms],
                      "max_over_mean": round(float(ms.max() / ms.mean()), 3),
                      "tokens_per_s_if_ranks_in_parallel": round(T / (ms.max() * 1e-3), 1)}

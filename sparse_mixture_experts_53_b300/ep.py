@@ -19,6 +19,12 @@ experts (``owner[e]`` is the rank of expert e):
    reverse all-to-all), which put them back in their ``x_perm`` order and
    combine the two rows of every token (``moe_combine``).
 
+When a rank has room for more than E/N experts' weights, ``replicated_placement``
+gives the hot experts copies on several ranks (``owner[e]`` becomes a list of
+ranks); each source then splits its rows of a copied expert into consecutive,
+near-equal chunks, one per copy, so no single rank carries a hot expert's rows
+alone. The result does not change: a row meets the same weights on any copy.
+
 Every token gets exactly the mixture of the single-GPU layer. ``plan`` is plain
 host logic. ``ExpertParallelLayer`` runs the steps over a torch.distributed
 process group (NCCL on GPUs; the tests run it over gloo with CPU stand-ins for
@@ -65,13 +71,71 @@ def balanced_owners(load, N: int) -> np.ndarray:
     return owner
 
 
+def _place_pieces(load, copies, N: int, slots: int):
+    """Longest-processing-time placement of every expert's copies.
+
+    Each copy of expert e carries load[e] / copies[e] rows. Copies go from the
+    largest to the smallest (ties: lower expert) to the least loaded rank
+    (ties: lower rank) that has a free slot and no copy of e yet. Returns the
+    ranks of each expert's copies and the largest rank load, or None when the
+    copies do not fit.
+    """
+    E = load.size
+    pieces = sorted(((load[e] / copies[e], e) for e in range(E) for _ in range(copies[e])),
+                    key=lambda t: (-t[0], t[1]))
+    rows = np.zeros(N)
+    held = np.zeros(N, dtype=np.int64)
+    place = [[] for _ in range(E)]
+    for size, e in pieces:
+        free = [q for q in range(N) if held[q] < slots and q not in place[e]]
+        if not free:
+            return None
+        q = min(free, key=lambda r: (rows[r], r))
+        place[e].append(q)
+        rows[q] += size
+        held[q] += 1
+    return place, rows.max()
+
+
+def replicated_placement(load, N: int, slots: int) -> list:
+    """Experts' copies over N ranks when a rank can hold `slots` experts' weights.
+
+    A hot expert bounds an expert-parallel step alone once its rows exceed a
+    rank's share; copies of it on several ranks split those rows. Starting from
+    one copy per expert, the expert whose copies carry the most rows gets one
+    more copy, while slots and ranks remain; every count of copies is placed by
+    ``_place_pieces`` and the placement with the smallest largest rank load
+    wins (ties: fewer copies). A replicated expert's rows are split evenly over
+    its copies (``plan`` splits every source's block). Returns one list of
+    ranks per expert.
+    """
+    load = np.asarray(load, dtype=np.float64)
+    E = load.size
+    if E > N * slots:
+        raise ValueError("the ranks' slots cannot hold every expert once")
+    copies = np.ones(E, dtype=np.int64)
+    best = _place_pieces(load, copies, N, slots)
+    while copies.sum() < N * slots:
+        e = max(range(E), key=lambda k: (load[k] / copies[k], -k))
+        if copies[e] == N or load[e] == 0:
+            break
+        copies[e] += 1
+        got = _place_pieces(load, copies, N, slots)
+        if got is not None and got[1] < best[1]:
+            best = got
+    return best[0]
+
+
 @dataclass
 class Plan:
     """Row movements of one expert-parallel step, identical on every rank.
 
     counts[s][e]  rows of expert e on source rank s (its x_perm rows
                   offsets[s][e] .. offsets[s][e+1])
-    experts[q]    experts of rank q, ascending
+    placement[e]  ranks holding expert e; source s's rows of e are split into
+                  len(placement[e]) consecutive chunks, chunk j going to
+                  placement[e][j]
+    experts[q]    experts held by rank q, ascending
     send_index[s] s's x_perm rows in send order: destination by destination,
                   each destination's experts in ascending order
     send_splits[s][q], recv_splits[q][s]   rows per (source, destination)
@@ -81,7 +145,7 @@ class Plan:
     """
     counts: np.ndarray
     offsets: np.ndarray
-    owner: np.ndarray
+    placement: list
     experts: list
     send_index: list
     send_splits: np.ndarray
@@ -93,40 +157,65 @@ class Plan:
     def rows_per_rank(self) -> np.ndarray:
         return np.array([lo[-1] for lo in self.local_offsets], dtype=np.int64)
 
+    @property
+    def owner(self) -> np.ndarray:
+        """The first rank of each expert (its only one without replication)."""
+        return np.array([reps[0] for reps in self.placement], dtype=np.int64)
+
+
+def _as_placement(owner_or_placement, E: int) -> list:
+    first = owner_or_placement[0] if len(owner_or_placement) else 0
+    if isinstance(first, (list, tuple)):
+        return [[int(q) for q in reps] for reps in owner_or_placement]
+    return [[int(q)] for q in np.asarray(owner_or_placement, dtype=np.int64)]
+
 
 def plan(counts, owner) -> Plan:
+    """owner: the rank of each expert, or a list of replica ranks per expert."""
     counts = np.asarray(counts, dtype=np.int64)
-    owner = np.asarray(owner, dtype=np.int64)
     N, E = counts.shape
+    place = _as_placement(owner, E)
     offsets = np.zeros((N, E + 1), dtype=np.int64)
     offsets[:, 1:] = np.cumsum(counts, axis=1)
-    experts = [[e for e in range(E) if owner[e] == q] for q in range(N)]
+    experts = [[e for e in range(E) if q in place[e]] for q in range(N)]
+
+    def chunk(s, e, q):
+        """Rows of source s's expert-e block that go to rank q."""
+        reps = place[e]
+        k, j = len(reps), reps.index(q)
+        c = counts[s, e]
+        lo = offsets[s, e] + (c * j) // k
+        hi = offsets[s, e] + (c * (j + 1)) // k
+        return lo, hi
+
     send_index, send_splits = [], np.zeros((N, N), dtype=np.int64)
     for s in range(N):
         idx = []
         for q in range(N):
             for e in experts[q]:
-                idx.extend(range(offsets[s, e], offsets[s, e + 1]))
-            send_splits[s, q] = sum(counts[s, e] for e in experts[q])
+                lo, hi = chunk(s, e, q)
+                idx.extend(range(lo, hi))
+                send_splits[s, q] += hi - lo
         send_index.append(np.array(idx, dtype=np.int64))
     recv_splits = send_splits.T.copy()
     regroup, local_offsets = [], []
     for q in range(N):
         # receive buffer of q: source after source, each source's rows in q's expert order
-        start = {}
-        at = 0
+        start, at = {}, 0
         for s in range(N):
             for e in experts[q]:
-                start[(s, e)] = at
-                at += counts[s, e]
-        idx, lo = [], [0]
+                lo, hi = chunk(s, e, q)
+                start[(s, e)] = (at, hi - lo)
+                at += hi - lo
+        idx, lo_off = [], [0]
         for e in experts[q]:
             for s in range(N):
-                idx.extend(range(start[(s, e)], start[(s, e)] + counts[s, e]))
-            lo.append(len(idx))
+                a, n = start[(s, e)]
+                idx.extend(range(a, a + n))
+            lo_off.append(len(idx))
         regroup.append(np.array(idx, dtype=np.int64))
-        local_offsets.append(np.array(lo, dtype=np.int64))
-    return Plan(counts, offsets, owner, experts, send_index, send_splits, recv_splits, regroup, local_offsets)
+        local_offsets.append(np.array(lo_off, dtype=np.int64))
+    return Plan(counts, offsets, place, experts, send_index, send_splits, recv_splits, regroup, local_offsets)
 
 
 def _gate_rows(perm_w):
@@ -217,9 +306,10 @@ class CudaOps:
 class ExpertParallelLayer:
     """One rank of an expert-parallel layer over a torch.distributed process group.
 
-    w_gate is replicated; w1, w3, w2 hold only this rank's experts (those with
-    owner[e] == rank, ascending). ``ops`` runs the per-rank steps (default: the
-    CUDA kernels); a test may pass CPU stand-ins.
+    w_gate is replicated; w1, w3, w2 hold only the experts this rank holds
+    (``owner[e] == rank``, or ``rank in owner[e]`` for a replica placement),
+    ascending. ``ops`` runs the per-rank steps (default: the CUDA kernels); a
+    test may pass CPU stand-ins.
     """
 
     def __init__(self, w_gate, w1_local, w3_local, w2_local, owner, group=None, ops=None):
@@ -228,10 +318,10 @@ class ExpertParallelLayer:
         self.group = group
         self.rank = dist.get_rank(group)
         self.world = dist.get_world_size(group)
-        self.owner = np.asarray(owner, dtype=np.int64)
-        self.E = self.owner.size
-        if sorted(set(self.owner.tolist())) != list(range(self.world)):
-            raise ValueError("every rank must own experts")
+        self.E = len(owner)
+        self.placement = _as_placement(owner, self.E)
+        if sorted({q for reps in self.placement for q in reps}) != list(range(self.world)):
+            raise ValueError("every rank must hold experts")
         self.w_gate, self.w1, self.w3, self.w2 = w_gate, w1_local, w3_local, w2_local
         self.ops = ops if ops is not None else CudaOps()
         self.last_plan = None
@@ -243,7 +333,7 @@ class ExpertParallelLayer:
         counts = g["counts"].to(torch.int64)
         every = [torch.zeros_like(counts) for _ in range(self.world)]
         dist.all_gather(every, counts, group=self.group)
-        p = plan(torch.stack(every).cpu().numpy(), self.owner)
+        p = plan(torch.stack(every).cpu().numpy(), self.placement)
         self.last_plan = p
         me = self.rank
         # dispatch rows and their gate weights
@@ -276,8 +366,9 @@ def emulate(xs, w_gate, w1, w3, w2, owner, time_experts: bool = False):
     """
     import torch
     ops = CudaOps()
-    owner = np.asarray(owner, dtype=np.int64)
-    N, E = int(owner.max()) + 1, owner.size
+    E = len(owner)
+    owner = _as_placement(owner, E)
+    N = 1 + max(q for reps in owner for q in reps)
     groups = [ops.route_and_group(x, w_gate, E) for x in xs]
     p = plan(np.stack([g["counts"].cpu().numpy() for g in groups]), owner)
     base = np.cumsum([0] + [g["x_perm"].shape[0] for g in groups])

@@ -71,6 +71,61 @@ def test_balanced_placement():
     assert np.bincount(ep.contiguous_owners(8, 4), weights=load, minlength=4).max() == 980
 
 
+@pytest.mark.parametrize("N,slots", [(2, 5), (4, 3), (8, 2), (8, 4)])
+def test_plan_with_replicas_splits_each_block_over_its_copies(N, slots):
+    rng = np.random.default_rng(100 + N)
+    counts = _counts(rng, N, 8, 53, skew=True)
+    place = ep.replicated_placement(counts.sum(0), N, slots)
+    assert all(len(set(r)) == len(r) for r in place)
+    assert max(sum(q in r for r in place) for q in range(N)) <= slots
+    # on two ranks the single-copy placement already splits the two hot experts
+    assert any(len(r) > 1 for r in place) == (N > 2)
+    p = ep.plan(counts, place)
+    assert np.array_equal(p.recv_splits, p.send_splits.T)
+    labels = []
+    for s in range(N):
+        lab = [(s, e, i) for e in range(8) for i in range(counts[s, e])]
+        assert sorted(p.send_index[s]) == list(range(len(lab)))
+        sent = [lab[j] for j in p.send_index[s]]
+        cuts = np.cumsum([0] + p.send_splits[s].tolist())
+        labels.append([sent[cuts[q]:cuts[q + 1]] for q in range(N)])
+    got = {}
+    for q in range(N):
+        recv = [r for s in range(N) for r in labels[s][q]]
+        local = [recv[j] for j in p.regroup[q]]
+        for j, e in enumerate(p.experts[q]):
+            grp = local[p.local_offsets[q][j]:p.local_offsets[q][j + 1]]
+            assert all(lab[1] == e for lab in grp) and grp == sorted(grp)
+            for lab in grp:
+                assert lab not in got
+                got[lab] = q
+    assert len(got) == int(counts.sum())
+    # source s's rows of e: consecutive chunks, in the order of e's copies, sizes within one
+    for s in range(N):
+        for e in range(8):
+            dest = [got[(s, e, i)] for i in range(counts[s, e])]
+            k = len(place[e])
+            want = [place[e][j] for j in range(k) for _ in range((counts[s, e] * (j + 1)) // k - (counts[s, e] * j) // k)]
+            assert dest == want
+
+
+def test_replicated_placement_spreads_a_hot_expert():
+    # one expert takes 40% of the rows: on 8 ranks it alone bounds the step
+    load = np.array([3200, 700, 700, 700, 700, 700, 700, 600])
+    own = ep.balanced_owners(load, 8)
+    assert np.bincount(own, weights=load, minlength=8).max() == 3200
+    place = ep.replicated_placement(load, 8, 2)
+    per = np.zeros(8)
+    for e, r in enumerate(place):
+        for q in r:
+            per[q] += load[e] / len(r)
+    assert per.max() <= 0.5 * 3200 and per.sum() == load.sum()
+    assert len(place[0]) >= 4
+    # a flat load gains nothing from copies, so none are made
+    flat = ep.replicated_placement(np.full(8, 100), 4, 4)
+    assert all(len(r) == 1 for r in flat)
+
+
 class CpuOps:
     """fp64 stand-ins of the per-rank kernels, from the oracle (test infrastructure)."""
 
@@ -111,7 +166,7 @@ def _layer(seed, T, d=16, ffn=8, E=8, skew=False):
     return x, wg, w1, w3, w2
 
 
-def _rank(rank, world, port, balanced, out):
+def _rank(rank, world, port, mode, out):
     import torch.distributed as dist
     os.environ["MASTER_ADDR"] = "127.0.0.1"
     os.environ["MASTER_PORT"] = str(port)
@@ -123,24 +178,33 @@ def _rank(rank, world, port, balanced, out):
         l = oracle.router_logits(x_all, wg)
         idx, _, _ = oracle.top_k_gates(l, 2)
         load = np.bincount(idx.ravel(), minlength=8)
-        owner = ep.balanced_owners(load, world) if balanced else ep.contiguous_owners(8, world)
-        mine = [e for e in range(8) if owner[e] == rank]
+        if mode == "replicated":
+            # copies of two hot experts (a load heavier than this small batch's)
+            owner = ep.replicated_placement(np.array([900, 700, 50, 50, 50, 50, 50, 50]), world, 8 // world + 1)
+            assert any(len(r) > 1 for r in owner)
+            mine = [e for e in range(8) if rank in owner[e]]
+        else:
+            owner = ep.balanced_owners(load, world) if mode == "balanced" else ep.contiguous_owners(8, world)
+            mine = [e for e in range(8) if owner[e] == rank]
         layer = ep.ExpertParallelLayer(torch.from_numpy(wg), torch.from_numpy(w1[mine]), torch.from_numpy(w3[mine]),
                                        torch.from_numpy(w2[mine]), owner, ops=CpuOps())
         y = layer.forward(torch.from_numpy(x)).numpy()
         ref = oracle.layer_forward(x, wg, w1, w3, w2)["y"]
         out.put((rank, float(np.max(np.abs(y - ref))), layer.last_plan.rows_per_rank.tolist()))
+    except Exception as e:  # report instead of leaving the parent waiting
+        out.put((rank, float("inf"), repr(e)))
+        raise
     finally:
         dist.destroy_process_group()
 
 
 @pytest.mark.timeout(180)
-@pytest.mark.parametrize("world,balanced", [(2, False), (4, False), (4, True)])
-def test_distributed_forward_equals_the_single_process_layer(world, balanced):
+@pytest.mark.parametrize("world,mode", [(2, "contiguous"), (4, "contiguous"), (4, "balanced"), (4, "replicated")])
+def test_distributed_forward_equals_the_single_process_layer(world, mode):
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
     port = _free_port()
-    procs = [ctx.Process(target=_rank, args=(r, world, port, balanced, q)) for r in range(world)]
+    procs = [ctx.Process(target=_rank, args=(r, world, port, mode, q)) for r in range(world)]
     for p in procs:
         p.start()
     res = sorted(q.get(timeout=150) for _ in range(world))

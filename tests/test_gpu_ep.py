@@ -69,15 +69,22 @@ def test_expert_ffn_with_a_share_of_the_experts(E, T):
     assert np.max(np.abs(ys.cpu().numpy()[:n] - ref[:n])) <= TOL["bf16"] * np.max(np.abs(ref[:n]))
 
 
-@pytest.mark.parametrize("N,T,balanced", [(2, 300, False), (4, 300, True), (8, 200, False), (4, 16, False)])
-def test_emulated_ranks_equal_the_single_gpu_layer(N, T, balanced):
+@pytest.mark.parametrize("N,T,mode", [(2, 300, "contiguous"), (4, 300, "balanced"), (8, 200, "contiguous"),
+                                      (4, 16, "contiguous"), (4, 300, "replicated"), (8, 200, "replicated")])
+def test_emulated_ranks_equal_the_single_gpu_layer(N, T, mode):
     d, ffn = 512, 1024
     L = make_layer(N * T, d, ffn, 8, "bf16", seed=77 + N, weight_seed=88)
     xs = [_margin_tokens(T, d, 1000 * N + s, L.w_gate).cuda() for s in range(N)]
     dev = {k: getattr(L, k).cuda() for k in ("w_gate", "w1", "w3", "w2")}
     load = sum(np.bincount(oracle.top_k_gates(oracle.router_logits(to_f64(x.cpu()), to_f64(L.w_gate)), 2)[0].ravel(),
                            minlength=8) for x in xs)
-    owner = ep.balanced_owners(load, N) if balanced else ep.contiguous_owners(8, N)
+    if mode == "replicated":
+        # two hot experts' copies (a heavier load than these tokens'), so rows of one expert
+        # from one source go to several ranks
+        owner = ep.replicated_placement(np.array([900, 700, 50, 50, 50, 50, 50, 50]), N, 8 // N + 1)
+        assert any(len(r) > 1 for r in owner)
+    else:
+        owner = ep.balanced_owners(load, N) if mode == "balanced" else ep.contiguous_owners(8, N)
     ys, plan, _ = ep.emulate(xs, dev["w_gate"], dev["w1"], dev["w3"], dev["w2"], owner)
     torch.cuda.synchronize()
     assert_status_ok()
@@ -106,3 +113,10 @@ def test_skewed_routing_is_rebalanced_by_placement():
     assert_status_ok()
     assert load[:2].sum() > 0.4 * load.sum()  # the two steered experts are hot
     assert p_b.rows_per_rank.max() < p_c.rows_per_rank.max()
+    # one more slot per rank: copies of the hot experts split their rows
+    ys_r, p_r, _ = ep.emulate(xs, dev["w_gate"], dev["w1"], dev["w3"], dev["w2"],
+                              ep.replicated_placement(load, N, 8 // N + 1))
+    assert_status_ok()
+    assert p_r.rows_per_rank.max() < p_b.rows_per_rank.max()
+    for y_b, y_r in zip(ys, ys_r):
+        assert torch.allclose(y_b.float(), y_r.float(), rtol=0, atol=1e-2 * float(y_b.float().abs().max()))
