@@ -23,3 +23,10 @@ from .moe_backward import (  # noqa: F401
     aux_score_grad,
     layer_backward,
 )
+from .decoder_block import (  # noqa: F401
+    rms_norm,
+    rope,
+    causal_gqa_attention,
+    attention_sublayer,
+    decoder_block,
+)
