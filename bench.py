@@ -480,6 +480,91 @@ def run_training(args) -> dict:
     }
 
 
+def run_block(args) -> dict:
+    """The decoder block around the layer (RMSNorm, Q/K/V projection, RoPE, causal GQA attention, Wo,
+    residual + RMSNorm, the MoE layer, residual) at the Mixtral shape, one 4096-token sequence."""
+    import torch
+
+    from moe_inputs import BLOCK_CONFIGS, make_block_config
+    from sparse_mixture_experts_53_b300 import moe
+
+    torch.cuda.set_device(0)
+    moe.moe_set_knob(moe.MOE_KNOB_PDL, args.pdl)
+    c = BLOCK_CONFIGS["mixtral"]
+    p = {k: v.cuda() for k, v in make_block_config("mixtral").items()}
+    B, S, d, Hq, Hkv, F = c["B"], c["S"], c["d"], c["n_heads"], c["n_kv_heads"], c["ffn"]
+    hd = 128
+    shape = moe.make_block_shape(B, S, d, Hq, Hkv, F)
+    ws = torch.empty(moe.moe_block_workspace_bytes(shape), dtype=torch.uint8, device="cuda")
+    wts = moe.block_weights(p)
+    out = torch.empty_like(p["x"])
+    stream = torch.cuda.current_stream()
+    T = B * S
+
+    def step():
+        moe.moe_block_forward(shape, p["x"], wts, out, ws, stream)
+
+    for _ in range(args.warmup):
+        step()
+    code, detail = moe.moe_get_device_status()
+    if code != moe.MOE_OK:
+        raise RuntimeError(f"device status after warm-up: {moe.status_string(code)} ({detail})")
+    sampler = ClockSampler(0)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with sampler:
+        a.record(stream)
+        for _ in range(args.steps):
+            step()
+        b.record(stream)
+        torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / args.steps
+    moe.moe_timing_enable(True)
+    for _ in range(args.steps):
+        step()
+    torch.cuda.synchronize()
+    kern = moe.moe_timing_read()
+    moe.moe_timing_enable(False)
+    code, detail = moe.moe_get_device_status()
+    if code != moe.MOE_OK:
+        raise RuntimeError(f"device status after timing: {moe.status_string(code)} ({detail})")
+    per = {n: v[1] / v[0] for n, v in kern.items()}
+    peaks = _peaks()
+    flops = {
+        "linear_qkv": 2.0 * T * d * (Hq + 2 * Hkv) * hd,
+        "attention": 4.0 * hd * Hq * B * S * (S + 1) / 2,   # causal: each query against the keys up to it
+        "linear_o": 2.0 * T * Hq * hd * d,
+        "moe": 6.0 * 2 * T * d * F,
+    }
+    total = sum(flops.values())
+
+    def tf(name):
+        return round(flops[name] / (per[name] * 1e-3) / 1e12, 1) if name in per else None
+
+    dom = max(per, key=per.get)
+    up = "tile_up_swiglu"
+    up_tf = 4.0 * 2 * T * d * F / (per[up] * 1e-3) / 1e12
+    return {
+        "metric": "Mixtral decoder-block tokens/s (attention + MoE layer, bf16)", "value": round(T / (ms * 1e-3), 1),
+        "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "dtype": "bf16", "data": "synthetic (seeded Mixtral-shape block, random init)",
+        "config": {"workload": c["name"], "B": B, "S": S, "d": d, "n_heads": Hq, "n_kv_heads": Hkv,
+                   "head_dim": hd, "ffn": F, "E": 8, "k": 2},
+        "step": {"tflops": round(total / (ms * 1e-3) / 1e12, 1),
+                 "frac_bf16": round(total / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4)},
+        "roofline": {"kernel": up, "bound": "tensor", "achieved": round(up_tf, 1), "peak": peaks["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": round(up_tf / peaks["bf16_tflops"], 4),
+                     "peak_source": peaks["source"] + " (burst)", "launch_ms": round(per[up], 5)},
+        "attention": {"ms": round(per.get("attention", 0.0), 5), "tflops": tf("attention"),
+                      "frac_bf16": round(tf("attention") / peaks["bf16_tflops"], 4) if "attention" in per else None},
+        "projections_tflops": {"linear_qkv": tf("linear_qkv"), "linear_o": tf("linear_o")},
+        "longest_kernel": dom,
+        "kernels_ms_per_step": {n: round(v[1] / max(1, args.steps), 5) for n, v in kern.items()},
+        "gpu_launches": int(sum(v[0] for v in kern.values())),
+        "clocks": sampler.summary(),
+    }
+
+
 def run_ep(args) -> dict:
     """Expert parallelism emulated on one GPU: the workload's tokens split over N ranks, each rank's
     expert FFNs timed, for the contiguous, the load-balanced and the replicated expert placement
@@ -598,6 +683,8 @@ def main():
                     help="emulate N expert-parallel ranks on one GPU and time each rank's experts")
     ap.add_argument("--train", action="store_true",
                     help="time a training step (forward that keeps its state + backward) instead of the forward")
+    ap.add_argument("--block", action="store_true",
+                    help="time the decoder block around the layer (attention + MoE) at the Mixtral shape")
     ap.add_argument("--tile-ctas", type=int, default=0, choices=[0, 1, 2, 4],
                     help="token tiles: automatic (0), single CTAs (1), CTA pairs (2), two pairs per cluster (4)")
     args = ap.parse_args()
@@ -606,6 +693,11 @@ def main():
     rank, world, local = _dist_env()
     if args.ep:
         print(json.dumps(run_ep(args)), flush=True)
+        return
+    if args.block:
+        if args.impl != "ours" or world != 1:
+            raise SystemExit("--block times this library's decoder block on one GPU")
+        print(json.dumps(run_block(args)), flush=True)
         return
     if args.train:
         if args.impl != "ours" or world != 1:

@@ -252,12 +252,91 @@ moe_status moe_layer_backward(const moe_shape* s, const void* x, const void* w_g
                               float* dw_gate, float* dw1, float* dw3, float* dw2,
                               void* ws, size_t ws_bytes, void* stream);
 
+/* ----------------------------------------------------------------------------
+ * Decoder block around the layer. Mixtral keeps the Mistral/LLaMA block and
+ * replaces its MLP by the MoE layer ("Mixtral" lineage page, step "GPT-2 vs
+ * Mixtral" and its Code):
+ *   h   = x + Wo . attention(RoPE(Wq xn), RoPE(Wk xn), Wv xn),  xn = RMSNorm(x)
+ *   out = h + MoE(RMSNorm(h))
+ * with 32 query heads and 8 KV heads of width 128 at d = 4096 (royalroad.pages.dev
+ * notes, Architecture; fdeinterviews.com breakdown, layer diagram: 41.9M
+ * attention parameters per layer). Readings where the pages are silent:
+ * RMSNorm(x) = g * x / sqrt(mean(x^2) + eps); RoPE turns channel pairs
+ * (2i, 2i+1) of every query and key head by pos * rope_base^(-2i/head_dim),
+ * pos = index inside the sequence; scores q.k / sqrt(head_dim), causal, no
+ * sliding window, no biases; query head h reads KV head h / (n_heads /
+ * n_kv_heads). A batch is B sequences of S tokens, token-major [B*S][d].
+ * Everything here is bf16 storage with fp32 accumulation; the residual stream
+ * h is rounded to bf16.
+ * ------------------------------------------------------------------------- */
+typedef struct {
+    int64_t B;           /* sequences, >= 1 */
+    int64_t S;           /* tokens per sequence, >= 1 */
+    int32_t d;           /* model width, multiple of 256 */
+    int32_t n_heads;     /* query heads */
+    int32_t n_kv_heads;  /* key/value heads, divides n_heads */
+    int32_t head_dim;    /* must be 128 */
+    int32_t ffn;         /* the MoE layer's expert width (multiple of 256) */
+    int32_t E;           /* experts: 8 */
+    int32_t k;           /* experts per token: 2 */
+    float eps;           /* RMSNorm epsilon */
+    float rope_base;     /* RoPE base */
+} moe_block_shape;
+
+typedef struct {
+    const void* attn_norm;  /* [d] bf16 gain of the first RMSNorm */
+    const void* wqkv;       /* [(n_heads + 2 n_kv_heads) head_dim][d] bf16: Wq rows, then Wk, then Wv */
+    const void* wo;         /* [d][n_heads head_dim] bf16 */
+    const void* ffn_norm;   /* [d] bf16 gain of the second RMSNorm */
+    const void* w_gate;     /* [E][d] bf16, the MoE layer's weights as for moe_layer_forward */
+    const void* w1;         /* [E][ffn][d] */
+    const void* w3;         /* [E][ffn][d] */
+    const void* w2;         /* [E][d][ffn] */
+} moe_block_weights;
+
+/* Workspace of moe_block_forward (0 for an unsupported shape). */
+size_t moe_block_workspace_bytes(const moe_block_shape* s);
+
+/* out [B*S][d] bf16 = the decoder block applied to x [B*S][d] bf16 (device
+ * pointers, 16-byte aligned; out may not alias x). Enqueues RMSNorm, the fused
+ * Q/K/V projection, RoPE, attention, the Wo projection, the residual add fused
+ * with the second RMSNorm, moe_layer_forward and the last residual add. */
+moe_status moe_block_forward(const moe_block_shape* s, const void* x, const moe_block_weights* w, void* out,
+                             void* ws, size_t ws_bytes, void* stream);
+
+/* The block's steps, one call each (the same kernels moe_block_forward runs). */
+
+/* y [rows][d] = RMSNorm(h) * g in bf16. With `add` (fp32 [rows][d], nullable)
+ * h = bf16(x + add) is formed first and written to h_out [rows][d]; without it
+ * h = x and h_out is unused. d % 8 == 0. */
+moe_status moe_rmsnorm(int64_t rows, int32_t d, const void* x, const float* add, const void* g, float eps,
+                       void* h_out, void* y, void* stream);
+
+/* y [rows][n_out] fp32 = x [rows][n_in] . w^T, w [n_out][n_in] bf16 (a linear
+ * layer; tcgen05 CTA-pair tiles of 256 rows x 256 columns). n_in % 64 == 0,
+ * n_out % 256 == 0. */
+moe_status moe_linear(int64_t rows, int32_t n_in, int32_t n_out, const void* x, const void* w, float* y,
+                      void* stream);
+
+/* Splits the fused projection qkv [B*S][(n_heads + 2 n_kv_heads) head_dim]
+ * fp32 into q [B*S][n_heads head_dim], k and v [B*S][n_kv_heads head_dim]
+ * (bf16), turning the channel pairs of q and k by RoPE. */
+moe_status moe_rope_split(const moe_block_shape* s, const float* qkv, void* q, void* k, void* v, void* stream);
+
+/* Causal grouped-query attention of each sequence: o [B*S][n_heads head_dim]
+ * bf16 from q, k, v as moe_rope_split writes them. head_dim must be 128. */
+moe_status moe_attention(const moe_block_shape* s, const void* q, const void* k, const void* v, void* o,
+                         void* stream);
+
+/* out [n] = bf16(a + b), bf16, n % 8 == 0. */
+moe_status moe_residual_add(int64_t n, const void* a, const void* b, void* out, void* stream);
+
 /* Synchronises the current device, then reports and clears its status word.
  * *code receives MOE_OK or the first device-side error since the last read;
  * *detail (nullable) receives 100 * kernel + where for diagnostics, with
  * kernel 1 router, 2 grouping, 3 row gather, 4 up tiles, 5 down tiles,
  * 6 streaming up, 7 streaming down, 12 the wait self-test, 13 backward tiles,
- * and where 1 TMA producer, 2 MMA issuer, 3 epilogue, 4 drain of in-flight
+ * 16 attention, and where 1 TMA producer, 2 MMA issuer, 3 epilogue, 4 drain of in-flight
  * work, 5 index check, 6 group larger than the kernel allows. Returns
  * MOE_ERR_CUDA if the device itself reports an error. */
 moe_status moe_get_device_status(int32_t* code, int32_t* detail);

@@ -41,6 +41,10 @@ STREAM_W3 = 4
 STREAM_W2 = 5
 STREAM_U = 6
 STREAM_REDRAW = 7
+STREAM_ATTN_NORM = 8
+STREAM_WQKV = 9
+STREAM_WO = 10
+STREAM_FFN_NORM = 11
 
 SCHEDULE_PATH = Path(__file__).resolve().parent.parent / "tests" / "golden" / "input_schedule.json"
 
@@ -180,6 +184,45 @@ def make_layer(T: int, d: int, ffn: int, E: int = 8, dtype: str = "bf16", seed: 
     meta = dict(name=name, seed=seed, weight_seed=weight_seed, skew_c=skew_c,
                 redraws=[list(r) for r in (redraws or [])])
     return Layer(T, d, ffn, E, dtype, x, wg, w1, w3, w2, meta)
+
+
+# Decoder-block workloads (the MoE layer inside its Mixtral block): B sequences
+# of S tokens. The Mixtral-shape block reuses the layer workloads' expert draw.
+BLOCK_CONFIGS = {
+    "small": dict(name="block_small_B2_S160", B=2, S=160, d=512, n_heads=4, n_kv_heads=2, ffn=512,
+                  seed=5320, weight_seed=5321),
+    "mixtral": dict(name="mixtral_block_prefill_B1_S4096", B=1, S=4096, d=4096, n_heads=32, n_kv_heads=8,
+                    ffn=14336, seed=5322, weight_seed=5310),
+}
+
+
+def make_block(B: int, S: int, d: int, n_heads: int, n_kv_heads: int, ffn: int, E: int = 8, head_dim: int = 128,
+               seed: int = 1, weight_seed: int | None = None, moe_weights=None) -> dict:
+    """Inputs of one decoder block as bf16 CPU tensors.
+
+    x [B*S][d] ~ N(0, 1) (the residual stream entering the block); RMSNorm
+    gains ~ N(1, 0.1^2); wqkv [(n_heads + 2 n_kv_heads) head_dim][d] ~ N(0, 1/d);
+    wo [d][n_heads head_dim] ~ N(0, 1/(n_heads head_dim)); the MoE layer's
+    w_gate, w1, w3, w2 as ``make_layer`` draws them.
+    """
+    ws = seed if weight_seed is None else weight_seed
+    T = B * S
+    rows = (n_heads + 2 * n_kv_heads) * head_dim
+    x = _store(normal_f32(seed, STREAM_X, T * d, 1.0), "bf16").view(T, d)
+    w_gate = _store(normal_f32(seed, STREAM_WG, E * d, 1.0 / np.sqrt(d)), "bf16").view(E, d)
+    g_attn = _store(1.0 + normal_f32(seed, STREAM_ATTN_NORM, d, 0.1), "bf16")
+    g_ffn = _store(1.0 + normal_f32(seed, STREAM_FFN_NORM, d, 0.1), "bf16")
+    wqkv = _store(normal_f32(ws, STREAM_WQKV, rows * d, 1.0 / np.sqrt(d)), "bf16").view(rows, d)
+    wo = _store(normal_f32(ws, STREAM_WO, d * n_heads * head_dim, 1.0 / np.sqrt(n_heads * head_dim)),
+                "bf16").view(d, n_heads * head_dim)
+    w1, w3, w2 = moe_weights if moe_weights is not None else make_weights(d, ffn, E, "bf16", ws)
+    return dict(x=x, attn_norm=g_attn, wqkv=wqkv, wo=wo, ffn_norm=g_ffn, w_gate=w_gate, w1=w1, w3=w3, w2=w2)
+
+
+def make_block_config(name: str, moe_weights=None) -> dict:
+    c = BLOCK_CONFIGS[name]
+    return make_block(c["B"], c["S"], c["d"], c["n_heads"], c["n_kv_heads"], c["ffn"], seed=c["seed"],
+                      weight_seed=c["weight_seed"], moe_weights=moe_weights)
 
 
 def load_schedule(path: Path | None = None) -> dict:

@@ -23,7 +23,7 @@ __device__ int g_status[4];
 enum KernelId : int {
     K_ROUTER = 1, K_PERMUTE = 2, K_GATHER = 3, K_TILE_UP = 4, K_TILE_DOWN = 5,
     K_STREAM_UP = 6, K_STREAM_DOWN = 7, K_REDUCE = 8, K_COMBINE = 9, K_AUX = 10, K_F32_FFN = 11,
-    K_SELFTEST = 12, K_TILE_BWD = 13
+    K_SELFTEST = 12, K_TILE_BWD = 13, K_NORM = 14, K_ROPE = 15, K_ATTN = 16, K_ADD = 17
 };
 enum Where : int {
     W_PRODUCER = 1, W_MMA = 2, W_EPILOGUE = 3, W_DRAIN = 4, W_INDEX = 5, W_COUNT = 6
@@ -231,6 +231,26 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
 
 __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Stores 16 consecutive columns of the warp's 32 lanes (the inverse of tmem_ld16).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Makes this thread's ordinary shared-memory stores visible to the tensor
+// core's (async proxy) reads of the same bytes.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // ---------------------------------------------------------------------------

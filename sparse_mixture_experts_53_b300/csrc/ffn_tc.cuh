@@ -110,6 +110,8 @@ struct TileArgs {
     int m_tiles;           // 256-row tiles of the gradient per expert
     int split_rows;        // rows of the first gradient matrix
     int64_t out_estride;   // elements per expert in each gradient matrix
+    // plain linear layer (pair kernel, PM_DOWN with offsets == nullptr): one group of this many rows
+    int dense_rows;
 };
 
 // Epilogue of one token tile for one thread (one row): reads the row's 256
@@ -217,7 +219,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     pdl_wait();
     if (threadIdx.x == 0) {
         int tiles = 0;
-        for (int e = 0; e <= args.E; ++e) ctl->off[e] = args.offsets[e];
+        if (args.offsets != nullptr) {
+            for (int e = 0; e <= args.E; ++e) ctl->off[e] = args.offsets[e];
+        } else {
+            ctl->off[0] = 0;
+            ctl->off[1] = args.dense_rows;
+        }
         for (int e = 0; e < args.E; ++e) {
             const int c = ctl->off[e + 1] - ctl->off[e];
             ctl->cnt[e] = c;
@@ -555,7 +562,12 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     pdl_wait();
     if (threadIdx.x == 0) {
         int tiles = 0;
-        for (int e = 0; e <= args.E; ++e) ctl->off[e] = args.offsets[e];
+        if (args.offsets != nullptr) {
+            for (int e = 0; e <= args.E; ++e) ctl->off[e] = args.offsets[e];
+        } else {
+            ctl->off[0] = 0;
+            ctl->off[1] = args.dense_rows;
+        }
         for (int e = 0; e < args.E; ++e) {
             const int c = ctl->off[e + 1] - ctl->off[e];
             ctl->cnt[e] = c;

@@ -22,6 +22,8 @@
 #include "bwd.cuh"
 #include "permute.cuh"
 #include "router.cuh"
+#include "block.cuh"
+#include "attention.cuh"
 
 namespace moe {
 namespace {
@@ -839,6 +841,149 @@ void* noalloc_scratch() {
     return addr[dev];
 }
 
+// ------------------------------------------------------------ decoder block
+moe_status check_block_shape(const moe_block_shape* s) {
+    if (s == nullptr) return MOE_ERR_INVALID_ARG;
+    if (s->B < 1 || s->S < 1 || s->d <= 0 || s->n_heads <= 0 || s->n_kv_heads <= 0 || s->head_dim <= 0 ||
+        s->ffn <= 0 || !(s->eps >= 0.f) || !std::isfinite(s->eps) || !(s->rope_base > 0.f) ||
+        !std::isfinite(s->rope_base))
+        return MOE_ERR_INVALID_ARG;
+    if (s->n_heads % s->n_kv_heads != 0) return MOE_ERR_INVALID_ARG;
+    if (s->head_dim != kAttnHD || s->d % 256 != 0 || s->ffn % 256 != 0 || s->E != 8 || s->k != 2)
+        return MOE_ERR_UNSUPPORTED;
+    // the fused projection runs on 256-column tiles
+    if ((int64_t)(s->n_heads + 2 * s->n_kv_heads) * s->head_dim % 256 != 0) return MOE_ERR_UNSUPPORTED;
+    if (s->B > (int64_t)INT32_MAX / s->S) return MOE_ERR_UNSUPPORTED;  // TMA row coordinates are int32
+    return MOE_OK;
+}
+
+moe_shape block_layer_shape(const moe_block_shape& s) {
+    moe_shape m;
+    m.T = s.B * s.S;
+    m.d = s.d;
+    m.ffn = s.ffn;
+    m.E = s.E;
+    m.k = s.k;
+    m.dtype = MOE_BF16;
+    return m;
+}
+
+struct BlockLayout {
+    size_t xn, qkv, q, k, v, attn, h, y, moe, total;
+};
+
+// xn (later the second norm's output), qkv (later Wo's fp32 output), q, k, v,
+// attention output, residual stream h, MoE output y, the MoE layer's workspace
+BlockLayout block_layout(const moe_block_shape& s) {
+    const size_t T = (size_t)(s.B * s.S), d = (size_t)s.d;
+    const size_t wq = (size_t)s.n_heads * s.head_dim, wkv = (size_t)s.n_kv_heads * s.head_dim;
+    BlockLayout L{};
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off = align_up(off + bytes, kAlign);
+        return at;
+    };
+    L.xn = take(T * d * 2);
+    L.qkv = take(T * std::max(wq + 2 * wkv, d) * 4);
+    L.q = take(T * wq * 2);
+    L.k = take(T * wkv * 2);
+    L.v = take(T * wkv * 2);
+    L.attn = take(T * wq * 2);
+    L.h = take(T * d * 2);
+    L.y = take(T * d * 2);
+    const moe_shape m = block_layer_shape(s);
+    L.moe = take(std::max<size_t>(moe_workspace_bytes(&m), 16));
+    L.total = off;
+    return L;
+}
+
+moe_status run_rmsnorm(int64_t rows, int d, const void* x, const float* add, const void* gain, float eps, void* h_out,
+                       void* y, cudaStream_t st) {
+    if (rows == 0) return MOE_OK;
+    const int64_t blocks_needed = (rows + kNormThreads / 32 - 1) / (kNormThreads / 32);
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(blocks_needed, (int64_t)sm_count() * 8));
+    const auto* xb = static_cast<const __nv_bfloat16*>(x);
+    const auto* gb = static_cast<const __nv_bfloat16*>(gain);
+    auto* hb = static_cast<__nv_bfloat16*>(h_out);
+    auto* yb = static_cast<__nv_bfloat16*>(y);
+    if (add != nullptr)
+        return launch("rmsnorm_add", st, [&] {
+            return klaunch(rmsnorm_kernel<true>, grid, kNormThreads, 0, st, xb, add, gb, eps, rows, d, hb, yb);
+        });
+    return launch("rmsnorm", st, [&] {
+        return klaunch(rmsnorm_kernel<false>, grid, kNormThreads, 0, st, xb, add, gb, eps, rows, d, hb, yb);
+    });
+}
+
+moe_status run_linear(int64_t rows, int n_in, int n_out, const void* x, const void* w, float* y, cudaStream_t st,
+                      const char* name = "linear") {
+    if (rows == 0) return MOE_OK;
+    CUtensorMap ma, mb;
+    if (!make_map(&ma, x, (uint64_t)n_in, (uint64_t)rows, 128) || !make_map(&mb, w, (uint64_t)n_in, (uint64_t)n_out, 128))
+        return MOE_ERR_CUDA;
+    TileArgs a{nullptr, nullptr, y, 1, n_in, n_out / kTileN, n_out, n_out, g.timeout_ns};
+    a.dense_rows = (int)rows;
+    const int64_t units = (rows + kPairM - 1) / kPairM * (n_out / kTileN);
+    // the same kernel (and attribute slots) as the expert FFN's down projection
+    return launch_pair<PM_DOWN>(name, 7, 1, ma, mb, mb, a, units, st);
+}
+
+moe_status run_rope(const moe_block_shape& s, const float* qkv, void* q, void* k, void* v, cudaStream_t st) {
+    const int64_t T = s.B * s.S;
+    if (T == 0) return MOE_OK;
+    RopeArgs a{};
+    a.qkv = qkv;
+    a.q = static_cast<__nv_bfloat16*>(q);
+    a.k = static_cast<__nv_bfloat16*>(k);
+    a.v = static_cast<__nv_bfloat16*>(v);
+    a.T = T;
+    a.S = s.S;
+    a.Hq = s.n_heads;
+    a.Hkv = s.n_kv_heads;
+    a.hd = s.head_dim;
+    for (int i = 0; i < s.head_dim / 2; ++i)
+        a.theta[i] = std::pow((double)s.rope_base, -2.0 * (double)i / (double)s.head_dim);
+    const dim3 block(s.head_dim / 2, kRopeTokens);
+    const int64_t grid = (T + kRopeTokens - 1) / kRopeTokens;
+    return launch("rope_split", st, [&] { return klaunch(rope_split_kernel, dim3((unsigned)grid), block, 0, st, a); });
+}
+
+moe_status run_attention(const moe_block_shape& s, const void* q, const void* k, const void* v, void* o,
+                         cudaStream_t st) {
+    const int64_t T = s.B * s.S;
+    CUtensorMap mq, mk, mv;
+    if (!make_map(&mq, q, (uint64_t)s.n_heads * kAttnHD, (uint64_t)T, 128) ||
+        !make_map(&mk, k, (uint64_t)s.n_kv_heads * kAttnHD, (uint64_t)T, 128) ||
+        !make_map(&mv, v, (uint64_t)s.n_kv_heads * kAttnHD, (uint64_t)T, 128))
+        return MOE_ERR_CUDA;
+    if (!ensure_smem(attention_kernel, 11, kAttnSmemBytes)) return MOE_ERR_CUDA;
+    AttnArgs a{};
+    a.o = static_cast<__nv_bfloat16*>(o);
+    a.S = s.S;
+    a.B = (int)s.B;
+    a.Hq = s.n_heads;
+    a.Hkv = s.n_kv_heads;
+    a.n_qt = (int)((s.S + kAttnTile - 1) / kAttnTile);
+    a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)s.head_dim));
+    a.timeout_ns = g.timeout_ns;
+    const int64_t grid = (int64_t)a.n_qt * s.B * s.n_heads;
+    if (grid > INT32_MAX) return MOE_ERR_UNSUPPORTED;
+    return launch("attention", st, [&] {
+        return klaunch(attention_kernel, dim3((unsigned)grid), dim3(kAttnThreads), kAttnSmemBytes, st, mq, mk, mv, a);
+    });
+}
+
+moe_status run_residual_add(int64_t n, const void* a, const void* b, void* out, cudaStream_t st) {
+    if (n == 0) return MOE_OK;
+    const int64_t chunks = n / 8;
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((chunks + 255) / 256, (int64_t)sm_count() * 8));
+    return launch("residual_add", st, [&] {
+        return klaunch(residual_add_kernel, grid, 256, 0, st, static_cast<const __nv_bfloat16*>(a),
+                       static_cast<const __nv_bfloat16*>(b), n, static_cast<__nv_bfloat16*>(out));
+    });
+}
+
 }  // namespace
 }  // namespace moe
 
@@ -981,6 +1126,92 @@ moe_status moe_layer_forward_noalloc(const moe_shape* s, const void* x, const vo
     if (scratch == nullptr) return MOE_ERR_CUDA;
     return moe_layer_forward(s, x, w_gate, w1, w3, w2, y, nullptr, nullptr, nullptr, scratch, kNoAllocScratchBytes,
                              stream);
+}
+
+size_t moe_block_workspace_bytes(const moe_block_shape* s) {
+    if (check_block_shape(s) != MOE_OK) return 0;
+    return block_layout(*s).total;
+}
+
+moe_status moe_block_forward(const moe_block_shape* s, const void* x, const moe_block_weights* w, void* out,
+                             void* ws, size_t ws_bytes, void* stream) {
+    NvtxRange nvtx("moe_block_forward");
+    MOE_TRY(check_block_shape(s));
+    if (w == nullptr || !ok_ptr(x) || !ok_ptr(out) || !ok_ptr(ws) || !ok_ptr(w->attn_norm) || !ok_ptr(w->wqkv) ||
+        !ok_ptr(w->wo) || !ok_ptr(w->ffn_norm) || !ok_ptr(w->w_gate) || !ok_ptr(w->w1) || !ok_ptr(w->w3) ||
+        !ok_ptr(w->w2) || x == out)
+        return MOE_ERR_INVALID_ARG;
+    const BlockLayout L = block_layout(*s);
+    if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    unsigned char* b = static_cast<unsigned char*>(ws);
+    const int64_t T = s->B * s->S;
+    const int d = s->d;
+    const int wq = s->n_heads * s->head_dim, wkv = s->n_kv_heads * s->head_dim;
+    void* xn = b + L.xn;
+    float* qkv = reinterpret_cast<float*>(b + L.qkv);
+    void* q = b + L.q;
+    void* k = b + L.k;
+    void* v = b + L.v;
+    void* attn = b + L.attn;
+    void* h = b + L.h;
+    void* y = b + L.y;
+    // h = x + Wo attention(RoPE(Wq xn), RoPE(Wk xn), Wv xn), xn = RMSNorm(x)
+    MOE_TRY(run_rmsnorm(T, d, x, nullptr, w->attn_norm, s->eps, nullptr, xn, st));
+    MOE_TRY(run_linear(T, d, wq + 2 * wkv, xn, w->wqkv, qkv, st, "linear_qkv"));
+    MOE_TRY(run_rope(*s, qkv, q, k, v, st));
+    MOE_TRY(run_attention(*s, q, k, v, attn, st));
+    float* o = qkv;  // the projection output is consumed: Wo's output takes its place
+    MOE_TRY(run_linear(T, wq, d, attn, w->wo, o, st, "linear_o"));
+    // out = h + MoE(RMSNorm(h)); the second norm's output takes xn's place
+    MOE_TRY(run_rmsnorm(T, d, x, o, w->ffn_norm, s->eps, h, xn, st));
+    const moe_shape m = block_layer_shape(*s);
+    MOE_TRY(moe_layer_forward(&m, xn, w->w_gate, w->w1, w->w3, w->w2, y, nullptr, nullptr, nullptr, b + L.moe,
+                              L.total - L.moe, stream));
+    return run_residual_add(T * d, h, y, out, st);
+}
+
+moe_status moe_rmsnorm(int64_t rows, int32_t d, const void* x, const float* add, const void* g, float eps,
+                       void* h_out, void* y, void* stream) {
+    NvtxRange nvtx("moe_rmsnorm");
+    if (rows < 0 || d <= 0 || d % 8 != 0 || !(eps >= 0.f) || !std::isfinite(eps)) return MOE_ERR_INVALID_ARG;
+    if (rows == 0) return MOE_OK;
+    if (!ok_ptr(x) || !ok_ptr(g) || !ok_ptr(y) || (add != nullptr && (!ok_ptr(add) || !ok_ptr(h_out))))
+        return MOE_ERR_INVALID_ARG;
+    return run_rmsnorm(rows, d, x, add, g, eps, add != nullptr ? h_out : nullptr, y, static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_linear(int64_t rows, int32_t n_in, int32_t n_out, const void* x, const void* w, float* y,
+                      void* stream) {
+    NvtxRange nvtx("moe_linear");
+    if (rows < 0 || n_in <= 0 || n_out <= 0) return MOE_ERR_INVALID_ARG;
+    if (n_in % kBK != 0 || n_out % kTileN != 0 || rows > INT32_MAX) return MOE_ERR_UNSUPPORTED;
+    if (rows == 0) return MOE_OK;
+    if (!ok_ptr(x) || !ok_ptr(w) || !ok_ptr(y)) return MOE_ERR_INVALID_ARG;
+    return run_linear(rows, n_in, n_out, x, w, y, static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_rope_split(const moe_block_shape* s, const float* qkv, void* q, void* k, void* v, void* stream) {
+    NvtxRange nvtx("moe_rope_split");
+    MOE_TRY(check_block_shape(s));
+    if (!ok_ptr(qkv) || !ok_ptr(q) || !ok_ptr(k) || !ok_ptr(v)) return MOE_ERR_INVALID_ARG;
+    return run_rope(*s, qkv, q, k, v, static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_attention(const moe_block_shape* s, const void* q, const void* k, const void* v, void* o,
+                         void* stream) {
+    NvtxRange nvtx("moe_attention");
+    MOE_TRY(check_block_shape(s));
+    if (!ok_ptr(q) || !ok_ptr(k) || !ok_ptr(v) || !ok_ptr(o)) return MOE_ERR_INVALID_ARG;
+    return run_attention(*s, q, k, v, o, static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_residual_add(int64_t n, const void* a, const void* b, void* out, void* stream) {
+    NvtxRange nvtx("moe_residual_add");
+    if (n < 0 || n % 8 != 0) return MOE_ERR_INVALID_ARG;
+    if (n == 0) return MOE_OK;
+    if (!ok_ptr(a) || !ok_ptr(b) || !ok_ptr(out)) return MOE_ERR_INVALID_ARG;
+    return run_residual_add(n, a, b, out, static_cast<cudaStream_t>(stream));
 }
 
 moe_status moe_gather_rows(const void* src, int64_t src_rows, const int32_t* index, int64_t rows, int64_t row_bytes,

@@ -40,13 +40,25 @@ EXPORTED = (
     "moe_layer_forward", "moe_layer_forward_noalloc", "moe_get_device_status", "moe_set_wait_timeout_ns", "moe_set_knob",
     "moe_timing_enable", "moe_timing_read", "moe_train_state_bytes", "moe_backward_workspace_bytes",
     "moe_layer_forward_train", "moe_layer_backward", "moe_gather_rows", "moe_selftest_wait_timeout",
-    "moe_check_device_status",
+    "moe_check_device_status", "moe_block_workspace_bytes", "moe_block_forward", "moe_rmsnorm", "moe_linear",
+    "moe_rope_split", "moe_attention", "moe_residual_add",
 )
 
 
 class moe_shape(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int64), ("d", ctypes.c_int32), ("ffn", ctypes.c_int32),
                 ("E", ctypes.c_int32), ("k", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+
+
+class moe_block_shape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int64), ("S", ctypes.c_int64), ("d", ctypes.c_int32), ("n_heads", ctypes.c_int32),
+                ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("ffn", ctypes.c_int32),
+                ("E", ctypes.c_int32), ("k", ctypes.c_int32), ("eps", ctypes.c_float),
+                ("rope_base", ctypes.c_float)]
+
+
+class moe_block_weights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("attn_norm", "wqkv", "wo", "ffn_norm", "w_gate", "w1", "w3", "w2")]
 
 
 class MoEError(RuntimeError):
@@ -63,6 +75,7 @@ def _load() -> ctypes.CDLL:
     lib = ctypes.CDLL(str(_LIB_PATH))
     P = ctypes.c_void_p
     S = ctypes.POINTER(moe_shape)
+    BS = ctypes.POINTER(moe_block_shape)
     I = ctypes.c_int
     sig = {
         "moe_version": ([], ctypes.c_char_p),
@@ -90,6 +103,13 @@ def _load() -> ctypes.CDLL:
         "moe_layer_forward_train": ([S, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P], I),
         "moe_layer_backward": ([S, P, P, P, P, P, P, ctypes.c_float, P, ctypes.c_size_t, P, P, P, P, P, P,
                                 ctypes.c_size_t, P], I),
+        "moe_block_workspace_bytes": ([BS], ctypes.c_size_t),
+        "moe_block_forward": ([BS, P, ctypes.POINTER(moe_block_weights), P, P, ctypes.c_size_t, P], I),
+        "moe_rmsnorm": ([ctypes.c_int64, ctypes.c_int32, P, P, P, ctypes.c_float, P, P, P], I),
+        "moe_linear": ([ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, P, P, P, P], I),
+        "moe_rope_split": ([BS, P, P, P, P, P], I),
+        "moe_attention": ([BS, P, P, P, P, P], I),
+        "moe_residual_add": ([ctypes.c_int64, P, P, P, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -332,3 +352,64 @@ def layer_backward(x, w_gate, w1, w3, w2, dy, state, aux_coef: float = 0.0, ws=N
     dw2 = torch.empty(w2.shape, **f32)
     moe_layer_backward(shape, x, w_gate, w1, w3, w2, dy, aux_coef, state, dx, dw_gate, dw1, dw3, dw2, ws, stream)
     return dx, dw_gate, dw1, dw3, dw2
+
+
+# ------------------------------------------------------------ decoder block
+
+def make_block_shape(B: int, S: int, d: int, n_heads: int, n_kv_heads: int, ffn: int, head_dim: int = 128,
+                     E: int = 8, k: int = 2, eps: float = 1e-5, rope_base: float = 10000.0) -> moe_block_shape:
+    return moe_block_shape(int(B), int(S), int(d), int(n_heads), int(n_kv_heads), int(head_dim), int(ffn), int(E),
+                           int(k), float(eps), float(rope_base))
+
+
+def moe_block_workspace_bytes(shape: moe_block_shape) -> int:
+    return int(lib.moe_block_workspace_bytes(ctypes.byref(shape)))
+
+
+def block_weights(p: dict) -> moe_block_weights:
+    """p: device tensors attn_norm, wqkv, wo, ffn_norm, w_gate, w1, w3, w2 (bf16)."""
+    return moe_block_weights(*[_ptr(p[n]) for n, _ in moe_block_weights._fields_])
+
+
+def moe_block_forward(shape, x, weights: moe_block_weights, out, ws, stream=None):
+    _check("moe_block_forward", lib.moe_block_forward(ctypes.byref(shape), _ptr(x), ctypes.byref(weights), _ptr(out),
+                                                      _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def moe_rmsnorm(x, g, eps, y, add=None, h_out=None, stream=None):
+    rows, d = x.shape
+    _check("moe_rmsnorm", lib.moe_rmsnorm(rows, d, _ptr(x), _ptr(add), _ptr(g), float(eps), _ptr(h_out), _ptr(y),
+                                          _stream(stream)))
+
+
+def moe_linear(x, w, y, stream=None):
+    """y [rows][n_out] fp32 = x [rows][n_in] . w^T (bf16 operands)."""
+    rows, n_in = x.shape
+    _check("moe_linear", lib.moe_linear(rows, n_in, w.shape[0], _ptr(x), _ptr(w), _ptr(y), _stream(stream)))
+
+
+def moe_rope_split(shape, qkv, q, k, v, stream=None):
+    _check("moe_rope_split", lib.moe_rope_split(ctypes.byref(shape), _ptr(qkv), _ptr(q), _ptr(k), _ptr(v),
+                                                _stream(stream)))
+
+
+def moe_attention(shape, q, k, v, o, stream=None):
+    _check("moe_attention", lib.moe_attention(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(o),
+                                              _stream(stream)))
+
+
+def moe_residual_add(a, b, out, stream=None):
+    _check("moe_residual_add", lib.moe_residual_add(a.numel(), _ptr(a), _ptr(b), _ptr(out), _stream(stream)))
+
+
+def block_forward(x, p: dict, shape: moe_block_shape, ws=None, stream=None):
+    """Allocates out (and the workspace) with torch and calls moe_block_forward."""
+    if ws is None:
+        n = moe_block_workspace_bytes(shape)
+        if n == 0:
+            raise MoEError("moe_block_workspace_bytes", MOE_ERR_UNSUPPORTED)
+        ws = _bytes(n, x.device)
+    out = torch.empty_like(x)
+    moe_block_forward(shape, x, block_weights(p), out, ws, stream)
+    return out
+

@@ -113,3 +113,55 @@ def test_knobs_and_timeouts():
 def test_device_status_without_a_device_reports_cuda_error():
     code = ctypes.c_int32(0)
     assert moe.lib.moe_get_device_status(ctypes.byref(code), None) == moe.MOE_ERR_CUDA
+
+
+# ------------------------------------------------------------ decoder block
+
+def _block(**kw):
+    base = dict(B=1, S=4096, d=4096, n_heads=32, n_kv_heads=8, ffn=14336)
+    base.update(kw)
+    extra = {k: base.pop(k) for k in ("head_dim", "eps", "rope_base") if k in base}
+    return moe.make_block_shape(base["B"], base["S"], base["d"], base["n_heads"], base["n_kv_heads"], base["ffn"],
+                                **extra)
+
+
+def _block_forward(shape, ws_bytes=1 << 40, x=FAKE, out=ctypes.c_void_p(2 << 20)):
+    w = moe.moe_block_weights(*([FAKE] * 8))
+    return moe.lib.moe_block_forward(ctypes.byref(shape), x, ctypes.byref(w), out, FAKE, ws_bytes, None)
+
+
+def test_block_workspace_covers_its_buffers():
+    s = _block()
+    T, d = 4096, 4096
+    n = moe.moe_block_workspace_bytes(s)
+    own = T * d * 2 + T * 6144 * 4 + T * 4096 * 2 + 2 * T * 1024 * 2 + T * 4096 * 2 + 2 * T * d * 2
+    layer = moe.moe_workspace_bytes(moe.make_shape(T, d, 14336, moe.MOE_BF16))
+    assert own + layer <= n <= own + layer + 16 * 1024
+
+
+def test_block_shape_validation_codes():
+    assert _block_forward(_block(n_kv_heads=3)) == moe.MOE_ERR_INVALID_ARG      # 32 % 3
+    assert _block_forward(_block(B=0)) == moe.MOE_ERR_INVALID_ARG
+    assert _block_forward(_block(eps=-1.0)) == moe.MOE_ERR_INVALID_ARG
+    assert _block_forward(_block(rope_base=0.0)) == moe.MOE_ERR_INVALID_ARG
+    assert _block_forward(_block(head_dim=64)) == moe.MOE_ERR_UNSUPPORTED
+    assert _block_forward(_block(d=4000)) == moe.MOE_ERR_UNSUPPORTED
+    assert _block_forward(_block(n_heads=1, n_kv_heads=1)) == moe.MOE_ERR_UNSUPPORTED  # projection 384 wide
+    assert _block_forward(_block(), x=MISALIGNED) == moe.MOE_ERR_INVALID_ARG
+    assert _block_forward(_block(), out=FAKE) == moe.MOE_ERR_INVALID_ARG           # out aliases x
+    s = _block()
+    assert _block_forward(s, ws_bytes=moe.moe_block_workspace_bytes(s) - 1) == moe.MOE_ERR_WORKSPACE
+
+
+def test_block_step_validation_codes():
+    lib = moe.lib
+    assert lib.moe_rmsnorm(4, 12, FAKE, None, FAKE, 1e-5, None, FAKE, None) == moe.MOE_ERR_INVALID_ARG  # d % 8
+    assert lib.moe_rmsnorm(4, 16, FAKE, FAKE, FAKE, 1e-5, None, FAKE, None) == moe.MOE_ERR_INVALID_ARG  # no h_out
+    assert lib.moe_rmsnorm(0, 16, None, None, None, 1e-5, None, None, None) == moe.MOE_OK
+    assert lib.moe_linear(4, 96, 256, FAKE, FAKE, FAKE, None) == moe.MOE_ERR_UNSUPPORTED
+    assert lib.moe_linear(4, 64, 200, FAKE, FAKE, FAKE, None) == moe.MOE_ERR_UNSUPPORTED
+    assert lib.moe_linear(0, 64, 256, None, None, None, None) == moe.MOE_OK
+    assert lib.moe_residual_add(12, FAKE, FAKE, FAKE, None) == moe.MOE_ERR_INVALID_ARG
+    s = _block(head_dim=64)
+    assert lib.moe_attention(ctypes.byref(s), FAKE, FAKE, FAKE, FAKE, None) == moe.MOE_ERR_UNSUPPORTED
+    assert lib.moe_rope_split(ctypes.byref(_block()), None, FAKE, FAKE, FAKE, None) == moe.MOE_ERR_INVALID_ARG
