@@ -333,4 +333,312 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (warp == 1) tmem_dealloc(ctl->tmem_base, 256);
 }
 
+// ---------------------------------------------------------------------------
+// Two query heads of one KV group per CTA (grouped-query attention with an
+// even group): both heads read the same K and V tiles, loaded once. Each head
+// has its own 4 softmax warps, score tile S and accumulator O in tensor
+// memory (512 columns); the MMA warp alternates between the heads, so one
+// head's S = Q K^T and O += P V run on the tensor core while the other head's
+// softmax runs on the CUDA cores. P (bf16) is written into the head's S
+// columns with tcgen05.st and read from there as the A operand of P V: the
+// MMAs of one thread run in issue order, so O += P_j V_j has read P_j before
+// the next S = Q K_{j+1} overwrites those columns, and the completion of that
+// S also tells the softmax warps that O holds P_j V_j. The running maximum is
+// rescaled lazily: O and l keep their reference until a row's maximum grows by
+// more than 2^8 (the result is exact either way; the reference only bounds
+// the size of P).
+// ---------------------------------------------------------------------------
+constexpr int kAttnPairThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2-5 head 0, warps 6-9 head 1
+constexpr float kAttnRescaleLog2 = 8.f;
+
+struct AttnPairControl {
+    uint64_t q_full;
+    uint64_t kv_full[2];
+    uint64_t kv_empty[2];
+    uint64_t s_full[2];
+    uint64_t p_full[2];
+    uint64_t o_full[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+// Q0 | Q1 | K0 | V0 | K1 | V1 | control
+constexpr size_t kAttnPairSmemBytes = 1024 + 6 * (size_t)kAttnTileBytes + sizeof(AttnPairControl);
+static_assert(kAttnPairSmemBytes <= 227 * 1024, "attention CTA exceeds the shared memory of a CTA");
+
+__device__ __forceinline__ void attn_pair_abort(AttnPairControl* c, int where) {
+    report_error(MOE_ERR_TIMEOUT, K_ATTN, where);
+    *reinterpret_cast<volatile int*>(&c->abort_flag) = 1;
+}
+
+// Grid: n_qt * B * Hq / 2 CTAs, the query tiles with the most keys first.
+__global__ void __launch_bounds__(kAttnPairThreads, 1)
+    attention_pair_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+                          const __grid_constant__ CUtensorMap map_v, const AttnArgs a) {
+    extern __shared__ unsigned char attn_smem_raw[];
+    unsigned char* smem = align1024(attn_smem_raw);
+    AttnPairControl* ctl = reinterpret_cast<AttnPairControl*>(smem + 6 * (size_t)kAttnTileBytes);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint64_t tmo = a.timeout_ns;
+    volatile int* abort_flag = &ctl->abort_flag;
+
+    const int pairs = a.Hq >> 1;
+    const int per_qt = a.B * pairs;
+    const int qt = a.n_qt - 1 - (int)(blockIdx.x / per_qt);
+    const int rem = (int)(blockIdx.x % per_qt);
+    const int b = rem / pairs;
+    const int h0 = 2 * (rem - b * pairs);          // heads h0 and h0 + 1
+    const int kvh = h0 / (a.Hq / a.Hkv);
+    const int64_t row0 = (int64_t)b * a.S;
+    const int q0 = qt * kAttnTile;
+    const int nkv = qt + 1;
+
+    const uint32_t sQ = smem_u32(smem);
+    auto sQh = [&](int x) { return sQ + (uint32_t)x * kAttnTileBytes; };
+    auto sK = [&](int st) { return sQ + (uint32_t)(2 + 2 * st) * kAttnTileBytes; };
+    auto sV = [&](int st) { return sQ + (uint32_t)(3 + 2 * st) * kAttnTileBytes; };
+
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&ctl->q_full), 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(smem_u32(&ctl->kv_full[s]), 1);
+            mbar_init(smem_u32(&ctl->kv_empty[s]), 1);
+            mbar_init(smem_u32(&ctl->s_full[s]), 1);
+            mbar_init(smem_u32(&ctl->p_full[s]), 4);
+            mbar_init(smem_u32(&ctl->o_full[s]), 1);
+        }
+        mbar_init(smem_u32(&ctl->drain), 1);
+        ctl->abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&map_q);
+        tma_prefetch_desc(&map_k);
+        tma_prefetch_desc(&map_v);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&ctl->tmem_base), 512);
+        tmem_relinquish();
+    }
+    pdl_trigger();
+    pdl_wait();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    // head x: S (and P) at columns 256 x .. 256 x + 127, O at 256 x + 128 .. 256 x + 255
+    const uint32_t tmem = ctl->tmem_base;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA
+        if (lane == 0) {
+            const uint64_t pol_q = policy_evict_first();
+            const uint64_t pol_kv = policy_evict_normal();
+            const uint32_t qb = smem_u32(&ctl->q_full);
+            mbar_arrive_expect_tx(qb, 2 * kAttnTileBytes);
+            for (int x = 0; x < 2; ++x) {
+                tma_load_2d(sQh(x), &map_q, qb, (h0 + x) * kAttnHD, (int)(row0 + q0), pol_q);
+                tma_load_2d(sQh(x) + kAttnBox, &map_q, qb, (h0 + x) * kAttnHD + 64, (int)(row0 + q0), pol_q);
+            }
+            uint32_t issued = 0, issued_ph = 0;
+            for (int j = 0; j < nkv; ++j) {
+                const int st = j & 1;
+                const uint32_t ph = (uint32_t)(j >> 1) & 1u;
+                if (!mbar_wait(smem_u32(&ctl->kv_empty[st]), ph ^ 1u, tmo, abort_flag)) {
+                    attn_pair_abort(ctl, W_PRODUCER);
+                    break;
+                }
+                const uint32_t fb = smem_u32(&ctl->kv_full[st]);
+                mbar_arrive_expect_tx(fb, 2 * kAttnTileBytes);
+                const int ky = (int)(row0 + (int64_t)j * kAttnTile);
+                tma_load_2d(sK(st), &map_k, fb, kvh * kAttnHD, ky, pol_kv);
+                tma_load_2d(sK(st) + kAttnBox, &map_k, fb, kvh * kAttnHD + 64, ky, pol_kv);
+                tma_load_2d(sV(st), &map_v, fb, kvh * kAttnHD, ky, pol_kv);
+                tma_load_2d(sV(st) + kAttnBox, &map_v, fb, kvh * kAttnHD + 64, ky, pol_kv);
+                issued |= 1u << st;
+                issued_ph = (issued_ph & ~(1u << st)) | (ph << st);
+            }
+            drain_wait(smem_u32(&ctl->q_full), 0, tmo, K_ATTN);
+            for (int st = 0; st < 2; ++st)
+                if (issued & (1u << st)) drain_wait(smem_u32(&ctl->kv_full[st]), (issued_ph >> st) & 1u, tmo, K_ATTN);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128);
+            constexpr uint32_t idesc_o = idesc_bf16_f32(128, 128, false, true);
+            bool ok = mbar_wait(smem_u32(&ctl->q_full), 0, tmo, abort_flag) &&
+                      mbar_wait(smem_u32(&ctl->kv_full[0]), 0, tmo, abort_flag);
+            bool any = false;
+            auto issue_s = [&](int x, int st) {
+                const uint32_t d = tmem + 256u * (uint32_t)x;
+#pragma unroll
+                for (int kk = 0; kk < kAttnHD / 16; ++kk) {
+                    const uint32_t off = (uint32_t)(kk >> 2) * kAttnBox;
+                    const uint64_t ad = sw128_kmajor_desc(sQh(x) + off) + 2ull * (kk & 3);
+                    const uint64_t bd = sw128_kmajor_desc(sK(st) + off) + 2ull * (kk & 3);
+                    mma_bf16(d, ad, bd, idesc_s, kk > 0);
+                }
+                mma_commit(smem_u32(&ctl->s_full[x]));
+            };
+            if (ok) {
+                tc_fence_after();
+                issue_s(0, 0);
+                issue_s(1, 0);
+                any = true;
+            } else {
+                attn_pair_abort(ctl, W_MMA);
+            }
+            for (int j = 0; ok && j < nkv; ++j) {
+                const int st = j & 1;
+                for (int x = 0; ok && x < 2; ++x) {
+                    if (!mbar_wait(smem_u32(&ctl->p_full[x]), (uint32_t)j & 1u, tmo, abort_flag)) {
+                        attn_pair_abort(ctl, W_MMA);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t p_tmem = tmem + 256u * (uint32_t)x;
+                    const uint32_t o_tmem = p_tmem + 128u;
+#pragma unroll
+                    for (int kk = 0; kk < kAttnTile / 16; ++kk) {
+                        const uint64_t bd = sw128_mnmajor_desc(sV(st), kAttnBox) + 128ull * kk;
+                        mma_bf16_ts(o_tmem, p_tmem + 8u * (uint32_t)kk, bd, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    if (x == 1) mma_commit(smem_u32(&ctl->kv_empty[st]));  // both heads are done with K_j, V_j
+                    if (j + 1 < nkv) {
+                        if (x == 0 &&
+                            !mbar_wait(smem_u32(&ctl->kv_full[st ^ 1]), (uint32_t)((j + 1) >> 1) & 1u, tmo, abort_flag)) {
+                            attn_pair_abort(ctl, W_MMA);
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        issue_s(x, st ^ 1);
+                    } else {
+                        mma_commit(smem_u32(&ctl->o_full[x]));
+                    }
+                }
+            }
+            if (any) {
+                mma_commit(smem_u32(&ctl->drain));
+                drain_wait(smem_u32(&ctl->drain), 0, tmo, K_ATTN);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ softmax + epilogue of one head
+        const int x = (warp - 2) >> 2;             // head slot
+        const int sub = warp & 3;                  // tensor-memory lanes 32 sub .. 32 sub + 31
+        const int row = sub * 32 + lane;
+        const int qpos = q0 + row;
+        const uint32_t lane_off = (uint32_t)(sub * 32) << 16;
+        const uint32_t tS = tmem + 256u * (uint32_t)x + lane_off;
+        const uint32_t tO = tS + 128u;
+        const float sl2 = a.scale_log2;
+        float m_ref = 0.f, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < nkv; ++j) {
+            // warp-wide vote: the tensor-memory loads and stores below need all 32 lanes
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->s_full[x]), (uint32_t)j & 1u, tmo, abort_flag))) {
+                attn_pair_abort(ctl, W_EPILOGUE);
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t sv[128];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) tmem_ld16(tS + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(&sv[16 * c]));
+            tmem_wait_ld();
+            if (j == qt) {
+                // the diagonal tile: keys after the query, and past the sequence's end, drop out
+                const int kbase = j * kAttnTile;
+#pragma unroll
+                for (int c = 0; c < 128; ++c) {
+                    const int key = kbase + c;
+                    if (key > qpos || (int64_t)key >= a.S) sv[c] = __float_as_uint(-INFINITY);
+                }
+            }
+            // row maximum over 8 independent chains
+            float mx8[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) mx8[i] = __uint_as_float(sv[i]);
+#pragma unroll
+            for (int c = 8; c < 128; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], __uint_as_float(sv[c]));
+            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+            const float m_tile = mx * sl2;
+            if (j == 0) {
+                m_ref = m_tile == -INFINITY ? 0.f : m_tile;
+            } else {
+                const bool grow = m_tile > m_ref + kAttnRescaleLog2;
+                if (__any_sync(0xffffffffu, grow)) {
+                    // O holds P_{j-1} V_{j-1} (the MMA that wrote S_j ran after it): rescale it in place
+                    const float m_new = grow ? m_tile : m_ref;
+                    const float alpha = fast_exp2(m_ref - m_new);
+#pragma unroll 1
+                    for (int c = 0; c < 8; ++c) {
+                        uint32_t o[16];
+                        tmem_ld16(tO + 16 * c, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        tmem_st16(tO + 16 * c, o);
+                    }
+                    l *= alpha;
+                    m_ref = m_new;
+                }
+            }
+            float sum8[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) sum8[i] = 0.f;
+            uint32_t pk[64];
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+                const float p0 = fast_exp2(fmaf(__uint_as_float(sv[2 * c]), sl2, -m_ref));
+                const float p1 = fast_exp2(fmaf(__uint_as_float(sv[2 * c + 1]), sl2, -m_ref));
+                sum8[c & 7] += p0 + p1;
+                pk[c] = pack_bf16x2(p0, p1);
+            }
+            l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+            // P over the first 64 columns of S: keys 2c and 2c + 1 in column c
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_st16(tS + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(&pk[16 * c]));
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&ctl->p_full[x]));
+        }
+        if (ok && __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->o_full[x]), 0, tmo, abort_flag))) {
+            tc_fence_after();
+            const float inv_l = 1.f / l;
+            const bool valid = (int64_t)qpos < a.S;
+            __nv_bfloat16* out = a.o + (row0 + qpos) * (int64_t)a.Hq * kAttnHD + (int64_t)(h0 + x) * kAttnHD;
+#pragma unroll 1
+            for (int c = 0; c < 8; ++c) {
+                uint32_t o[16];
+                tmem_ld16(tO + 16 * c, o);
+                tmem_wait_ld();
+                uint32_t pk[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+                if (valid) {
+                    uint4* dst = reinterpret_cast<uint4*>(out + 16 * c);
+                    dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                }
+            }
+        } else if (ok) {
+            attn_pair_abort(ctl, W_EPILOGUE);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(ctl->tmem_base, 512);
+}
+
 }  // namespace moe

@@ -957,7 +957,6 @@ moe_status run_attention(const moe_block_shape& s, const void* q, const void* k,
         !make_map(&mk, k, (uint64_t)s.n_kv_heads * kAttnHD, (uint64_t)T, 128) ||
         !make_map(&mv, v, (uint64_t)s.n_kv_heads * kAttnHD, (uint64_t)T, 128))
         return MOE_ERR_CUDA;
-    if (!ensure_smem(attention_kernel, 11, kAttnSmemBytes)) return MOE_ERR_CUDA;
     AttnArgs a{};
     a.o = static_cast<__nv_bfloat16*>(o);
     a.S = s.S;
@@ -967,8 +966,18 @@ moe_status run_attention(const moe_block_shape& s, const void* q, const void* k,
     a.n_qt = (int)((s.S + kAttnTile - 1) / kAttnTile);
     a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)s.head_dim));
     a.timeout_ns = g.timeout_ns;
-    const int64_t grid = (int64_t)a.n_qt * s.B * s.n_heads;
+    // heads of an even GQA group go two per CTA and share their K and V tiles
+    const bool paired = (s.n_heads / s.n_kv_heads) % 2 == 0;
+    const int64_t grid = (int64_t)a.n_qt * s.B * (paired ? s.n_heads / 2 : s.n_heads);
     if (grid > INT32_MAX) return MOE_ERR_UNSUPPORTED;
+    if (paired) {
+        if (!ensure_smem(attention_pair_kernel, 14, kAttnPairSmemBytes)) return MOE_ERR_CUDA;
+        return launch("attention", st, [&] {
+            return klaunch(attention_pair_kernel, dim3((unsigned)grid), dim3(kAttnPairThreads), kAttnPairSmemBytes, st,
+                           mq, mk, mv, a);
+        });
+    }
+    if (!ensure_smem(attention_kernel, 11, kAttnSmemBytes)) return MOE_ERR_CUDA;
     return launch("attention", st, [&] {
         return klaunch(attention_kernel, dim3((unsigned)grid), dim3(kAttnThreads), kAttnSmemBytes, st, mq, mk, mv, a);
     });
