@@ -62,6 +62,36 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float fmax3f(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// (a0, a1) * (b0, b1) + (c0, c1) as one paired fp32 FMA.
+__device__ __forceinline__ void ffma2(float a0, float a1, float b0, float b1, float c0, float c1, float& d0, float& d1) {
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rb, {%4, %5};\n\t"
+        "mov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
+// (a0, a1) + (b0, b1) as one paired fp32 add.
+__device__ __forceinline__ void fadd2(float a0, float a1, float b0, float b1, float& d0, float& d1) {
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 __device__ __forceinline__ void attn_abort(AttnControl* c, int where) {
     report_error(MOE_ERR_TIMEOUT, K_ATTN, where);
     *reinterpret_cast<volatile int*>(&c->abort_flag) = 1;
@@ -550,9 +580,10 @@ __global__ void __launch_bounds__(kAttnPairThreads, 1)
             tc_fence_after();
             uint32_t sv[128];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) tmem_ld16(tS + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(&sv[16 * c]));
+            for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, &sv[32 * c]);
             tmem_wait_ld();
-            if (j == qt) {
+            const bool diag = j == qt;
+            if (diag) {
                 // the diagonal tile: keys after the query, and past the sequence's end, drop out
                 const int kbase = j * kAttnTile;
 #pragma unroll
@@ -561,14 +592,16 @@ __global__ void __launch_bounds__(kAttnPairThreads, 1)
                     if (key > qpos || (int64_t)key >= a.S) sv[c] = __float_as_uint(-INFINITY);
                 }
             }
-            // row maximum over 8 independent chains
-            float mx8[8];
+            // row maximum: three-input max over 4 independent chains
+            float mx4[4];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) mx8[i] = __uint_as_float(sv[i]);
+            for (int i = 0; i < 4; ++i) mx4[i] = fmaxf(__uint_as_float(sv[i]), __uint_as_float(sv[4 + i]));
 #pragma unroll
-            for (int c = 8; c < 128; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], __uint_as_float(sv[c]));
-            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+            for (int c = 8; c < 128; c += 8)
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    mx4[i] = fmax3f(mx4[i], __uint_as_float(sv[c + i]), __uint_as_float(sv[c + 4 + i]));
+            const float mx = fmax3f(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]));
             const float m_tile = mx * sl2;
             if (j == 0) {
                 m_ref = m_tile == -INFINITY ? 0.f : m_tile;
@@ -591,18 +624,23 @@ __global__ void __launch_bounds__(kAttnPairThreads, 1)
                     m_ref = m_new;
                 }
             }
-            float sum8[8];
+            // p = 2^(s log2(e) / sqrt(hd) - m): the scaling as paired FMAs, row
+            // sums over 4 paired chains. (Moving a share of the exponentials to
+            // a polynomial on the FMA pipe measured slower: the softmax is
+            // bound by instruction issue, not by the special-function unit.)
+            float sa[4], sb[4];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) sum8[i] = 0.f;
+            for (int i = 0; i < 4; ++i) sa[i] = sb[i] = 0.f;
             uint32_t pk[64];
 #pragma unroll
             for (int c = 0; c < 64; ++c) {
-                const float p0 = fast_exp2(fmaf(__uint_as_float(sv[2 * c]), sl2, -m_ref));
-                const float p1 = fast_exp2(fmaf(__uint_as_float(sv[2 * c + 1]), sl2, -m_ref));
-                sum8[c & 7] += p0 + p1;
+                float x0, x1;
+                ffma2(__uint_as_float(sv[2 * c]), __uint_as_float(sv[2 * c + 1]), sl2, sl2, -m_ref, -m_ref, x0, x1);
+                const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+                fadd2(sa[c & 3], sb[c & 3], p0, p1, sa[c & 3], sb[c & 3]);
                 pk[c] = pack_bf16x2(p0, p1);
             }
-            l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+            l += ((sa[0] + sb[0]) + (sa[1] + sb[1])) + ((sa[2] + sb[2]) + (sa[3] + sb[3]));
             // P over the first 64 columns of S: keys 2c and 2c + 1 in column c
 #pragma unroll
             for (int c = 0; c < 4; ++c) tmem_st16(tS + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(&pk[16 * c]));
