@@ -502,7 +502,7 @@ def run_block(args) -> dict:
     T = B * S
 
     def step():
-        moe.moe_block_forward(shape, p["x"], wts, out, ws, stream)
+        moe.moe_block_forward(shape, p["x"], wts, out, ws, stream=stream)
 
     for _ in range(args.warmup):
         step()
@@ -581,6 +581,88 @@ def run_block(args) -> dict:
                       "timing": "50 launches back to back on seeded q, k, v of the block's shapes"},
         "projections_tflops": {"linear_qkv": tf("linear_qkv"), "linear_o": tf("linear_o")},
         "longest_kernel": dom,
+        "kernels_ms_per_step": {n: round(v[1] / max(1, args.steps), 5) for n, v in kern.items()},
+        "kernels_timing": "CUDA events around each launch, launches serialised (no programmatic dependent launch)",
+        "gpu_launches": int(sum(v[0] for v in kern.values())),
+        "clocks": sampler.summary(),
+    }
+
+
+def run_block_decode(args) -> dict:
+    """One decode step of the Mixtral decoder block: 16 sequences, one new token each, against key/value
+    caches holding 4096 earlier tokens (seeded values) -- the block around the decode batch of the layer."""
+    import torch
+
+    from moe_inputs import CONFIGS, make_block, make_weights
+    from sparse_mixture_experts_53_b300 import moe
+
+    torch.cuda.set_device(0)
+    moe.moe_set_knob(moe.MOE_KNOB_PDL, args.pdl)
+    B, L, d, Hq, Hkv, F, hd = 16, 4096, 4096, 32, 8, 14336, 128
+    cfg = CONFIGS[1]
+    experts = make_weights(d, F, 8, "bf16", cfg["weight_seed"])
+    p = {k: v.cuda() for k, v in make_block(B, 1, d, Hq, Hkv, F, seed=5350, weight_seed=5310,
+                                            moe_weights=experts).items()}
+    del experts
+    cmax = L + args.warmup + 2 * args.steps + 8
+    shape = moe.make_block_shape(B, 1, d, Hq, Hkv, F, cache_max=cmax)
+    g = torch.Generator(device="cuda").manual_seed(5351)
+    kc = torch.randn((B, Hkv, cmax, hd), device="cuda", generator=g).to(torch.bfloat16)
+    vc = torch.randn((B, Hkv, cmax, hd), device="cuda", generator=g).to(torch.bfloat16)
+    clen = torch.full((B,), L, dtype=torch.int32, device="cuda")
+    ws = torch.empty(moe.moe_block_decode_workspace_bytes(shape), dtype=torch.uint8, device="cuda")
+    wts = moe.block_weights(p)
+    out = torch.empty_like(p["x"])
+    stream = torch.cuda.current_stream()
+
+    def step():
+        moe.moe_block_decode(shape, p["x"], wts, kc, vc, clen, out, ws, stream)
+
+    for _ in range(args.warmup):
+        step()
+    code, detail = moe.moe_get_device_status()
+    if code != moe.MOE_OK:
+        raise RuntimeError(f"device status after warm-up: {moe.status_string(code)} ({detail})")
+    sampler = ClockSampler(0)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ctx0 = int(clen[0].item())
+    torch.cuda.synchronize()
+    with sampler:
+        a.record(stream)
+        for _ in range(args.steps):
+            step()
+        b.record(stream)
+        torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / args.steps
+    moe.moe_set_knob(moe.MOE_KNOB_PDL, 0)
+    moe.moe_timing_enable(True)
+    for _ in range(args.steps):
+        step()
+    torch.cuda.synchronize()
+    kern = moe.moe_timing_read()
+    moe.moe_timing_enable(False)
+    moe.moe_set_knob(moe.MOE_KNOB_PDL, args.pdl)
+    code, detail = moe.moe_get_device_status()
+    if code != moe.MOE_OK:
+        raise RuntimeError(f"device status after timing: {moe.status_string(code)} ({detail})")
+    per = {n: v[1] / v[0] for n, v in kern.items()}
+    peaks = _peaks()
+    ctx = ctx0 + args.steps // 2 + 1                   # keys per sequence, middle of the timed steps
+    cache_bytes = 2.0 * B * ctx * Hkv * hd * 2         # keys and values read once
+    att_ms = per.get("attention_decode", 0.0)
+    return {
+        "metric": "Mixtral decoder-block decode tokens/s (16 sequences, 4096-token caches, bf16)",
+        "value": round(B / (ms * 1e-3), 1), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "dtype": "bf16",
+        "data": "synthetic (seeded Mixtral-shape block and cache values, random init)",
+        "config": {"workload": "mixtral_block_decode_B16_ctx4096", "B": B, "context": L, "d": d, "n_heads": Hq,
+                   "n_kv_heads": Hkv, "head_dim": hd, "ffn": F, "E": 8, "k": 2},
+        "attention_decode": {"bound": "hbm", "launch_ms": round(att_ms, 5),
+                             "achieved": round(cache_bytes / (att_ms * 1e-3) / 1e9, 1) if att_ms else None,
+                             "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                             "frac": round(cache_bytes / (att_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)
+                             if att_ms else None,
+                             "bytes": cache_bytes},
         "kernels_ms_per_step": {n: round(v[1] / max(1, args.steps), 5) for n, v in kern.items()},
         "kernels_timing": "CUDA events around each launch, launches serialised (no programmatic dependent launch)",
         "gpu_launches": int(sum(v[0] for v in kern.values())),
@@ -708,6 +790,8 @@ def main():
                     help="time a training step (forward that keeps its state + backward) instead of the forward")
     ap.add_argument("--block", action="store_true",
                     help="time the decoder block around the layer (attention + MoE) at the Mixtral shape")
+    ap.add_argument("--block-decode", action="store_true",
+                    help="time one decode step of the Mixtral block (16 sequences, 4096-token caches)")
     ap.add_argument("--tile-ctas", type=int, default=0, choices=[0, 1, 2, 4],
                     help="token tiles: automatic (0), single CTAs (1), CTA pairs (2), two pairs per cluster (4)")
     args = ap.parse_args()
@@ -716,6 +800,11 @@ def main():
     rank, world, local = _dist_env()
     if args.ep:
         print(json.dumps(run_ep(args)), flush=True)
+        return
+    if args.block_decode:
+        if args.impl != "ours" or world != 1:
+            raise SystemExit("--block-decode times this library's decode step on one GPU")
+        print(json.dumps(run_block_decode(args)), flush=True)
         return
     if args.block:
         if args.impl != "ours" or world != 1:

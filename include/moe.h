@@ -281,6 +281,7 @@ typedef struct {
     int32_t k;           /* experts per token: 2 */
     float eps;           /* RMSNorm epsilon */
     float rope_base;     /* RoPE base */
+    int64_t cache_max;   /* key/value cache capacity per sequence (0: no cache) */
 } moe_block_shape;
 
 typedef struct {
@@ -300,9 +301,28 @@ size_t moe_block_workspace_bytes(const moe_block_shape* s);
 /* out [B*S][d] bf16 = the decoder block applied to x [B*S][d] bf16 (device
  * pointers, 16-byte aligned; out may not alias x). Enqueues RMSNorm, the fused
  * Q/K/V projection, RoPE, attention, the Wo projection, the residual add fused
- * with the second RMSNorm, moe_layer_forward and the last residual add. */
-moe_status moe_block_forward(const moe_block_shape* s, const void* x, const moe_block_weights* w, void* out,
-                             void* ws, size_t ws_bytes, void* stream);
+ * with the second RMSNorm, moe_layer_forward and the last residual add.
+ * k_cache, v_cache (nullable, both or neither): [B][n_kv_heads][cache_max]
+ * [head_dim] bf16; when given, every sequence's keys (after RoPE) and values
+ * are also stored at positions 0 .. S-1 (needs S <= cache_max), ready for
+ * moe_block_decode. */
+moe_status moe_block_forward(const moe_block_shape* s, const void* x, const moe_block_weights* w, void* k_cache,
+                             void* v_cache, void* out, void* ws, size_t ws_bytes, void* stream);
+
+/* Workspace of moe_block_decode (0 for an unsupported shape). */
+size_t moe_block_decode_workspace_bytes(const moe_block_shape* s);
+
+/* One decode step: B sequences, one new token each (s->S must be 1).
+ * x [B][d] bf16 holds the new tokens; cache_len [B] int32 (device) the number
+ * of tokens each sequence has cached, so the new token sits at that position.
+ * The step appends the token's key and value to the caches, attends over the
+ * cache (cache_len[b] + 1 keys), runs the rest of the block (the MoE layer on
+ * its weight-streaming path for up to 64 sequences) into out [B][d] bf16, and
+ * advances cache_len[b] by one, all on the device, so steps follow each other
+ * without a host round trip. A sequence whose cache is full (cache_len[b] >=
+ * cache_max) latches MOE_ERR_DEVICE_CHECK and is not appended. */
+moe_status moe_block_decode(const moe_block_shape* s, const void* x, const moe_block_weights* w, void* k_cache,
+                            void* v_cache, int32_t* cache_len, void* out, void* ws, size_t ws_bytes, void* stream);
 
 /* The block's steps, one call each (the same kernels moe_block_forward runs). */
 
@@ -313,20 +333,42 @@ moe_status moe_rmsnorm(int64_t rows, int32_t d, const void* x, const float* add,
                        void* h_out, void* y, void* stream);
 
 /* y [rows][n_out] fp32 = x [rows][n_in] . w^T, w [n_out][n_in] bf16 (a linear
- * layer; tcgen05 CTA-pair tiles of 256 rows x 256 columns). n_in % 64 == 0,
- * n_out % 256 == 0. */
-moe_status moe_linear(int64_t rows, int32_t n_in, int32_t n_out, const void* x, const void* w, float* y,
-                      void* stream);
+ * layer). n_in % 64 == 0, n_out % 256 == 0. Up to 64 rows with a workspace of
+ * moe_linear_workspace_bytes: weight streaming (128 weight rows x the rows per
+ * tcgen05 MMA, K split over the SMs, partials summed in slice order);
+ * otherwise (or ws NULL) CTA-pair tiles of 256 rows x 256 columns. */
+size_t moe_linear_workspace_bytes(int64_t rows, int32_t n_in, int32_t n_out);
+moe_status moe_linear(int64_t rows, int32_t n_in, int32_t n_out, const void* x, const void* w, float* y, void* ws,
+                      size_t ws_bytes, void* stream);
 
 /* Splits the fused projection qkv [B*S][(n_heads + 2 n_kv_heads) head_dim]
  * fp32 into q [B*S][n_heads head_dim], k and v [B*S][n_kv_heads head_dim]
- * (bf16), turning the channel pairs of q and k by RoPE. */
-moe_status moe_rope_split(const moe_block_shape* s, const float* qkv, void* q, void* k, void* v, void* stream);
+ * (bf16), turning the channel pairs of q and k by RoPE. Positions are t mod S
+ * within each sequence, or, with pos (device int32 [B], s->S == 1, decode),
+ * pos[b] for sequence b's one token. k_cache, v_cache (nullable, both or
+ * neither; [B][n_kv_heads][cache_max][head_dim]) also receive each key and
+ * value at its position; k and v may then be NULL. A position outside the
+ * cache latches MOE_ERR_DEVICE_CHECK and is not written. */
+moe_status moe_rope_split(const moe_block_shape* s, const float* qkv, const int32_t* pos, void* q, void* k, void* v,
+                          void* k_cache, void* v_cache, void* stream);
 
 /* Causal grouped-query attention of each sequence: o [B*S][n_heads head_dim]
  * bf16 from q, k, v as moe_rope_split writes them. head_dim must be 128. */
 moe_status moe_attention(const moe_block_shape* s, const void* q, const void* k, const void* v, void* o,
                          void* stream);
+
+/* Decode attention of one new token per sequence: q [B][n_heads head_dim]
+ * bf16 against the head-major caches ([B][n_kv_heads][cache_max][head_dim],
+ * the token's own key and value already stored at position cache_len[b]),
+ * cache_len[b] + 1 keys; o [B][n_heads head_dim] bf16. Splits each
+ * sequence's keys over a few CTAs per KV head (each streams its share in
+ * chunks of 64 keys through shared memory by bulk copies, with a running
+ * softmax) and merges the partials; advances cache_len[b] by one (up to
+ * cache_max). ws: moe_attention_decode_workspace_bytes. head_dim 128,
+ * n_heads / n_kv_heads one of 1, 2, 4, 8. */
+size_t moe_attention_decode_workspace_bytes(const moe_block_shape* s);
+moe_status moe_attention_decode(const moe_block_shape* s, const void* q, const void* k_cache, const void* v_cache,
+                                int32_t* cache_len, void* o, void* ws, size_t ws_bytes, void* stream);
 
 /* out [n] = bf16(a + b), bf16, n % 8 == 0. */
 moe_status moe_residual_add(int64_t n, const void* a, const void* b, void* out, void* stream);
@@ -336,7 +378,7 @@ moe_status moe_residual_add(int64_t n, const void* a, const void* b, void* out, 
  * *detail (nullable) receives 100 * kernel + where for diagnostics, with
  * kernel 1 router, 2 grouping, 3 row gather, 4 up tiles, 5 down tiles,
  * 6 streaming up, 7 streaming down, 12 the wait self-test, 13 backward tiles,
- * 16 attention, and where 1 TMA producer, 2 MMA issuer, 3 epilogue, 4 drain of in-flight
+ * 15 RoPE / cache append, 16 attention, and where 1 TMA producer, 2 MMA issuer, 3 epilogue, 4 drain of in-flight
  * work, 5 index check, 6 group larger than the kernel allows. Returns
  * MOE_ERR_CUDA if the device itself reports an error. */
 moe_status moe_get_device_status(int32_t* code, int32_t* detail);

@@ -29,4 +29,6 @@ from .decoder_block import (  # noqa: F401
     causal_gqa_attention,
     attention_sublayer,
     decoder_block,
+    attention_one_query,
+    decoder_block_decode,
 )

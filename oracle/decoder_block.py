@@ -35,7 +35,9 @@ Readings where the pages are silent (each is listed in the design doc):
 Parity status: every function here is pinned in tests/test_oracle_block_pins.py
 by closed forms (constant vectors, rotations by known angles, single-key and
 two-key attention, equal keys) and by invariants (causality, independence of
-the sequences of a batch, the residual paths).
+the sequences of a batch, the residual paths); the decode step is pinned
+against the whole-sequence block (the last token of a sequence computed both
+ways) and by a single-key closed form.
 """
 from __future__ import annotations
 
@@ -140,3 +142,48 @@ def decoder_block(x, p: dict, seq_len: int, n_heads: int, n_kv_heads: int, eps: 
     hn = rms_norm(a["h"], p["g_ffn"], eps)
     m = layer_forward(hn, p["w_gate"], p["w1"], p["w3"], p["w2"], k)
     return dict(a, hn=hn, moe=m, out=a["h"] + m["y"])
+
+
+def attention_one_query(q, k, v) -> np.ndarray:
+    """One new token per sequence: q [Hq][hd] against keys k, v [n][Hkv][hd] (all
+    positions up to and including the token's own) -> [Hq][hd]."""
+    Q, K, V = _f64(q), _f64(k), _f64(v)
+    Hq, hd = Q.shape
+    group = Hq // K.shape[1]
+    out = np.zeros((Hq, hd), dtype=np.float64)
+    for h in range(Hq):
+        s = K[:, h // group, :] @ Q[h] / np.sqrt(hd)
+        w = np.exp(s - s.max())
+        out[h] = (w / w.sum()) @ V[:, h // group, :]
+    return out
+
+
+def decoder_block_decode(x_new, k_prefix, v_prefix, p: dict, n_heads: int, n_kv_heads: int,
+                         eps: float = 1e-5, base: float = 10000.0, k: int = 2) -> dict:
+    """One decode step of the block for B sequences, one new token each.
+
+    x_new [B][d]; k_prefix[b], v_prefix[b] [L_b][Hkv][hd] hold the keys (after
+    RoPE) and values of the sequence's earlier tokens, so the new token sits at
+    position L_b. Returns out [B][d] and the new token's k, v (to append).
+    """
+    X = _f64(x_new)
+    B, d = X.shape
+    W = _f64(p["wqkv"])
+    hd = W.shape[0] // (n_heads + 2 * n_kv_heads)
+    xn = rms_norm(X, p["g_attn"], eps)
+    qkv = xn @ W.T
+    attn = np.zeros((B, n_heads * hd), dtype=np.float64)
+    k_new = np.zeros((B, n_kv_heads, hd))
+    v_new = np.zeros((B, n_kv_heads, hd))
+    for b in range(B):
+        pos = np.array([len(k_prefix[b])])
+        q = rope(qkv[b, :n_heads * hd].reshape(1, n_heads, hd), pos, base)[0]
+        k_new[b] = rope(qkv[b, n_heads * hd:(n_heads + n_kv_heads) * hd].reshape(1, n_kv_heads, hd), pos, base)[0]
+        v_new[b] = qkv[b, (n_heads + n_kv_heads) * hd:].reshape(n_kv_heads, hd)
+        keys = np.concatenate([_f64(k_prefix[b]).reshape(-1, n_kv_heads, hd), k_new[b][None]])
+        vals = np.concatenate([_f64(v_prefix[b]).reshape(-1, n_kv_heads, hd), v_new[b][None]])
+        attn[b] = attention_one_query(q, keys, vals).reshape(-1)
+    h = X + attn @ _f64(p["wo"]).T
+    hn = rms_norm(h, p["g_ffn"], eps)
+    m = layer_forward(hn, p["w_gate"], p["w1"], p["w3"], p["w2"], k)
+    return dict(h=h, hn=hn, attn=attn, moe=m, out=h + m["y"], k_new=k_new, v_new=v_new)

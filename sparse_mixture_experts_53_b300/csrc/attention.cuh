@@ -56,6 +56,16 @@ struct AttnArgs {
     uint64_t timeout_ns;
 };
 
+__device__ __forceinline__ void unpack_bf16x8_attn(const uint4& u, float (&v)[8]) {
+    const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(p[i]);
+        v[2 * i] = f.x;
+        v[2 * i + 1] = f.y;
+    }
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -677,6 +687,317 @@ __global__ void __launch_bounds__(kAttnPairThreads, 1)
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(ctl->tmem_base, 512);
+}
+
+// ---------------------------------------------------------------------------
+// Decode: one new token per sequence against its key/value cache. The cache
+// is head-major, [B][Hkv][cache_max][128] bf16, so a KV head's keys are one
+// contiguous run. CTA (split s, KV head, sequence) takes an equal share of the
+// n = len + 1 valid keys (the new token's were appended by the RoPE step), 64
+// keys per step, for the G query heads that share the KV head:
+//   S = Q K^T     tcgen05.mma M = 128 (rows 0 .. G-1 are the heads, the rest
+//                 zero), N = 64 keys, K = 128 channels; Q, K by TMA (128-byte
+//                 swizzle), S in tensor memory
+//   softmax       warp 0, one row per lane: running maximum and sum, O
+//                 rescaled in place when the maximum grows, P (bf16) written
+//                 over S
+//   O += P V      tcgen05.mma M = 128, N = 128 channels, K = 64 keys, P from
+//                 tensor memory, V as stored (MN-major)
+// Keys and values stream through two shared-memory stages, so the tensor core
+// only waits on HBM. Each CTA writes one unnormalised partial (O, m, l) per
+// head; a second kernel merges the splits in order (flash decoding).
+// ---------------------------------------------------------------------------
+constexpr int kDecChunk = 64;                        // keys per step
+constexpr int kDecThreads = 96;                      // warp 0 softmax, warp 1 TMA, warp 2 MMA
+constexpr int kDecMaxGroup = 32;                     // query heads per KV head (one row per lane)
+constexpr int kDecCtasPerSm = 2;
+constexpr uint32_t kDecBox = 64 * 64 * 2;            // 8 KB: 64 keys x 64 channels
+constexpr uint32_t kDecStageBytes = 4 * kDecBox;     // keys (two boxes) + values (two boxes)
+
+struct DecControl {
+    uint64_t q_full;
+    uint64_t kv_full[2];
+    uint64_t kv_empty[2];
+    uint64_t s_full, p_full, o_full, drain;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+// Q (128 rows x 128 channels) | stage 0 | stage 1 | control
+constexpr size_t kDecSmemBytes = 1024 + (size_t)kAttnTileBytes + 2 * (size_t)kDecStageBytes + sizeof(DecControl);
+
+struct DecodeArgs {
+    const int32_t* len;           // [B] keys cached before this token
+    float* part_o;                // [B][Hq][splits][hd]
+    float* part_ml;               // [B][Hq][splits][2]
+    int64_t cache_max;
+    int Hq, Hkv, splits;
+    float scale_log2;
+    uint64_t timeout_ns;
+};
+
+__device__ __forceinline__ void dec_abort(DecControl* c, int where) {
+    report_error(MOE_ERR_TIMEOUT, K_ATTN, where);
+    *reinterpret_cast<volatile int*>(&c->abort_flag) = 1;
+}
+
+// map_q: q viewed as [B Hq][128], boxes of 64 channels x G rows; map_k, map_v:
+// the caches viewed as [B Hkv cache_max][128], boxes of 64 channels x 64 keys.
+__global__ void __launch_bounds__(kDecThreads, 1)
+    attention_decode_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+                            const __grid_constant__ CUtensorMap map_v, const DecodeArgs a) {
+    extern __shared__ unsigned char dec_smem_raw[];
+    unsigned char* smem = align1024(dec_smem_raw);
+    DecControl* ctl = reinterpret_cast<DecControl*>(smem + kAttnTileBytes + 2 * (size_t)kDecStageBytes);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint64_t tmo = a.timeout_ns;
+    volatile int* abort_flag = &ctl->abort_flag;
+    const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+    const int G = a.Hq / a.Hkv;
+    const uint32_t sQ = smem_u32(smem);
+    auto sK = [&](int st) { return sQ + kAttnTileBytes + (uint32_t)st * kDecStageBytes; };
+    auto sV = [&](int st) { return sK(st) + 2 * kDecBox; };
+
+    // rows G .. 127 of the query tile stay zero: clear the tile before TMA writes rows 0 .. G-1
+    for (uint32_t i = threadIdx.x; i < kAttnTileBytes / 16; i += kDecThreads)
+        reinterpret_cast<uint4*>(smem)[i] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&ctl->q_full), 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(smem_u32(&ctl->kv_full[s]), 1);
+            mbar_init(smem_u32(&ctl->kv_empty[s]), 1);
+        }
+        mbar_init(smem_u32(&ctl->s_full), 1);
+        mbar_init(smem_u32(&ctl->p_full), 1);
+        mbar_init(smem_u32(&ctl->o_full), 1);
+        mbar_init(smem_u32(&ctl->drain), 1);
+        ctl->abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(smem_u32(&ctl->tmem_base), 256);
+        tmem_relinquish();
+    }
+    if (warp == 1 && lane == 0) {
+        tma_prefetch_desc(&map_q);
+        tma_prefetch_desc(&map_k);
+        tma_prefetch_desc(&map_v);
+    }
+    pdl_trigger();
+    pdl_wait();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tS = ctl->tmem_base;         // columns 0-63: scores (P over columns 0-31)
+    const uint32_t tO = ctl->tmem_base + 128;   // columns 128-255: output accumulator
+
+    const int64_t n_all = (int64_t)a.len[b] + 1;
+    const int64_t n = n_all < a.cache_max ? n_all : a.cache_max;
+    const int64_t nch = (n + kDecChunk - 1) / kDecChunk;
+    const int64_t per = (nch + a.splits - 1) / a.splits;
+    const int64_t c_begin = split * per;
+    const int64_t c_end = c_begin + per < nch ? c_begin + per : nch;
+    const int steps = c_end > c_begin ? (int)(c_end - c_begin) : 0;
+    const int64_t row0 = ((int64_t)b * a.Hkv + kvh) * a.cache_max;
+
+    if (warp == 1) {
+        // ------------------------------------------------------------ TMA
+        if (lane == 0 && steps > 0) {
+            const uint64_t pol = policy_evict_first();
+            const uint32_t qb = smem_u32(&ctl->q_full);
+            mbar_arrive_expect_tx(qb, 2u * (uint32_t)G * 128u);
+            tma_load_2d(sQ, &map_q, qb, 0, b * a.Hq + kvh * G, pol);
+            tma_load_2d(sQ + kAttnBox, &map_q, qb, 64, b * a.Hq + kvh * G, pol);
+            uint32_t issued = 0, issued_ph = 0;
+            for (int i = 0; i < steps; ++i) {
+                const int st = i & 1;
+                const uint32_t ph = (uint32_t)(i >> 1) & 1u;
+                if (!mbar_wait(smem_u32(&ctl->kv_empty[st]), ph ^ 1u, tmo, abort_flag)) {
+                    dec_abort(ctl, W_PRODUCER);
+                    break;
+                }
+                const uint32_t fb = smem_u32(&ctl->kv_full[st]);
+                mbar_arrive_expect_tx(fb, kDecStageBytes);
+                const int ky = (int)(row0 + (c_begin + i) * kDecChunk);
+                tma_load_2d(sK(st), &map_k, fb, 0, ky, pol);
+                tma_load_2d(sK(st) + kDecBox, &map_k, fb, 64, ky, pol);
+                tma_load_2d(sV(st), &map_v, fb, 0, ky, pol);
+                tma_load_2d(sV(st) + kDecBox, &map_v, fb, 64, ky, pol);
+                issued |= 1u << st;
+                issued_ph = (issued_ph & ~(1u << st)) | (ph << st);
+            }
+            drain_wait(smem_u32(&ctl->q_full), 0, tmo, K_ATTN);
+            for (int st = 0; st < 2; ++st)
+                if (issued & (1u << st)) drain_wait(smem_u32(&ctl->kv_full[st]), (issued_ph >> st) & 1u, tmo, K_ATTN);
+        }
+        __syncwarp();
+    } else if (warp == 2) {
+        // ------------------------------------------------------------ MMA
+        if (lane == 0 && steps > 0) {
+            constexpr uint32_t idesc_s = idesc_bf16_f32(128, kDecChunk);
+            constexpr uint32_t idesc_o = idesc_bf16_f32(128, 128, false, true);
+            bool ok = mbar_wait(smem_u32(&ctl->q_full), 0, tmo, abort_flag);
+            if (!ok) dec_abort(ctl, W_MMA);
+            bool any = false;
+            for (int i = 0; ok && i < steps; ++i) {
+                const int st = i & 1;
+                if (!mbar_wait(smem_u32(&ctl->kv_full[st]), (uint32_t)(i >> 1) & 1u, tmo, abort_flag)) {
+                    dec_abort(ctl, W_MMA);
+                    break;
+                }
+                tc_fence_after();
+                // S = Q K^T (issued after the previous P V, which read P from these columns)
+#pragma unroll
+                for (int kk = 0; kk < kAttnHD / 16; ++kk) {
+                    const uint32_t off = (uint32_t)(kk >> 2);
+                    const uint64_t ad = sw128_kmajor_desc(sQ + off * kAttnBox) + 2ull * (kk & 3);
+                    const uint64_t bd = sw128_kmajor_desc(sK(st) + off * kDecBox) + 2ull * (kk & 3);
+                    mma_bf16(tS, ad, bd, idesc_s, kk > 0);
+                }
+                any = true;
+                mma_commit(smem_u32(&ctl->s_full));
+                if (!mbar_wait(smem_u32(&ctl->p_full), (uint32_t)i & 1u, tmo, abort_flag)) {
+                    dec_abort(ctl, W_MMA);
+                    break;
+                }
+                tc_fence_after();
+                // O += P V
+#pragma unroll
+                for (int kk = 0; kk < kDecChunk / 16; ++kk) {
+                    const uint64_t bd = sw128_mnmajor_desc(sV(st), kDecBox) + 128ull * kk;
+                    mma_bf16_ts(tO, tS + 8u * (uint32_t)kk, bd, idesc_o, (i > 0 || kk > 0) ? 1u : 0u);
+                }
+                mma_commit(smem_u32(&ctl->kv_empty[st]));
+                if (i + 1 == steps) mma_commit(smem_u32(&ctl->o_full));
+            }
+            if (any) {
+                mma_commit(smem_u32(&ctl->drain));
+                drain_wait(smem_u32(&ctl->drain), 0, tmo, K_ATTN);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ softmax + partial (warp 0: lanes = rows)
+        const int row = lane;
+        const float sl2 = a.scale_log2;
+        float m_run = -INFINITY, l_run = 0.f;
+        bool ok = true;
+        for (int i = 0; i < steps; ++i) {
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->s_full), (uint32_t)i & 1u, tmo, abort_flag))) {
+                dec_abort(ctl, W_EPILOGUE);
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t sv[kDecChunk];
+            tmem_ld32(tS, &sv[0]);
+            tmem_ld32(tS + 32, &sv[32]);
+            tmem_wait_ld();
+            const int64_t k0 = (c_begin + i) * kDecChunk;
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < kDecChunk; ++c) {
+                if (k0 + c >= n) sv[c] = __float_as_uint(-INFINITY);
+                mx = fmaxf(mx, __uint_as_float(sv[c]));
+            }
+            const float m_new = fmaxf(m_run, mx * sl2);
+            const float m_use = m_new == -INFINITY ? 0.f : m_new;
+            const float alpha = m_run == -INFINITY ? 0.f : fast_exp2(m_run - m_use);
+            if (i > 0 && __any_sync(0xffffffffu, alpha < 1.f)) {
+                // O holds P_{i-1} V_{i-1} (the MMA that wrote S_i ran after it): rescale it in place
+#pragma unroll 1
+                for (int c = 0; c < 8; ++c) {
+                    uint32_t o[16];
+                    tmem_ld16(tO + 16 * c, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * alpha);
+                    tmem_st16(tO + 16 * c, o);
+                }
+            }
+            float sum = 0.f;
+            uint32_t pk[kDecChunk / 2];
+#pragma unroll
+            for (int c = 0; c < kDecChunk / 2; ++c) {
+                const float p0 = fast_exp2(fmaf(__uint_as_float(sv[2 * c]), sl2, -m_use));
+                const float p1 = fast_exp2(fmaf(__uint_as_float(sv[2 * c + 1]), sl2, -m_use));
+                sum += p0 + p1;
+                pk[c] = pack_bf16x2(p0, p1);
+            }
+            l_run = l_run * alpha + sum;
+            m_run = m_new;
+            tmem_st16(tS, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
+            tmem_st16(tS + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&ctl->p_full));
+        }
+        const int64_t part = ((int64_t)b * a.Hq + kvh * G + row) * a.splits + split;
+        if (ok && steps > 0 &&
+            __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->o_full), 0, tmo, abort_flag))) {
+            tc_fence_after();
+#pragma unroll 1
+            for (int c = 0; c < 8; ++c) {
+                uint32_t o[16];
+                tmem_ld16(tO + 16 * c, o);
+                tmem_wait_ld();
+                if (row < G) {
+                    float4* dst = reinterpret_cast<float4*>(a.part_o + part * kAttnHD + 16 * c);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        dst[q] = make_float4(__uint_as_float(o[4 * q]), __uint_as_float(o[4 * q + 1]),
+                                             __uint_as_float(o[4 * q + 2]), __uint_as_float(o[4 * q + 3]));
+                }
+            }
+        } else if (ok && steps > 0) {
+            dec_abort(ctl, W_EPILOGUE);
+        } else if (steps == 0 && row < G) {
+            // no keys for this split: an empty partial
+            for (int c = 0; c < kAttnHD; c += 4)
+                *reinterpret_cast<float4*>(a.part_o + part * kAttnHD + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        if (row < G) {
+            a.part_ml[2 * part] = m_run;
+            a.part_ml[2 * part + 1] = l_run;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(ctl->tmem_base, 256);
+}
+
+// out[b][h] = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c over the splits c
+// in order (empty ones carry m = -inf, l = 0), bf16. Block (h, b), one thread per
+// channel. The block of head 0 then advances the sequence's cache length
+// (nothing later in the step reads it).
+__global__ void __launch_bounds__(kAttnHD) attention_decode_merge_kernel(const float* __restrict__ part_o,
+                                                                         const float* __restrict__ part_ml, int Hq,
+                                                                         int chunks, int32_t* len, int64_t cache_max,
+                                                                         __nv_bfloat16* __restrict__ out) {
+    pdl_trigger();
+    pdl_wait();
+    const int h = blockIdx.x, b = blockIdx.y, e = threadIdx.x;
+    const int64_t hb = (int64_t)b * Hq + h;
+    const float* ml = part_ml + hb * chunks * 2;
+    const float* po = part_o + hb * chunks * kAttnHD + e;
+    float M = -INFINITY;
+#pragma unroll 8
+    for (int c = 0; c < chunks; ++c) M = fmaxf(M, ml[2 * c]);
+    float L = 0.f, O = 0.f;
+#pragma unroll 8
+    for (int c = 0; c < chunks; ++c) {
+        const float m = ml[2 * c];
+        const float w = m == -INFINITY ? 0.f : fast_exp2(m - M);
+        L = fmaf(w, ml[2 * c + 1], L);
+        O = fmaf(w, po[(int64_t)c * kAttnHD], O);
+    }
+    out[hb * kAttnHD + e] = __float2bfloat16_rn(O / L);
+    __syncthreads();
+    if (h == 0 && e == 0 && len[b] < cache_max) len[b] += 1;
 }
 
 }  // namespace moe

@@ -85,10 +85,14 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const __nv_bfloat
 struct RopeArgs {
     const float* qkv;     // [T][(Hq + 2 Hkv) hd] fp32: the fused projection's output
     __nv_bfloat16* q;     // [T][Hq hd]
-    __nv_bfloat16* k;     // [T][Hkv hd]
-    __nv_bfloat16* v;     // [T][Hkv hd]
+    __nv_bfloat16* k;     // [T][Hkv hd] (nullable: keys only to the cache)
+    __nv_bfloat16* v;     // [T][Hkv hd] (nullable)
     int64_t T;
-    int64_t S;            // tokens per sequence: position = t mod S
+    int64_t S;            // tokens per sequence (prefill): position = t mod S, sequence t / S
+    const int32_t* pos;   // decode: token t is sequence t's next token, at position pos[t] (nullable)
+    __nv_bfloat16* k_cache;  // [B][Hkv][cache_max][hd] (nullable): keys appended at their position
+    __nv_bfloat16* v_cache;
+    int64_t cache_max;
     int Hq, Hkv, hd;
     double theta[kRopeMaxPairs];  // base^(-2i/hd), i = 0 .. hd/2 - 1
 };
@@ -96,14 +100,25 @@ struct RopeArgs {
 // Block (hd/2, kRopeTokens): thread x handles channel pair x of every head of
 // one token. The angle pos * theta_i is formed and reduced modulo 2 pi in
 // double precision (pos reaches 32767 and beyond, where a float product would
-// be off by 1e-3 rad), then the reduced angle goes to sincosf.
+// be off by 1e-3 rad), then the reduced angle goes to sincosf. With caches,
+// the token's keys and values are also stored at their position in the
+// head-major caches (prefill: positions 0 .. S-1 of every sequence; decode:
+// position pos[t] of sequence t).
 __global__ void __launch_bounds__(256) rope_split_kernel(const __grid_constant__ RopeArgs a) {
     pdl_trigger();
     pdl_wait();
     const int i = threadIdx.x;
     const int64_t t = (int64_t)blockIdx.x * kRopeTokens + threadIdx.y;
     if (t >= a.T) return;
-    const double pos = (double)(t % a.S);
+    const int64_t seq = a.pos != nullptr ? t : t / a.S;
+    const int64_t p = a.pos != nullptr ? (int64_t)a.pos[t] : t % a.S;
+    // a cache write needs a slot: a full cache is reported and not written
+    bool to_cache = a.k_cache != nullptr;
+    if (to_cache && (p < 0 || p >= a.cache_max)) {
+        if (i == 0) report_error(MOE_ERR_DEVICE_CHECK, K_ROPE, W_INDEX);
+        to_cache = false;
+    }
+    const double pos = (double)p;
     const double twopi = 6.283185307179586476925;
     double ang = pos * a.theta[i];
     ang -= twopi * rint(ang / twopi);
@@ -113,19 +128,25 @@ __global__ void __launch_bounds__(256) rope_split_kernel(const __grid_constant__
     const float2* row = reinterpret_cast<const float2*>(a.qkv + t * W);
     const int P = a.hd >> 1;
     uint32_t* q = reinterpret_cast<uint32_t*>(a.q + t * (int64_t)a.Hq * a.hd);
-    uint32_t* k = reinterpret_cast<uint32_t*>(a.k + t * (int64_t)a.Hkv * a.hd);
-    uint32_t* v = reinterpret_cast<uint32_t*>(a.v + t * (int64_t)a.Hkv * a.hd);
+    uint32_t* k = a.k != nullptr ? reinterpret_cast<uint32_t*>(a.k + t * (int64_t)a.Hkv * a.hd) : nullptr;
+    uint32_t* v = a.v != nullptr ? reinterpret_cast<uint32_t*>(a.v + t * (int64_t)a.Hkv * a.hd) : nullptr;
     for (int h = 0; h < a.Hq; ++h) {
         const float2 z = row[h * P + i];
         q[h * P + i] = pack_bf16x2(z.x * cs - z.y * sn, z.x * sn + z.y * cs);
     }
     for (int h = 0; h < a.Hkv; ++h) {
         const float2 z = row[(a.Hq + h) * P + i];
-        k[h * P + i] = pack_bf16x2(z.x * cs - z.y * sn, z.x * sn + z.y * cs);
+        const uint32_t kv = pack_bf16x2(z.x * cs - z.y * sn, z.x * sn + z.y * cs);
+        if (k != nullptr) k[h * P + i] = kv;
+        if (to_cache)
+            reinterpret_cast<uint32_t*>(a.k_cache + ((seq * a.Hkv + h) * a.cache_max + p) * a.hd)[i] = kv;
     }
     for (int h = 0; h < a.Hkv; ++h) {
         const float2 z = row[(a.Hq + a.Hkv + h) * P + i];
-        v[h * P + i] = pack_bf16x2(z.x, z.y);
+        const uint32_t vv = pack_bf16x2(z.x, z.y);
+        if (v != nullptr) v[h * P + i] = vv;
+        if (to_cache)
+            reinterpret_cast<uint32_t*>(a.v_cache + ((seq * a.Hkv + h) * a.cache_max + p) * a.hd)[i] = vv;
     }
 }
 

@@ -798,6 +798,7 @@ struct StreamArgs {
     int stages;     // pipeline depth
     uint32_t stage_bytes;
     uint64_t timeout_ns;
+    int dense_rows;  // plain linear layer (offsets == nullptr, E == 1): one group of this many rows
 };
 
 inline size_t stream_smem_bytes(int nb, int stages) {
@@ -848,7 +849,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     pdl_wait();
     if (threadIdx.x == 0) {
         int n_act = 0;
-        for (int e = 0; e <= args.E; ++e) ctl->off[e] = args.offsets[e];
+        if (args.offsets != nullptr) {
+            for (int e = 0; e <= args.E; ++e) ctl->off[e] = args.offsets[e];
+        } else {
+            ctl->off[0] = 0;
+            ctl->off[1] = args.dense_rows;
+        }
         bool too_many = false;
         for (int e = 0; e < args.E; ++e) {
             const int c = ctl->off[e + 1] - ctl->off[e];
@@ -1048,7 +1054,7 @@ __global__ void __launch_bounds__(256)
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
         float acc = 0.f;
         for (int s = 0; s < S; ++s) acc += part[(int64_t)s * n + i];
-        y_slot[i] = perm_w[i / d] * acc;
+        y_slot[i] = perm_w != nullptr ? perm_w[i / d] * acc : acc;
     }
 }
 

@@ -848,7 +848,7 @@ moe_status check_block_shape(const moe_block_shape* s) {
         s->ffn <= 0 || !(s->eps >= 0.f) || !std::isfinite(s->eps) || !(s->rope_base > 0.f) ||
         !std::isfinite(s->rope_base))
         return MOE_ERR_INVALID_ARG;
-    if (s->n_heads % s->n_kv_heads != 0) return MOE_ERR_INVALID_ARG;
+    if (s->n_heads % s->n_kv_heads != 0 || s->cache_max < 0) return MOE_ERR_INVALID_ARG;
     if (s->head_dim != kAttnHD || s->d % 256 != 0 || s->ffn % 256 != 0 || s->E != 8 || s->k != 2)
         return MOE_ERR_UNSUPPORTED;
     // the fused projection runs on 256-column tiles
@@ -916,9 +916,65 @@ moe_status run_rmsnorm(int64_t rows, int d, const void* x, const float* add, con
     });
 }
 
+// Weight streaming for a linear layer of few rows (<= 64, a decode batch):
+// the streaming kernel's M side is 128 weight rows and its N side the rows of
+// x, K split into slices so that the units fill the GPU; fp32 partials per
+// slice, summed in slice order.
+struct LinearStreamPlan {
+    int ks = 0, S = 0, nb = 0;
+    size_t part_bytes = 0;
+};
+
+LinearStreamPlan linear_stream_plan(int64_t rows, int n_in, int n_out) {
+    LinearStreamPlan L;
+    if (rows < 1 || rows > kStreamMaxTokens || n_out % 128 != 0) return L;
+    const int64_t rb = n_out / 128, grid = sm_count();
+    double best_fill = -1.0;
+    // the largest slice (256 .. 2048, dividing n_in) whose units fill the last wave best
+    for (int ks = 256; ks <= 2048 && ks <= n_in; ks += kBK) {
+        if (n_in % ks != 0) continue;
+        const double waves = (double)(rb * (n_in / ks)) / (double)grid;
+        const double fill = waves / std::ceil(waves);
+        if (fill >= best_fill - 1e-9) {
+            best_fill = fill;
+            L.ks = ks;
+        }
+    }
+    if (L.ks == 0) L.ks = n_in;  // n_in < 256: one slice
+    L.S = n_in / L.ks;
+    L.nb = (int)align_up((size_t)rows, 16);
+    L.part_bytes = align_up((size_t)L.S * (size_t)rows * (size_t)n_out * 4, kAlign);
+    return L;
+}
+
 moe_status run_linear(int64_t rows, int n_in, int n_out, const void* x, const void* w, float* y, cudaStream_t st,
-                      const char* name = "linear") {
+                      const char* name = "linear", unsigned char* ws = nullptr, size_t ws_bytes = 0) {
     if (rows == 0) return MOE_OK;
+    const LinearStreamPlan P = linear_stream_plan(rows, n_in, n_out);
+    if (P.S > 0 && ws != nullptr && ws_bytes >= P.part_bytes) {
+        float* part = reinterpret_cast<float*>(ws);
+        const uint32_t stage_bytes = kStreamABytes + (uint32_t)align_up((size_t)P.nb * 128, 1024);
+        const int grid = tc_grid((int64_t)(n_out / 128) * P.S);
+        const size_t per_cta = kStreamInflightBytes / ((size_t)grid * kStreamABytes);
+        const size_t fit = (kSmemBudget - 1024 - sizeof(TcControl)) / stage_bytes;
+        const int stages = (int)std::max<size_t>(2, std::min<size_t>({per_cta, fit, (size_t)kMaxStreamStages}));
+        CUtensorMap mw, mx;
+        if (!make_map(&mw, w, (uint64_t)n_in, (uint64_t)n_out, 128) ||
+            !make_map(&mx, x, (uint64_t)n_in, (uint64_t)rows, (uint32_t)P.nb))
+            return MOE_ERR_CUDA;
+        if (!ensure_smem(stream_gemm_kernel<false>, 5, kSmemBudget)) return MOE_ERR_CUDA;
+        StreamArgs a{nullptr, part, 1, (int)rows, P.ks, P.S, n_out / 128, 1, n_out, P.nb, stages, stage_bytes,
+                     g.timeout_ns};
+        a.dense_rows = (int)rows;
+        MOE_TRY(launch(name, st, [&] {
+            return klaunch(stream_gemm_kernel<false>, grid, kTcThreads, stream_smem_bytes(P.nb, stages), st, mw, mw,
+                           mx, a);
+        }));
+        const int rgrid = (int)std::min<int64_t>((rows * n_out + 255) / 256, (int64_t)sm_count() * 8);
+        return launch("linear_reduce", st, [&] {
+            return klaunch(reduce_down_kernel, rgrid, 256, 0, st, part, P.S, rows, n_out, (const float*)nullptr, y);
+        });
+    }
     CUtensorMap ma, mb;
     if (!make_map(&ma, x, (uint64_t)n_in, (uint64_t)rows, 128) || !make_map(&mb, w, (uint64_t)n_in, (uint64_t)n_out, 128))
         return MOE_ERR_CUDA;
@@ -929,7 +985,8 @@ moe_status run_linear(int64_t rows, int n_in, int n_out, const void* x, const vo
     return launch_pair<PM_DOWN>(name, 7, 1, ma, mb, mb, a, units, st);
 }
 
-moe_status run_rope(const moe_block_shape& s, const float* qkv, void* q, void* k, void* v, cudaStream_t st) {
+moe_status run_rope(const moe_block_shape& s, const float* qkv, void* q, void* k, void* v, cudaStream_t st,
+                    const int32_t* pos = nullptr, void* k_cache = nullptr, void* v_cache = nullptr) {
     const int64_t T = s.B * s.S;
     if (T == 0) return MOE_OK;
     RopeArgs a{};
@@ -939,6 +996,10 @@ moe_status run_rope(const moe_block_shape& s, const float* qkv, void* q, void* k
     a.v = static_cast<__nv_bfloat16*>(v);
     a.T = T;
     a.S = s.S;
+    a.pos = pos;
+    a.k_cache = static_cast<__nv_bfloat16*>(k_cache);
+    a.v_cache = static_cast<__nv_bfloat16*>(v_cache);
+    a.cache_max = s.cache_max;
     a.Hq = s.n_heads;
     a.Hkv = s.n_kv_heads;
     a.hd = s.head_dim;
@@ -981,6 +1042,93 @@ moe_status run_attention(const moe_block_shape& s, const void* q, const void* k,
     return launch("attention", st, [&] {
         return klaunch(attention_kernel, dim3((unsigned)grid), dim3(kAttnThreads), kAttnSmemBytes, st, mq, mk, mv, a);
     });
+}
+
+// CTAs per (sequence, KV head) of the decode attention: enough that the grid fills every SM
+// with kDecCtasPerSm CTAs once, but no more splits than chunks of the cache.
+int decode_splits(const moe_block_shape& s) {
+    const int64_t pairs = std::max<int64_t>(1, s.B * s.n_kv_heads);
+    const int64_t want = std::max<int64_t>(1, (int64_t)kDecCtasPerSm * sm_count() / pairs);
+    const int64_t chunks = (s.cache_max + kDecChunk - 1) / kDecChunk;
+    return (int)std::max<int64_t>(1, std::min<int64_t>(want, chunks));
+}
+
+size_t decode_attention_ws_bytes(const moe_block_shape& s) {
+    const size_t parts = (size_t)s.B * s.n_heads * decode_splits(s);
+    return align_up(parts * kAttnHD * 4, kAlign) + align_up(parts * 2 * 4, kAlign);
+}
+
+bool decode_supported(const moe_block_shape& s) {
+    const int group = s.n_heads / s.n_kv_heads;
+    return s.S == 1 && s.cache_max >= 1 && group <= kDecMaxGroup && s.B <= 65535 && s.n_kv_heads <= 65535 &&
+           s.B * s.n_kv_heads * s.cache_max <= INT32_MAX && s.B * s.n_heads <= INT32_MAX;
+}
+
+moe_status run_attention_decode(const moe_block_shape& s, const void* q, const void* kc, const void* vc,
+                                int32_t* len, void* o, unsigned char* ws, cudaStream_t st) {
+    const int splits = decode_splits(s);
+    const size_t parts = (size_t)s.B * s.n_heads * splits;
+    const int group = s.n_heads / s.n_kv_heads;
+    CUtensorMap mq, mk, mv;
+    const uint64_t cache_rows = (uint64_t)s.B * s.n_kv_heads * s.cache_max;
+    if (!make_map(&mq, q, kAttnHD, (uint64_t)s.B * s.n_heads, (uint32_t)group) ||
+        !make_map(&mk, kc, kAttnHD, cache_rows, kDecChunk) || !make_map(&mv, vc, kAttnHD, cache_rows, kDecChunk))
+        return MOE_ERR_CUDA;
+    DecodeArgs a{};
+    a.len = len;
+    a.part_o = reinterpret_cast<float*>(ws);
+    a.part_ml = reinterpret_cast<float*>(ws + align_up(parts * kAttnHD * 4, kAlign));
+    a.cache_max = s.cache_max;
+    a.Hq = s.n_heads;
+    a.Hkv = s.n_kv_heads;
+    a.splits = splits;
+    a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)s.head_dim));
+    a.timeout_ns = g.timeout_ns;
+    if (!ensure_smem(attention_decode_kernel, 15, kDecSmemBytes)) return MOE_ERR_CUDA;
+    MOE_TRY(launch("attention_decode", st, [&] {
+        return klaunch(attention_decode_kernel, dim3((unsigned)splits, (unsigned)s.n_kv_heads, (unsigned)s.B),
+                       dim3(kDecThreads), kDecSmemBytes, st, mq, mk, mv, a);
+    }));
+    return launch("attention_decode_merge", st, [&] {
+        return klaunch(attention_decode_merge_kernel, dim3((unsigned)s.n_heads, (unsigned)s.B), dim3(kAttnHD), 0, st,
+                       (const float*)a.part_o, (const float*)a.part_ml, s.n_heads, splits, len, s.cache_max,
+                       static_cast<__nv_bfloat16*>(o));
+    });
+}
+
+struct DecodeLayout {
+    size_t xn, qkv, q, attn, h, y, lin, att, moe, total;
+    size_t lin_bytes;
+};
+
+// One decode step's buffers: xn [B][d] (later the second norm's output), the
+// projection output [B][max((Hq+2Hkv) hd, d)] fp32 (later Wo's), q and the
+// attention output [B][Hq hd], h and y [B][d], the linear layers' K-slice
+// partials, the attention partials, the MoE layer's workspace.
+DecodeLayout decode_layout(const moe_block_shape& s) {
+    const size_t B = (size_t)s.B, d = (size_t)s.d;
+    const size_t wq = (size_t)s.n_heads * s.head_dim, wqkv = wq + 2 * (size_t)s.n_kv_heads * s.head_dim;
+    DecodeLayout L{};
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off = align_up(off + bytes, kAlign);
+        return at;
+    };
+    L.xn = take(B * d * 2);
+    L.qkv = take(B * std::max(wqkv, d) * 4);
+    L.q = take(B * wq * 2);
+    L.attn = take(B * wq * 2);
+    L.h = take(B * d * 2);
+    L.y = take(B * d * 2);
+    L.lin_bytes = std::max(linear_stream_plan(s.B, s.d, (int)wqkv).part_bytes,
+                           linear_stream_plan(s.B, (int)wq, s.d).part_bytes);
+    L.lin = take(std::max<size_t>(L.lin_bytes, 16));
+    L.att = take(decode_attention_ws_bytes(s));
+    const moe_shape m = block_layer_shape(s);
+    L.moe = take(std::max<size_t>(moe_workspace_bytes(&m), 16));
+    L.total = off;
+    return L;
 }
 
 moe_status run_residual_add(int64_t n, const void* a, const void* b, void* out, cudaStream_t st) {
@@ -1142,14 +1290,19 @@ size_t moe_block_workspace_bytes(const moe_block_shape* s) {
     return block_layout(*s).total;
 }
 
-moe_status moe_block_forward(const moe_block_shape* s, const void* x, const moe_block_weights* w, void* out,
-                             void* ws, size_t ws_bytes, void* stream) {
+bool block_weights_ok(const moe_block_weights* w) {
+    return w != nullptr && ok_ptr(w->attn_norm) && ok_ptr(w->wqkv) && ok_ptr(w->wo) && ok_ptr(w->ffn_norm) &&
+           ok_ptr(w->w_gate) && ok_ptr(w->w1) && ok_ptr(w->w3) && ok_ptr(w->w2);
+}
+
+moe_status moe_block_forward(const moe_block_shape* s, const void* x, const moe_block_weights* w, void* k_cache,
+                             void* v_cache, void* out, void* ws, size_t ws_bytes, void* stream) {
     NvtxRange nvtx("moe_block_forward");
     MOE_TRY(check_block_shape(s));
-    if (w == nullptr || !ok_ptr(x) || !ok_ptr(out) || !ok_ptr(ws) || !ok_ptr(w->attn_norm) || !ok_ptr(w->wqkv) ||
-        !ok_ptr(w->wo) || !ok_ptr(w->ffn_norm) || !ok_ptr(w->w_gate) || !ok_ptr(w->w1) || !ok_ptr(w->w3) ||
-        !ok_ptr(w->w2) || x == out)
+    if (!block_weights_ok(w) || !ok_ptr(x) || !ok_ptr(out) || !ok_ptr(ws) || x == out)
         return MOE_ERR_INVALID_ARG;
+    if ((k_cache == nullptr) != (v_cache == nullptr)) return MOE_ERR_INVALID_ARG;
+    if (k_cache != nullptr && (!ok_ptr(k_cache) || !ok_ptr(v_cache) || s->S > s->cache_max)) return MOE_ERR_INVALID_ARG;
     const BlockLayout L = block_layout(*s);
     if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -1168,7 +1321,7 @@ moe_status moe_block_forward(const moe_block_shape* s, const void* x, const moe_
     // h = x + Wo attention(RoPE(Wq xn), RoPE(Wk xn), Wv xn), xn = RMSNorm(x)
     MOE_TRY(run_rmsnorm(T, d, x, nullptr, w->attn_norm, s->eps, nullptr, xn, st));
     MOE_TRY(run_linear(T, d, wq + 2 * wkv, xn, w->wqkv, qkv, st, "linear_qkv"));
-    MOE_TRY(run_rope(*s, qkv, q, k, v, st));
+    MOE_TRY(run_rope(*s, qkv, q, k, v, st, nullptr, k_cache, v_cache));
     MOE_TRY(run_attention(*s, q, k, v, attn, st));
     float* o = qkv;  // the projection output is consumed: Wo's output takes its place
     MOE_TRY(run_linear(T, wq, d, attn, w->wo, o, st, "linear_o"));
@@ -1178,6 +1331,68 @@ moe_status moe_block_forward(const moe_block_shape* s, const void* x, const moe_
     MOE_TRY(moe_layer_forward(&m, xn, w->w_gate, w->w1, w->w3, w->w2, y, nullptr, nullptr, nullptr, b + L.moe,
                               L.total - L.moe, stream));
     return run_residual_add(T * d, h, y, out, st);
+}
+
+size_t moe_block_decode_workspace_bytes(const moe_block_shape* s) {
+    if (check_block_shape(s) != MOE_OK || !decode_supported(*s)) return 0;
+    return decode_layout(*s).total;
+}
+
+moe_status moe_block_decode(const moe_block_shape* s, const void* x, const moe_block_weights* w, void* k_cache,
+                            void* v_cache, int32_t* cache_len, void* out, void* ws, size_t ws_bytes, void* stream) {
+    NvtxRange nvtx("moe_block_decode");
+    MOE_TRY(check_block_shape(s));
+    if (s->S != 1 || s->cache_max < 1) return MOE_ERR_INVALID_ARG;
+    if (!decode_supported(*s)) return MOE_ERR_UNSUPPORTED;
+    if (!block_weights_ok(w) || !ok_ptr(x) || !ok_ptr(out) || !ok_ptr(ws) || !ok_ptr(k_cache) || !ok_ptr(v_cache) ||
+        cache_len == nullptr || x == out)
+        return MOE_ERR_INVALID_ARG;
+    const DecodeLayout L = decode_layout(*s);
+    if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    unsigned char* b = static_cast<unsigned char*>(ws);
+    const int64_t B = s->B;
+    const int d = s->d;
+    const int wq = s->n_heads * s->head_dim, wkv = s->n_kv_heads * s->head_dim;
+    void* xn = b + L.xn;
+    float* qkv = reinterpret_cast<float*>(b + L.qkv);
+    void* q = b + L.q;
+    void* attn = b + L.attn;
+    void* h = b + L.h;
+    void* y = b + L.y;
+    unsigned char* lin = b + L.lin;
+    MOE_TRY(run_rmsnorm(B, d, x, nullptr, w->attn_norm, s->eps, nullptr, xn, st));
+    MOE_TRY(run_linear(B, d, wq + 2 * wkv, xn, w->wqkv, qkv, st, "linear_qkv", lin, L.lin_bytes));
+    // q to the workspace; the new key and value straight into the caches at position cache_len[b]
+    moe_block_shape one = *s;
+    one.S = 1;
+    MOE_TRY(run_rope(one, qkv, q, nullptr, nullptr, st, cache_len, k_cache, v_cache));
+    MOE_TRY(run_attention_decode(*s, q, k_cache, v_cache, cache_len, attn, b + L.att, st));
+    float* o = qkv;
+    MOE_TRY(run_linear(B, wq, d, attn, w->wo, o, st, "linear_o", lin, L.lin_bytes));
+    MOE_TRY(run_rmsnorm(B, d, x, o, w->ffn_norm, s->eps, h, xn, st));
+    const moe_shape m = block_layer_shape(*s);
+    MOE_TRY(moe_layer_forward(&m, xn, w->w_gate, w->w1, w->w3, w->w2, y, nullptr, nullptr, nullptr, b + L.moe,
+                              L.total - L.moe, stream));
+    return run_residual_add(B * d, h, y, out, st);
+}
+
+size_t moe_attention_decode_workspace_bytes(const moe_block_shape* s) {
+    if (check_block_shape(s) != MOE_OK || !decode_supported(*s)) return 0;
+    return decode_attention_ws_bytes(*s);
+}
+
+moe_status moe_attention_decode(const moe_block_shape* s, const void* q, const void* k_cache, const void* v_cache,
+                                int32_t* cache_len, void* o, void* ws, size_t ws_bytes, void* stream) {
+    NvtxRange nvtx("moe_attention_decode");
+    MOE_TRY(check_block_shape(s));
+    if (s->S != 1 || s->cache_max < 1) return MOE_ERR_INVALID_ARG;
+    if (!decode_supported(*s)) return MOE_ERR_UNSUPPORTED;
+    if (!ok_ptr(q) || !ok_ptr(k_cache) || !ok_ptr(v_cache) || cache_len == nullptr || !ok_ptr(o) || !ok_ptr(ws))
+        return MOE_ERR_INVALID_ARG;
+    if (ws_bytes < decode_attention_ws_bytes(*s)) return MOE_ERR_WORKSPACE;
+    return run_attention_decode(*s, q, k_cache, v_cache, cache_len, o, static_cast<unsigned char*>(ws),
+                                static_cast<cudaStream_t>(stream));
 }
 
 moe_status moe_rmsnorm(int64_t rows, int32_t d, const void* x, const float* add, const void* g, float eps,
@@ -1190,21 +1405,34 @@ moe_status moe_rmsnorm(int64_t rows, int32_t d, const void* x, const float* add,
     return run_rmsnorm(rows, d, x, add, g, eps, add != nullptr ? h_out : nullptr, y, static_cast<cudaStream_t>(stream));
 }
 
-moe_status moe_linear(int64_t rows, int32_t n_in, int32_t n_out, const void* x, const void* w, float* y,
-                      void* stream) {
+size_t moe_linear_workspace_bytes(int64_t rows, int32_t n_in, int32_t n_out) {
+    if (rows <= 0 || n_in <= 0 || n_out <= 0 || n_in % kBK != 0 || n_out % kTileN != 0) return 0;
+    return linear_stream_plan(rows, n_in, n_out).part_bytes;
+}
+
+moe_status moe_linear(int64_t rows, int32_t n_in, int32_t n_out, const void* x, const void* w, float* y, void* ws,
+                      size_t ws_bytes, void* stream) {
     NvtxRange nvtx("moe_linear");
     if (rows < 0 || n_in <= 0 || n_out <= 0) return MOE_ERR_INVALID_ARG;
     if (n_in % kBK != 0 || n_out % kTileN != 0 || rows > INT32_MAX) return MOE_ERR_UNSUPPORTED;
     if (rows == 0) return MOE_OK;
-    if (!ok_ptr(x) || !ok_ptr(w) || !ok_ptr(y)) return MOE_ERR_INVALID_ARG;
-    return run_linear(rows, n_in, n_out, x, w, y, static_cast<cudaStream_t>(stream));
+    if (!ok_ptr(x) || !ok_ptr(w) || !ok_ptr(y) || (ws != nullptr && !ok_ptr(ws))) return MOE_ERR_INVALID_ARG;
+    return run_linear(rows, n_in, n_out, x, w, y, static_cast<cudaStream_t>(stream), "linear",
+                      static_cast<unsigned char*>(ws), ws != nullptr ? ws_bytes : 0);
 }
 
-moe_status moe_rope_split(const moe_block_shape* s, const float* qkv, void* q, void* k, void* v, void* stream) {
+moe_status moe_rope_split(const moe_block_shape* s, const float* qkv, const int32_t* pos, void* q, void* k, void* v,
+                          void* k_cache, void* v_cache, void* stream) {
     NvtxRange nvtx("moe_rope_split");
     MOE_TRY(check_block_shape(s));
-    if (!ok_ptr(qkv) || !ok_ptr(q) || !ok_ptr(k) || !ok_ptr(v)) return MOE_ERR_INVALID_ARG;
-    return run_rope(*s, qkv, q, k, v, static_cast<cudaStream_t>(stream));
+    if (!ok_ptr(qkv) || !ok_ptr(q) || (k != nullptr && !ok_ptr(k)) || (v != nullptr && !ok_ptr(v)) ||
+        (k == nullptr) != (v == nullptr) || (k_cache == nullptr) != (v_cache == nullptr))
+        return MOE_ERR_INVALID_ARG;
+    if (k_cache != nullptr && (!ok_ptr(k_cache) || !ok_ptr(v_cache) || s->cache_max < 1)) return MOE_ERR_INVALID_ARG;
+    if (pos != nullptr && s->S != 1) return MOE_ERR_INVALID_ARG;
+    if (k == nullptr && k_cache == nullptr) return MOE_ERR_INVALID_ARG;
+    if (pos == nullptr && k_cache != nullptr && s->S > s->cache_max) return MOE_ERR_INVALID_ARG;
+    return run_rope(*s, qkv, q, k, v, static_cast<cudaStream_t>(stream), pos, k_cache, v_cache);
 }
 
 moe_status moe_attention(const moe_block_shape* s, const void* q, const void* k, const void* v, void* o,

@@ -41,7 +41,8 @@ EXPORTED = (
     "moe_timing_enable", "moe_timing_read", "moe_train_state_bytes", "moe_backward_workspace_bytes",
     "moe_layer_forward_train", "moe_layer_backward", "moe_gather_rows", "moe_selftest_wait_timeout",
     "moe_check_device_status", "moe_block_workspace_bytes", "moe_block_forward", "moe_rmsnorm", "moe_linear",
-    "moe_rope_split", "moe_attention", "moe_residual_add",
+    "moe_rope_split", "moe_attention", "moe_residual_add", "moe_block_decode_workspace_bytes", "moe_block_decode",
+    "moe_linear_workspace_bytes", "moe_attention_decode_workspace_bytes", "moe_attention_decode",
 )
 
 
@@ -54,7 +55,7 @@ class moe_block_shape(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int64), ("S", ctypes.c_int64), ("d", ctypes.c_int32), ("n_heads", ctypes.c_int32),
                 ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("ffn", ctypes.c_int32),
                 ("E", ctypes.c_int32), ("k", ctypes.c_int32), ("eps", ctypes.c_float),
-                ("rope_base", ctypes.c_float)]
+                ("rope_base", ctypes.c_float), ("cache_max", ctypes.c_int64)]
 
 
 class moe_block_weights(ctypes.Structure):
@@ -104,10 +105,15 @@ def _load() -> ctypes.CDLL:
         "moe_layer_backward": ([S, P, P, P, P, P, P, ctypes.c_float, P, ctypes.c_size_t, P, P, P, P, P, P,
                                 ctypes.c_size_t, P], I),
         "moe_block_workspace_bytes": ([BS], ctypes.c_size_t),
-        "moe_block_forward": ([BS, P, ctypes.POINTER(moe_block_weights), P, P, ctypes.c_size_t, P], I),
+        "moe_block_forward": ([BS, P, ctypes.POINTER(moe_block_weights), P, P, P, P, ctypes.c_size_t, P], I),
+        "moe_block_decode_workspace_bytes": ([BS], ctypes.c_size_t),
+        "moe_block_decode": ([BS, P, ctypes.POINTER(moe_block_weights), P, P, P, P, P, ctypes.c_size_t, P], I),
         "moe_rmsnorm": ([ctypes.c_int64, ctypes.c_int32, P, P, P, ctypes.c_float, P, P, P], I),
-        "moe_linear": ([ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, P, P, P, P], I),
-        "moe_rope_split": ([BS, P, P, P, P, P], I),
+        "moe_linear_workspace_bytes": ([ctypes.c_int64, ctypes.c_int32, ctypes.c_int32], ctypes.c_size_t),
+        "moe_linear": ([ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, P, P, P, P, ctypes.c_size_t, P], I),
+        "moe_rope_split": ([BS, P, P, P, P, P, P, P, P], I),
+        "moe_attention_decode_workspace_bytes": ([BS], ctypes.c_size_t),
+        "moe_attention_decode": ([BS, P, P, P, P, P, P, ctypes.c_size_t, P], I),
         "moe_attention": ([BS, P, P, P, P, P], I),
         "moe_residual_add": ([ctypes.c_int64, P, P, P, P], I),
     }
@@ -357,9 +363,10 @@ def layer_backward(x, w_gate, w1, w3, w2, dy, state, aux_coef: float = 0.0, ws=N
 # ------------------------------------------------------------ decoder block
 
 def make_block_shape(B: int, S: int, d: int, n_heads: int, n_kv_heads: int, ffn: int, head_dim: int = 128,
-                     E: int = 8, k: int = 2, eps: float = 1e-5, rope_base: float = 10000.0) -> moe_block_shape:
+                     E: int = 8, k: int = 2, eps: float = 1e-5, rope_base: float = 10000.0,
+                     cache_max: int = 0) -> moe_block_shape:
     return moe_block_shape(int(B), int(S), int(d), int(n_heads), int(n_kv_heads), int(head_dim), int(ffn), int(E),
-                           int(k), float(eps), float(rope_base))
+                           int(k), float(eps), float(rope_base), int(cache_max))
 
 
 def moe_block_workspace_bytes(shape: moe_block_shape) -> int:
@@ -371,9 +378,30 @@ def block_weights(p: dict) -> moe_block_weights:
     return moe_block_weights(*[_ptr(p[n]) for n, _ in moe_block_weights._fields_])
 
 
-def moe_block_forward(shape, x, weights: moe_block_weights, out, ws, stream=None):
-    _check("moe_block_forward", lib.moe_block_forward(ctypes.byref(shape), _ptr(x), ctypes.byref(weights), _ptr(out),
-                                                      _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+def moe_block_forward(shape, x, weights: moe_block_weights, out, ws, k_cache=None, v_cache=None, stream=None):
+    _check("moe_block_forward", lib.moe_block_forward(ctypes.byref(shape), _ptr(x), ctypes.byref(weights),
+                                                      _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(ws),
+                                                      ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def moe_block_decode_workspace_bytes(shape: moe_block_shape) -> int:
+    return int(lib.moe_block_decode_workspace_bytes(ctypes.byref(shape)))
+
+
+def moe_block_decode(shape, x, weights: moe_block_weights, k_cache, v_cache, cache_len, out, ws, stream=None):
+    _check("moe_block_decode", lib.moe_block_decode(ctypes.byref(shape), _ptr(x), ctypes.byref(weights),
+                                                    _ptr(k_cache), _ptr(v_cache), _ptr(cache_len), _ptr(out),
+                                                    _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def moe_attention_decode_workspace_bytes(shape: moe_block_shape) -> int:
+    return int(lib.moe_attention_decode_workspace_bytes(ctypes.byref(shape)))
+
+
+def moe_attention_decode(shape, q, k_cache, v_cache, cache_len, o, ws, stream=None):
+    _check("moe_attention_decode", lib.moe_attention_decode(ctypes.byref(shape), _ptr(q), _ptr(k_cache),
+                                                            _ptr(v_cache), _ptr(cache_len), _ptr(o), _ptr(ws),
+                                                            ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def moe_rmsnorm(x, g, eps, y, add=None, h_out=None, stream=None):
@@ -382,15 +410,21 @@ def moe_rmsnorm(x, g, eps, y, add=None, h_out=None, stream=None):
                                           _stream(stream)))
 
 
-def moe_linear(x, w, y, stream=None):
-    """y [rows][n_out] fp32 = x [rows][n_in] . w^T (bf16 operands)."""
+def moe_linear_workspace_bytes(rows: int, n_in: int, n_out: int) -> int:
+    return int(lib.moe_linear_workspace_bytes(int(rows), int(n_in), int(n_out)))
+
+
+def moe_linear(x, w, y, ws=None, stream=None):
+    """y [rows][n_out] fp32 = x [rows][n_in] . w^T (bf16 operands); ws: weight streaming for <= 64 rows."""
     rows, n_in = x.shape
-    _check("moe_linear", lib.moe_linear(rows, n_in, w.shape[0], _ptr(x), _ptr(w), _ptr(y), _stream(stream)))
+    nbytes = ws.numel() * ws.element_size() if ws is not None else 0
+    _check("moe_linear", lib.moe_linear(rows, n_in, w.shape[0], _ptr(x), _ptr(w), _ptr(y), _ptr(ws), nbytes,
+                                        _stream(stream)))
 
 
-def moe_rope_split(shape, qkv, q, k, v, stream=None):
-    _check("moe_rope_split", lib.moe_rope_split(ctypes.byref(shape), _ptr(qkv), _ptr(q), _ptr(k), _ptr(v),
-                                                _stream(stream)))
+def moe_rope_split(shape, qkv, q, k, v, pos=None, k_cache=None, v_cache=None, stream=None):
+    _check("moe_rope_split", lib.moe_rope_split(ctypes.byref(shape), _ptr(qkv), _ptr(pos), _ptr(q), _ptr(k), _ptr(v),
+                                                _ptr(k_cache), _ptr(v_cache), _stream(stream)))
 
 
 def moe_attention(shape, q, k, v, o, stream=None):
@@ -402,7 +436,7 @@ def moe_residual_add(a, b, out, stream=None):
     _check("moe_residual_add", lib.moe_residual_add(a.numel(), _ptr(a), _ptr(b), _ptr(out), _stream(stream)))
 
 
-def block_forward(x, p: dict, shape: moe_block_shape, ws=None, stream=None):
+def block_forward(x, p: dict, shape: moe_block_shape, ws=None, k_cache=None, v_cache=None, stream=None):
     """Allocates out (and the workspace) with torch and calls moe_block_forward."""
     if ws is None:
         n = moe_block_workspace_bytes(shape)
@@ -410,6 +444,25 @@ def block_forward(x, p: dict, shape: moe_block_shape, ws=None, stream=None):
             raise MoEError("moe_block_workspace_bytes", MOE_ERR_UNSUPPORTED)
         ws = _bytes(n, x.device)
     out = torch.empty_like(x)
-    moe_block_forward(shape, x, block_weights(p), out, ws, stream)
+    moe_block_forward(shape, x, block_weights(p), out, ws, k_cache, v_cache, stream)
+    return out
+
+
+def kv_cache(shape: moe_block_shape, device="cuda"):
+    """Empty key and value caches [B][n_kv_heads][cache_max][head_dim] bf16 for the shape."""
+    dims = (shape.B, shape.n_kv_heads, shape.cache_max, shape.head_dim)
+    return (torch.zeros(dims, dtype=torch.bfloat16, device=device),
+            torch.zeros(dims, dtype=torch.bfloat16, device=device))
+
+
+def block_decode(x, p: dict, shape: moe_block_shape, k_cache, v_cache, cache_len, ws=None, stream=None):
+    """One decode step (x [B][d]: each sequence's next token); appends to the caches, advances cache_len."""
+    if ws is None:
+        n = moe_block_decode_workspace_bytes(shape)
+        if n == 0:
+            raise MoEError("moe_block_decode_workspace_bytes", MOE_ERR_UNSUPPORTED)
+        ws = _bytes(n, x.device)
+    out = torch.empty_like(x)
+    moe_block_decode(shape, x, block_weights(p), k_cache, v_cache, cache_len, out, ws, stream)
     return out
 

@@ -120,14 +120,14 @@ def test_device_status_without_a_device_reports_cuda_error():
 def _block(**kw):
     base = dict(B=1, S=4096, d=4096, n_heads=32, n_kv_heads=8, ffn=14336)
     base.update(kw)
-    extra = {k: base.pop(k) for k in ("head_dim", "eps", "rope_base") if k in base}
+    extra = {k: base.pop(k) for k in ("head_dim", "eps", "rope_base", "cache_max") if k in base}
     return moe.make_block_shape(base["B"], base["S"], base["d"], base["n_heads"], base["n_kv_heads"], base["ffn"],
                                 **extra)
 
 
 def _block_forward(shape, ws_bytes=1 << 40, x=FAKE, out=ctypes.c_void_p(2 << 20)):
     w = moe.moe_block_weights(*([FAKE] * 8))
-    return moe.lib.moe_block_forward(ctypes.byref(shape), x, ctypes.byref(w), out, FAKE, ws_bytes, None)
+    return moe.lib.moe_block_forward(ctypes.byref(shape), x, ctypes.byref(w), None, None, out, FAKE, ws_bytes, None)
 
 
 def test_block_workspace_covers_its_buffers():
@@ -158,10 +158,42 @@ def test_block_step_validation_codes():
     assert lib.moe_rmsnorm(4, 12, FAKE, None, FAKE, 1e-5, None, FAKE, None) == moe.MOE_ERR_INVALID_ARG  # d % 8
     assert lib.moe_rmsnorm(4, 16, FAKE, FAKE, FAKE, 1e-5, None, FAKE, None) == moe.MOE_ERR_INVALID_ARG  # no h_out
     assert lib.moe_rmsnorm(0, 16, None, None, None, 1e-5, None, None, None) == moe.MOE_OK
-    assert lib.moe_linear(4, 96, 256, FAKE, FAKE, FAKE, None) == moe.MOE_ERR_UNSUPPORTED
-    assert lib.moe_linear(4, 64, 200, FAKE, FAKE, FAKE, None) == moe.MOE_ERR_UNSUPPORTED
-    assert lib.moe_linear(0, 64, 256, None, None, None, None) == moe.MOE_OK
+    assert lib.moe_linear(4, 96, 256, FAKE, FAKE, FAKE, None, 0, None) == moe.MOE_ERR_UNSUPPORTED
+    assert lib.moe_linear(4, 64, 200, FAKE, FAKE, FAKE, None, 0, None) == moe.MOE_ERR_UNSUPPORTED
+    assert lib.moe_linear(0, 64, 256, None, None, None, None, 0, None) == moe.MOE_OK
+    # weight streaming for up to 64 rows: K-slice partials of rows x n_out fp32
+    n = moe.moe_linear_workspace_bytes(16, 4096, 6144)
+    assert n > 0 and n % (16 * 6144 * 4) == 0
+    assert moe.moe_linear_workspace_bytes(65, 4096, 6144) == 0
     assert lib.moe_residual_add(12, FAKE, FAKE, FAKE, None) == moe.MOE_ERR_INVALID_ARG
     s = _block(head_dim=64)
     assert lib.moe_attention(ctypes.byref(s), FAKE, FAKE, FAKE, FAKE, None) == moe.MOE_ERR_UNSUPPORTED
-    assert lib.moe_rope_split(ctypes.byref(_block()), None, FAKE, FAKE, FAKE, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_rope_split(ctypes.byref(_block()), None, None, FAKE, FAKE, FAKE, None, None, None) == \
+        moe.MOE_ERR_INVALID_ARG
+    # positions (decode) need one token per sequence; a cache needs room for the prefill
+    assert lib.moe_rope_split(ctypes.byref(_block()), FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None) == \
+        moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_rope_split(ctypes.byref(_block(cache_max=100)), FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, None) \
+        == moe.MOE_ERR_INVALID_ARG
+
+
+def test_block_decode_validation_codes():
+    w = moe.moe_block_weights(*([FAKE] * 8))
+    dec = _block(S=1, B=16, cache_max=4096)
+    n = moe.moe_block_decode_workspace_bytes(dec)
+    assert n > 0
+
+    def call(s, cache_len=FAKE, ws_bytes=1 << 40):
+        return moe.lib.moe_block_decode(ctypes.byref(s), FAKE, ctypes.byref(w), FAKE, FAKE, cache_len,
+                                        ctypes.c_void_p(2 << 20), FAKE, ws_bytes, None)
+    assert call(_block(S=2, B=16, cache_max=4096)) == moe.MOE_ERR_INVALID_ARG    # one token per sequence
+    assert call(_block(S=1, B=16, cache_max=0)) == moe.MOE_ERR_INVALID_ARG       # no cache
+    assert call(dec, cache_len=None) == moe.MOE_ERR_INVALID_ARG
+    assert call(dec, ws_bytes=n - 1) == moe.MOE_ERR_WORKSPACE
+    # the decode attention covers 1, 2, 4 or 8 query heads per KV head
+    assert moe.moe_block_decode_workspace_bytes(_block(S=1, n_heads=32, n_kv_heads=2, cache_max=64)) == 0
+    assert moe.moe_block_decode_workspace_bytes(_block(S=1, n_heads=24, n_kv_heads=8, cache_max=64)) == 0
+    assert moe.moe_block_decode_workspace_bytes(_block(S=1, n_heads=16, n_kv_heads=2, cache_max=64)) > 0
+    # one partial (128 channels, maximum, sum) per query head and split; splits fill the SMs once
+    att = moe.moe_attention_decode_workspace_bytes(dec)
+    assert 16 * 32 * (128 + 2) * 4 <= att <= 16 * 32 * 64 * (128 + 2) * 4 + 4096

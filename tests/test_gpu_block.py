@@ -316,5 +316,5 @@ def test_block_rejects_bad_shapes_and_small_workspace():
     out = torch.empty_like(p["x"])
     ws = torch.empty(moe.moe_block_workspace_bytes(ok) - 1024, dtype=torch.uint8, device="cuda")
     with pytest.raises(moe.MoEError) as e:
-        moe.moe_block_forward(ok, p["x"], moe.block_weights(p), out, ws)
+        moe.moe_block_forward(ok, p["x"], moe.block_weights(p), out, ws)  # no caches
     assert e.value.code == moe.MOE_ERR_WORKSPACE

@@ -237,3 +237,38 @@ def test_block_rejects_bad_shapes(bad):
             oracle.attention_sublayer(x, p["g_attn"], p["wqkv"], p["wo"], 4, 4, 2)
         else:
             oracle.causal_gqa_attention(np.zeros((2, 3, 4)), np.zeros((2, 2, 4)), np.zeros((2, 2, 4)))
+
+
+# ----------------------------------------------------------- decode step ---
+
+def test_decode_step_equals_the_last_token_of_the_whole_sequence():
+    # the prefix's keys and values come from the whole-sequence sublayer; the
+    # decode step then recomputes the last token incrementally
+    for L in (1, 5, 9):
+        x, p = _small_block(20 + L, 2 * (L + 1))
+        full = oracle.decoder_block(x, p, L + 1, 4, 2)
+        kp = [full["k"][b * (L + 1):b * (L + 1) + L] for b in range(2)]
+        vp = [full["v"][b * (L + 1):b * (L + 1) + L] for b in range(2)]
+        step = oracle.decoder_block_decode(x[[L, 2 * L + 1]], kp, vp, p, 4, 2)
+        assert np.allclose(step["out"], full["out"][[L, 2 * L + 1]], rtol=1e-12, atol=1e-12)
+        assert np.allclose(step["k_new"], full["k"][[L, 2 * L + 1]], rtol=1e-12, atol=1e-12)
+
+
+def test_decode_step_of_a_first_token_attends_to_itself_only():
+    x, p = _small_block(30, 3)
+    step = oracle.decoder_block_decode(x, [np.zeros((0, 2, 4))] * 3, [np.zeros((0, 2, 4))] * 3, p, 4, 2)
+    # one key: the attention output is the token's own value, per KV head
+    for b in range(3):
+        v = step["v_new"][b]
+        assert np.allclose(step["attn"][b].reshape(4, 4), v[[0, 0, 1, 1]], rtol=1e-14)
+
+
+def test_one_query_attention_two_key_closed_form():
+    q = np.zeros((1, 4))
+    q[0, 0] = 0.9
+    k = np.zeros((2, 1, 4))
+    k[1, 0, 0] = 2.0
+    v = np.array([[[1.0, 0.0, 0.0, 0.0]], [[0.0, 1.0, 0.0, 0.0]]])
+    out = oracle.attention_one_query(q, k, v)
+    w1 = math.exp(0.9) / (1 + math.exp(0.9))
+    assert np.allclose(out[0], [1 - w1, w1, 0, 0], rtol=1e-14)
