@@ -695,38 +695,41 @@ __global__ void __launch_bounds__(kAttnPairThreads, 1)
 // contiguous run. CTA (split s, KV head, sequence) takes an equal share of the
 // n = len + 1 valid keys (the new token's were appended by the RoPE step), 64
 // keys per step, for the G query heads that share the KV head:
-//   S = Q K^T     tcgen05.mma M = 128 (rows 0 .. G-1 are the heads, the rest
-//                 zero), N = 64 keys, K = 128 channels; Q, K by TMA (128-byte
-//                 swizzle), S in tensor memory
+//   S = Q K^T     tcgen05.mma M = 128 (rows 0 .. G-1 are the heads; the other
+//                 rows are not read), N = 64 keys, K = 128 channels; Q held in
+//                 tensor memory (A operand), K by TMA (128-byte swizzle), S in
+//                 tensor memory
 //   softmax       warp 0, one row per lane: running maximum and sum, O
 //                 rescaled in place when the maximum grows, P (bf16) written
 //                 over S
 //   O += P V      tcgen05.mma M = 128, N = 128 channels, K = 64 keys, P from
 //                 tensor memory, V as stored (MN-major)
-// Keys and values stream through two shared-memory stages, so the tensor core
-// only waits on HBM. Each CTA writes one unnormalised partial (O, m, l) per
+// Keys and values stream through three shared-memory stages, so the tensor
+// core only waits on HBM. Each CTA writes one unnormalised partial (O, m, l) per
 // head; a second kernel merges the splits in order (flash decoding).
 // ---------------------------------------------------------------------------
 constexpr int kDecChunk = 64;                        // keys per step
 constexpr int kDecThreads = 96;                      // warp 0 softmax, warp 1 TMA, warp 2 MMA
 constexpr int kDecMaxGroup = 32;                     // query heads per KV head (one row per lane)
 constexpr int kDecCtasPerSm = 2;
+constexpr int kDecStages = 3;
 constexpr uint32_t kDecBox = 64 * 64 * 2;            // 8 KB: 64 keys x 64 channels
 constexpr uint32_t kDecStageBytes = 4 * kDecBox;     // keys (two boxes) + values (two boxes)
 
 struct DecControl {
-    uint64_t q_full;
-    uint64_t kv_full[2];
-    uint64_t kv_empty[2];
+    uint64_t q_ready;
+    uint64_t kv_full[kDecStages];
+    uint64_t kv_empty[kDecStages];
     uint64_t s_full, p_full, o_full, drain;
     uint32_t tmem_base;
     int abort_flag;
 };
 
-// Q (128 rows x 128 channels) | stage 0 | stage 1 | control
-constexpr size_t kDecSmemBytes = 1024 + (size_t)kAttnTileBytes + 2 * (size_t)kDecStageBytes + sizeof(DecControl);
+// stages | control
+constexpr size_t kDecSmemBytes = 1024 + (size_t)kDecStages * kDecStageBytes + sizeof(DecControl);
 
 struct DecodeArgs {
+    const __nv_bfloat16* q;       // [B][Hq hd]
     const int32_t* len;           // [B] keys cached before this token
     float* part_o;                // [B][Hq][splits][hd]
     float* part_ml;               // [B][Hq][splits][2]
@@ -741,31 +744,27 @@ __device__ __forceinline__ void dec_abort(DecControl* c, int where) {
     *reinterpret_cast<volatile int*>(&c->abort_flag) = 1;
 }
 
-// map_q: q viewed as [B Hq][128], boxes of 64 channels x G rows; map_k, map_v:
-// the caches viewed as [B Hkv cache_max][128], boxes of 64 channels x 64 keys.
+// map_k, map_v: the caches viewed as [B Hkv cache_max][128], boxes of 64
+// channels x 64 keys.
 __global__ void __launch_bounds__(kDecThreads, 1)
-    attention_decode_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
-                            const __grid_constant__ CUtensorMap map_v, const DecodeArgs a) {
+    attention_decode_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
+                            const DecodeArgs a) {
     extern __shared__ unsigned char dec_smem_raw[];
     unsigned char* smem = align1024(dec_smem_raw);
-    DecControl* ctl = reinterpret_cast<DecControl*>(smem + kAttnTileBytes + 2 * (size_t)kDecStageBytes);
+    DecControl* ctl = reinterpret_cast<DecControl*>(smem + (size_t)kDecStages * kDecStageBytes);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const uint64_t tmo = a.timeout_ns;
     volatile int* abort_flag = &ctl->abort_flag;
     const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     const int G = a.Hq / a.Hkv;
-    const uint32_t sQ = smem_u32(smem);
-    auto sK = [&](int st) { return sQ + kAttnTileBytes + (uint32_t)st * kDecStageBytes; };
+    const uint32_t sbase = smem_u32(smem);
+    auto sK = [&](int st) { return sbase + (uint32_t)st * kDecStageBytes; };
     auto sV = [&](int st) { return sK(st) + 2 * kDecBox; };
 
-    // rows G .. 127 of the query tile stay zero: clear the tile before TMA writes rows 0 .. G-1
-    for (uint32_t i = threadIdx.x; i < kAttnTileBytes / 16; i += kDecThreads)
-        reinterpret_cast<uint4*>(smem)[i] = make_uint4(0u, 0u, 0u, 0u);
-    fence_proxy_async_smem();
     if (threadIdx.x == 0) {
-        mbar_init(smem_u32(&ctl->q_full), 1);
-        for (int s = 0; s < 2; ++s) {
+        mbar_init(smem_u32(&ctl->q_ready), 1);
+        for (int s = 0; s < kDecStages; ++s) {
             mbar_init(smem_u32(&ctl->kv_full[s]), 1);
             mbar_init(smem_u32(&ctl->kv_empty[s]), 1);
         }
@@ -781,7 +780,6 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         tmem_relinquish();
     }
     if (warp == 1 && lane == 0) {
-        tma_prefetch_desc(&map_q);
         tma_prefetch_desc(&map_k);
         tma_prefetch_desc(&map_v);
     }
@@ -791,6 +789,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tS = ctl->tmem_base;         // columns 0-63: scores (P over columns 0-31)
+    const uint32_t tQ = ctl->tmem_base + 64;    // columns 64-127: the queries, two bf16 per column
     const uint32_t tO = ctl->tmem_base + 128;   // columns 128-255: output accumulator
 
     const int64_t n_all = (int64_t)a.len[b] + 1;
@@ -806,14 +805,10 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         // ------------------------------------------------------------ TMA
         if (lane == 0 && steps > 0) {
             const uint64_t pol = policy_evict_first();
-            const uint32_t qb = smem_u32(&ctl->q_full);
-            mbar_arrive_expect_tx(qb, 2u * (uint32_t)G * 128u);
-            tma_load_2d(sQ, &map_q, qb, 0, b * a.Hq + kvh * G, pol);
-            tma_load_2d(sQ + kAttnBox, &map_q, qb, 64, b * a.Hq + kvh * G, pol);
             uint32_t issued = 0, issued_ph = 0;
             for (int i = 0; i < steps; ++i) {
-                const int st = i & 1;
-                const uint32_t ph = (uint32_t)(i >> 1) & 1u;
+                const int st = i % kDecStages;
+                const uint32_t ph = (uint32_t)(i / kDecStages) & 1u;
                 if (!mbar_wait(smem_u32(&ctl->kv_empty[st]), ph ^ 1u, tmo, abort_flag)) {
                     dec_abort(ctl, W_PRODUCER);
                     break;
@@ -828,8 +823,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                 issued |= 1u << st;
                 issued_ph = (issued_ph & ~(1u << st)) | (ph << st);
             }
-            drain_wait(smem_u32(&ctl->q_full), 0, tmo, K_ATTN);
-            for (int st = 0; st < 2; ++st)
+            for (int st = 0; st < kDecStages; ++st)
                 if (issued & (1u << st)) drain_wait(smem_u32(&ctl->kv_full[st]), (issued_ph >> st) & 1u, tmo, K_ATTN);
         }
         __syncwarp();
@@ -838,12 +832,12 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         if (lane == 0 && steps > 0) {
             constexpr uint32_t idesc_s = idesc_bf16_f32(128, kDecChunk);
             constexpr uint32_t idesc_o = idesc_bf16_f32(128, 128, false, true);
-            bool ok = mbar_wait(smem_u32(&ctl->q_full), 0, tmo, abort_flag);
+            bool ok = mbar_wait(smem_u32(&ctl->q_ready), 0, tmo, abort_flag);
             if (!ok) dec_abort(ctl, W_MMA);
             bool any = false;
             for (int i = 0; ok && i < steps; ++i) {
-                const int st = i & 1;
-                if (!mbar_wait(smem_u32(&ctl->kv_full[st]), (uint32_t)(i >> 1) & 1u, tmo, abort_flag)) {
+                const int st = i % kDecStages;
+                if (!mbar_wait(smem_u32(&ctl->kv_full[st]), (uint32_t)(i / kDecStages) & 1u, tmo, abort_flag)) {
                     dec_abort(ctl, W_MMA);
                     break;
                 }
@@ -852,9 +846,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 #pragma unroll
                 for (int kk = 0; kk < kAttnHD / 16; ++kk) {
                     const uint32_t off = (uint32_t)(kk >> 2);
-                    const uint64_t ad = sw128_kmajor_desc(sQ + off * kAttnBox) + 2ull * (kk & 3);
                     const uint64_t bd = sw128_kmajor_desc(sK(st) + off * kDecBox) + 2ull * (kk & 3);
-                    mma_bf16(tS, ad, bd, idesc_s, kk > 0);
+                    mma_bf16_ts(tS, tQ + 8u * (uint32_t)kk, bd, idesc_s, kk > 0);
                 }
                 any = true;
                 mma_commit(smem_u32(&ctl->s_full));
@@ -884,6 +877,27 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         const float sl2 = a.scale_log2;
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
+        if (steps > 0) {
+            // the group's queries into tensor memory, one head per lane (rows G .. 31 zero)
+            const uint4* qr = reinterpret_cast<const uint4*>(a.q + ((int64_t)b * a.Hq + kvh * G + row) * kAttnHD);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t w[16];
+#pragma unroll
+                for (int v4 = 0; v4 < 4; ++v4) {
+                    const uint4 u = row < G ? qr[4 * c + v4] : make_uint4(0u, 0u, 0u, 0u);
+                    w[4 * v4] = u.x;
+                    w[4 * v4 + 1] = u.y;
+                    w[4 * v4 + 2] = u.z;
+                    w[4 * v4 + 3] = u.w;
+                }
+                tmem_st16(tQ + 16 * c, w);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&ctl->q_ready));
+        }
         for (int i = 0; i < steps; ++i) {
             if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->s_full), (uint32_t)i & 1u, tmo, abort_flag))) {
                 dec_abort(ctl, W_EPILOGUE);

@@ -1069,12 +1069,13 @@ moe_status run_attention_decode(const moe_block_shape& s, const void* q, const v
     const int splits = decode_splits(s);
     const size_t parts = (size_t)s.B * s.n_heads * splits;
     const int group = s.n_heads / s.n_kv_heads;
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mk, mv;
     const uint64_t cache_rows = (uint64_t)s.B * s.n_kv_heads * s.cache_max;
-    if (!make_map(&mq, q, kAttnHD, (uint64_t)s.B * s.n_heads, (uint32_t)group) ||
-        !make_map(&mk, kc, kAttnHD, cache_rows, kDecChunk) || !make_map(&mv, vc, kAttnHD, cache_rows, kDecChunk))
+    if (!make_map(&mk, kc, kAttnHD, cache_rows, kDecChunk) || !make_map(&mv, vc, kAttnHD, cache_rows, kDecChunk))
         return MOE_ERR_CUDA;
+    (void)group;
     DecodeArgs a{};
+    a.q = static_cast<const __nv_bfloat16*>(q);
     a.len = len;
     a.part_o = reinterpret_cast<float*>(ws);
     a.part_ml = reinterpret_cast<float*>(ws + align_up(parts * kAttnHD * 4, kAlign));
@@ -1087,7 +1088,7 @@ moe_status run_attention_decode(const moe_block_shape& s, const void* q, const v
     if (!ensure_smem(attention_decode_kernel, 15, kDecSmemBytes)) return MOE_ERR_CUDA;
     MOE_TRY(launch("attention_decode", st, [&] {
         return klaunch(attention_decode_kernel, dim3((unsigned)splits, (unsigned)s.n_kv_heads, (unsigned)s.B),
-                       dim3(kDecThreads), kDecSmemBytes, st, mq, mk, mv, a);
+                       dim3(kDecThreads), kDecSmemBytes, st, mk, mv, a);
     }));
     return launch("attention_decode_merge", st, [&] {
         return klaunch(attention_decode_merge_kernel, dim3((unsigned)s.n_heads, (unsigned)s.B), dim3(kAttnHD), 0, st,
