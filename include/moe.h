@@ -363,9 +363,10 @@ moe_status moe_attention(const moe_block_shape* s, const void* q, const void* k,
  * cache_len[b] + 1 keys; o [B][n_heads head_dim] bf16. Splits each
  * sequence's keys over a few CTAs per KV head (each streams its share in
  * steps of 64 keys through shared memory by TMA, S = Q K^T and O += P V on
- * the tensor cores, a running softmax) and merges the partials; advances cache_len[b] by one (up to
- * cache_max). ws: moe_attention_decode_workspace_bytes. head_dim 128,
- * n_heads / n_kv_heads <= 32. */
+ * the tensor cores, a running softmax) and merges the partials; advances
+ * cache_len[b] by one (up to cache_max). ws:
+ * moe_attention_decode_workspace_bytes. head_dim 128, n_heads / n_kv_heads
+ * <= 32. */
 size_t moe_attention_decode_workspace_bytes(const moe_block_shape* s);
 moe_status moe_attention_decode(const moe_block_shape* s, const void* q, const void* k_cache, const void* v_cache,
                                 int32_t* cache_len, void* o, void* ws, size_t ws_bytes, void* stream);
