@@ -419,8 +419,16 @@ moe_status moe_set_wait_timeout_ns(uint64_t ns);
  *                       CTAs; 2 = CTA pairs; 4 = two CTA pairs per cluster
  *                       sharing each token tile (loaded once, multicast). The
  *                       single-CTA kernel also runs when no CTA pair fits.
- * Returns MOE_ERR_INVALID_ARG for an unknown knob or value. */
-enum { MOE_KNOB_FFN_PATH = 1, MOE_KNOB_KSLICE = 2, MOE_KNOB_GRID = 3, MOE_KNOB_PDL = 4, MOE_KNOB_TILE_CTAS = 5 };
+ *   MOE_KNOB_DEBUG      1 = debug mode: every launch is followed by a wait on
+ *                       its stream and a look at the device status word, so a
+ *                       device-side error (timeout, index check) is returned by
+ *                       the call that launched the kernel and the kernel is
+ *                       named on stderr; 0 (default) = asynchronous
+ * Returns MOE_ERR_INVALID_ARG for an unknown knob or value.
+ * Environment, read when the library loads: MOE_DEBUG=1 starts in debug mode;
+ * MOE_WAIT_TIMEOUT_NS sets the initial wait limit (as moe_set_wait_timeout_ns). */
+enum { MOE_KNOB_FFN_PATH = 1, MOE_KNOB_KSLICE = 2, MOE_KNOB_GRID = 3, MOE_KNOB_PDL = 4, MOE_KNOB_TILE_CTAS = 5,
+       MOE_KNOB_DEBUG = 6 };
 moe_status moe_set_knob(int32_t knob, int64_t value);
 
 /* Per-kernel timing with CUDA events recorded on the launching stream.

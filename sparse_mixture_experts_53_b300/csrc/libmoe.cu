@@ -11,6 +11,7 @@
 #include <cmath>
 #include <utility>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <map>
 #include <string>
@@ -48,11 +49,26 @@ struct TimingRecord {
     cudaEvent_t start, stop;
 };
 
+// Initial wait limit: MOE_WAIT_TIMEOUT_NS from the environment (1 ns .. 10 s), else 2 s.
+uint64_t env_timeout_ns() {
+    const char* v = std::getenv("MOE_WAIT_TIMEOUT_NS");
+    if (v == nullptr) return 2000000000ull;
+    char* end = nullptr;
+    const unsigned long long t = std::strtoull(v, &end, 10);
+    return (end != v && *end == '\0' && t >= 1 && t <= 10000000000ull) ? (uint64_t)t : 2000000000ull;
+}
+
+bool env_flag(const char* name) {
+    const char* v = std::getenv(name);
+    return v != nullptr && v[0] != '\0' && std::strcmp(v, "0") != 0;
+}
+
 struct HostState {
     int ffn_path = 0;          // 0 auto, 1 token tiles, 2 weight streaming
     int64_t kslice = 0;        // 0 auto
     int grid = 0;              // 0 = one CTA per SM
-    uint64_t timeout_ns = 2000000000ull;
+    uint64_t timeout_ns = env_timeout_ns();
+    bool debug = env_flag("MOE_DEBUG");  // synchronise after every launch and report device errors at once
     bool timing = false;
     bool pdl = true;           // programmatic dependent launch between the library's kernels
     int tile_ctas = 0;         // token tiles: 0 auto, 1 single CTAs, 2 CTA pairs, 4 two pairs per cluster
@@ -171,7 +187,23 @@ moe_status launch(const char* name, cudaStream_t st, F&& f) {
         cudaEventRecord(b, st);
         g.records.push_back({name, a, b});
     }
-    return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    if (err != cudaSuccess) return MOE_ERR_CUDA;
+    if (g.debug) {
+        // debug mode: wait for this kernel and return a device-side error from the call that
+        // launched it, naming the kernel (the status word is left latched for the next read)
+        if (cudaStreamSynchronize(st) != cudaSuccess) {
+            std::fprintf(stderr, "moe debug: %s: %s\n", name, cudaGetErrorString(cudaGetLastError()));
+            return MOE_ERR_CUDA;
+        }
+        int h[4] = {0, 0, 0, 0};
+        if (cudaMemcpyFromSymbol(h, g_status, sizeof(h)) != cudaSuccess) return MOE_ERR_CUDA;
+        if (h[0] != 0) {
+            std::fprintf(stderr, "moe debug: %s: device status %d (kernel %d, where %d, block %d)\n", name, h[0],
+                         h[1], h[2], h[3]);
+            return static_cast<moe_status>(h[0]);
+        }
+    }
+    return MOE_OK;
 }
 
 #define MOE_TRY(expr)                         \
@@ -1549,8 +1581,10 @@ moe_status moe_layer_backward(const moe_shape* s, const void* x, const void* w_g
 moe_status moe_selftest_wait_timeout(uint64_t timeout_ns, int32_t* gave_up, void* stream) {
     if (timeout_ns == 0 || timeout_ns > 10000000000ull || !ok_ptr(gave_up)) return MOE_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    wait_selftest_kernel<<<1, 32, 0, st>>>(timeout_ns, gave_up);
-    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    return launch("wait_selftest", st, [&] {
+        wait_selftest_kernel<<<1, 32, 0, st>>>(timeout_ns, gave_up);
+        return cudaGetLastError();
+    });
 }
 
 moe_status moe_get_device_status(int32_t* code, int32_t* detail) {
@@ -1599,6 +1633,10 @@ moe_status moe_set_knob(int32_t knob, int64_t value) {
         case MOE_KNOB_TILE_CTAS:
             if (value < 0 || value > 4 || value == 3) return MOE_ERR_INVALID_ARG;
             g.tile_ctas = (int)value;
+            return MOE_OK;
+        case MOE_KNOB_DEBUG:
+            if (value < 0 || value > 1) return MOE_ERR_INVALID_ARG;
+            g.debug = value != 0;
             return MOE_OK;
     }
     return MOE_ERR_INVALID_ARG;

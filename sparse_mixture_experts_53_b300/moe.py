@@ -32,6 +32,7 @@ MOE_KNOB_KSLICE = 2
 MOE_KNOB_GRID = 3
 MOE_KNOB_PDL = 4
 MOE_KNOB_TILE_CTAS = 5
+MOE_KNOB_DEBUG = 6
 
 EXPORTED = (
     "moe_version", "moe_status_string", "moe_workspace_bytes", "moe_ffn_workspace_bytes",

@@ -197,3 +197,20 @@ def test_block_decode_validation_codes():
     # one partial (128 channels, maximum, sum) per query head and split; splits fill the SMs once
     att = moe.moe_attention_decode_workspace_bytes(dec)
     assert 16 * 32 * (128 + 2) * 4 <= att <= 16 * 32 * 64 * (128 + 2) * 4 + 4096
+
+
+def test_debug_knob_and_environment():
+    assert moe.lib.moe_set_knob(moe.MOE_KNOB_DEBUG, 2) == moe.MOE_ERR_INVALID_ARG
+    assert moe.lib.moe_set_knob(moe.MOE_KNOB_DEBUG, 1) == moe.MOE_OK
+    assert moe.lib.moe_set_knob(moe.MOE_KNOB_DEBUG, 0) == moe.MOE_OK
+    # the library loads with the debug flag and with a wait limit (valid or not) in the environment
+    import os
+    import subprocess
+    import sys
+    code = ("import sys; sys.path.insert(0, '.'); from sparse_mixture_experts_53_b300 import moe; "
+            "print(moe.version())")
+    for env in ({"MOE_DEBUG": "1", "MOE_WAIT_TIMEOUT_NS": "5000000"}, {"MOE_WAIT_TIMEOUT_NS": "not a number"}):
+        r = subprocess.run([sys.executable, "-c", code], env=dict(os.environ, **env), capture_output=True, text=True,
+                           cwd=str(HEADER.parent.parent), timeout=300)
+        assert r.returncode == 0 and "sm_103a" in r.stdout, r.stderr
+

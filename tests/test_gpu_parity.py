@@ -472,3 +472,28 @@ def test_device_wait_timeout_is_reported_and_the_device_stays_usable():
     got = run_staged(L)
     assert_status_ok()
     check_y(L, got["y"])
+
+
+def test_debug_mode_returns_device_errors_from_the_launching_call():
+    """With the debug knob on, a device-side error comes back from the call that launched the kernel."""
+    moe.moe_set_knob(moe.MOE_KNOB_DEBUG, 1)
+    try:
+        flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+        with pytest.raises(moe.MoEError) as e:
+            moe.moe_selftest_wait_timeout(5_000_000, flag)
+        assert e.value.code == moe.MOE_ERR_TIMEOUT
+        assert moe.moe_check_device_status() == moe.MOE_ERR_TIMEOUT  # still latched until read
+        src = torch.randn((8, 64), device="cuda").to(torch.bfloat16)
+        bad = torch.tensor([0, 9], dtype=torch.int32, device="cuda")
+        out = torch.empty((2, 64), dtype=torch.bfloat16, device="cuda")
+        with pytest.raises(moe.MoEError) as e:
+            moe.moe_gather_rows(src, bad, out)
+        assert e.value.code == moe.MOE_ERR_DEVICE_CHECK
+        assert moe.moe_check_device_status() == moe.MOE_ERR_DEVICE_CHECK
+        # a clean call passes in debug mode too
+        good = torch.tensor([3, 7], dtype=torch.int32, device="cuda")
+        moe.moe_gather_rows(src, good, out)
+        assert torch.equal(out, src[good.long()])
+    finally:
+        moe.moe_set_knob(moe.MOE_KNOB_DEBUG, 0)
+    assert_status_ok()
