@@ -18,7 +18,7 @@ Sources:
   attention parameters per layer, which fixes the head width at d / 32 = 128
   and the K and V projections at 8 * 128 rows each.
 
-Readings where the pages are silent (each is listed in the design doc):
+Readings where the pages are silent:
 
 * RMSNorm(x) = g * x / sqrt(mean(x^2) + eps) with a learned gain g per
   channel, no bias, eps = 1e-5 (the RMSNorm paper's form);

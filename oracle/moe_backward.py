@@ -14,7 +14,7 @@ pass, so this module is the chain rule applied to the forward definition in
     L = sum_t <dy_t, y_t> + aux_coef * L_aux,
 
 i.e. the gradients a caller receives for an upstream gradient dy. Readings
-(listed in DESIGN.md):
+where the pages are silent:
 
 * the top-k selection is piecewise constant: scores outside a token's top k
   get no gradient through the mixture, and the selection itself is not

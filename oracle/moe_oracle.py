@@ -28,7 +28,7 @@ Sources (web pages about "Mixtral of Experts", arXiv 2401.04088):
   each expert is a SwiGLU block; its layer diagram prints 176M parameters per
   expert and 41.9M attention parameters per layer.
 
-Readings where the pages are silent (each is listed in the design doc):
+Readings where the pages are silent:
 
 * ties in the top-k go to the lower expert index, and the k selected slots are
   ordered by score, highest first;
