@@ -8,10 +8,11 @@ and ``sin`` are the library primitives.
 
 Sources:
 
-* "Mixtral" lineage page (tokentrails.org), step "GPT-2 vs Mixtral": the block
-  is LLaMA's (RMSNorm, RoPE, grouped-query attention) with the MLP replaced by
-  the MoE layer; its Code: h = x + attention(rms_norm(x)), then
-  out = h + moe(rms_norm(h)).
+* "Mixtral" lineage page (tokentrails.org), step "GPT-2 vs Mixtral": Mixtral
+  keeps LLaMA's normalisation, rotary positions and grouped-query attention
+  and swaps only the MLP for the MoE layer; its Code gives the two residual
+  branches, attention on the normalised input and then the MoE layer on the
+  normalised result.
 * "Mixtral of Experts" notes (royalroad.pages.dev), Proposed Method /
   Architecture: d = 4096, 32 attention heads, 8 KV heads, context 32768.
 * "Mixtral of Experts" breakdown (fdeinterviews.com), layer diagram: 41.9M
