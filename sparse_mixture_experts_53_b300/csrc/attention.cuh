@@ -1,7 +1,7 @@
 // Causal grouped-query attention on the 5th-generation tensor cores.
 //
-// The block's attention is LLaMA's ("Mixtral" lineage page, step "GPT-2 vs
-// Mixtral": RMSNorm, RoPE, grouped-query attention); the Mixtral notes
+// Mixtral keeps LLaMA's attention: rotary positions and grouped-query heads
+// ("Mixtral" lineage page, step "GPT-2 vs Mixtral"); the Mixtral notes
 // (royalroad.pages.dev, Architecture) give 32 query heads and 8 KV heads, and
 // the breakdown's 41.9M attention parameters per layer make a head 128 wide.
 //

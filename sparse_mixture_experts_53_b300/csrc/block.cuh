@@ -1,8 +1,9 @@
 // Memory-bound steps of the decoder block around the MoE layer: RMSNorm (with
 // the residual add in front of it), RoPE on the fused Q/K/V projection, and
-// the final residual add. The block is LLaMA's with the MLP replaced by the
-// MoE layer ("Mixtral" lineage page, step "GPT-2 vs Mixtral" and its Code:
-// h = x + attention(rms_norm(x)), out = h + moe(rms_norm(h))).
+// the final residual add. Mixtral keeps LLaMA's block and swaps only the MLP
+// for the MoE layer; the two residual branches are attention on the
+// normalised input, then the MoE layer on the normalised sum ("Mixtral"
+// lineage page, step "GPT-2 vs Mixtral" and its Code).
 #pragma once
 
 #include "common.cuh"
