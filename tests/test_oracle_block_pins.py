@@ -272,3 +272,66 @@ def test_one_query_attention_two_key_closed_form():
     out = oracle.attention_one_query(q, k, v)
     w1 = math.exp(0.9) / (1 + math.exp(0.9))
     assert np.allclose(out[0], [1 - w1, w1, 0, 0], rtol=1e-14)
+
+
+# ------------------------------------------- the pins catch planted bugs ---
+
+import importlib  # noqa: E402
+
+_db = importlib.import_module("oracle.decoder_block")  # the module (the package exports a function of that name)
+
+
+def _plant(monkeypatch, name, fn):
+    monkeypatch.setattr(_db, name, fn)
+    monkeypatch.setattr(oracle, name, fn)
+
+
+def test_pins_catch_kv_head_map_by_remainder(monkeypatch):
+    orig = _db.causal_gqa_attention
+
+    def bad(q, k, v):  # query head h reads KV head h % Hkv instead of h // (Hq / Hkv)
+        g = q.shape[1] // k.shape[1]
+        return orig(q, np.tile(k, (1, g, 1)), np.tile(v, (1, g, 1)))
+    _plant(monkeypatch, "causal_gqa_attention", bad)
+    with pytest.raises(AssertionError):
+        test_attention_first_query_returns_the_first_value_of_its_kv_head()
+
+
+def test_pins_catch_scale_one_over_head_dim(monkeypatch):
+    orig = _db.causal_gqa_attention
+    _plant(monkeypatch, "causal_gqa_attention", lambda q, k, v: orig(q / math.sqrt(q.shape[-1]), k, v))
+    with pytest.raises(AssertionError):
+        test_attention_two_keys_closed_form_fixes_the_scale()
+
+
+def test_pins_catch_rotation_the_other_way(monkeypatch):
+    orig = _db.rope
+    _plant(monkeypatch, "rope", lambda x, pos, base=10000.0: orig(x, -np.asarray(pos, np.float64), base))
+    with pytest.raises(AssertionError):
+        test_rope_turns_the_first_pair_by_the_position()
+    # turning q and k both the other way keeps every score (cos is even): only the direct pin sees it
+    test_rope_rotates_queries_and_keys_but_not_values()
+
+
+def test_pins_catch_rmsnorm_without_eps(monkeypatch):
+    orig = _db.rms_norm
+    _plant(monkeypatch, "rms_norm", lambda x, g, eps=1e-5: orig(x, g, 0.0))
+    with pytest.raises(AssertionError):
+        test_rms_norm_of_a_constant_vector()
+
+
+def test_pins_catch_unrotated_keys_in_the_decode_step(monkeypatch):
+    # a decode step that forgets to turn the new key: the last token no longer matches the whole sequence
+    orig = _db.rope
+    calls = {"n": 0}
+
+    def bad(x, pos, base=10000.0):
+        calls["n"] += 1
+        return orig(x, pos, base) if calls["n"] % 2 == 1 else np.asarray(x, np.float64)  # q turned, k not
+    x, p = _small_block(40, 8)
+    full = oracle.decoder_block(x, p, 4, 4, 2)
+    kp = [full["k"][b * 4:b * 4 + 3] for b in range(2)]
+    vp = [full["v"][b * 4:b * 4 + 3] for b in range(2)]
+    monkeypatch.setattr(_db, "rope", bad)
+    step = oracle.decoder_block_decode(x[[3, 7]], kp, vp, p, 4, 2)
+    assert not np.allclose(step["out"], full["out"][[3, 7]], rtol=1e-12, atol=1e-12)
