@@ -4,10 +4,17 @@ python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl ours|re
 
 One step = one moe_layer_forward over one batch of synthetic tokens: router,
 grouping, both expert GEMMs and the combine (plus the load-balancing statistics
-for the T=16384 workload). Default workload: the decode batch (T=16, d=4096,
-ffn=14336, 8 experts, top-2, bf16), which is bound by reading the touched
-experts' weights from HBM. ``--config`` selects another of the five named
-workloads.
+f, P and L_aux for the T=16384 workload). Default workload: the large batch
+(T=16384, d=4096, ffn=14336, 8 experts, top-2, bf16, with the statistics), the
+largest single-GPU workload, bound by the dense bf16 tensor-core rate. The line
+also carries, under "decode", the decode batch (T=16) through the same layer
+weights, measured in the same process: it is bound by reading the touched
+experts' weights from HBM. ``--config`` selects another of the named workloads.
+
+Outside the timed regions the fp64 oracle runs on a bounded sample of the
+workload's tokens: its rate is the line's "cpu_baseline", and its results check
+the GPU's output of the timed steps ("parity": routing on every token, y on the
+sampled tokens, the statistics).
 
 Prints one JSON line (rank 0). For N > 1 every rank runs its own replica of
 the workload on its own GPU (the layer has no exchange step in this data-parallel
@@ -30,7 +37,7 @@ sys.path.insert(0, str(ROOT))
 
 METRIC = "MoE-layer tokens/s at Mixtral shape (bf16); % of BF16 TC peak / HBM BW"
 UNIT = "tokens/s"
-DEFAULT_CONFIG = 1
+DEFAULT_CONFIG = 3
 PROFILES = ROOT / "profiles"
 
 
@@ -228,46 +235,60 @@ def _algorithmic(cfg: dict, counts) -> dict:
                 act_bytes=T * d * 2 * 2)
 
 
-def run_ours(args, rank, world, local) -> dict | None:
+def _device_status_ok(moe, when: str) -> None:
+    code, detail = moe.moe_get_device_status()
+    if code != moe.MOE_OK:
+        raise RuntimeError(f"device status {when}: {moe.status_string(code)} ({detail})")
+
+
+def read_peak_gbs(moe, stream, nbytes: int = 4 << 30, reps: int = 10) -> float:
+    """HBM read rate of this GPU: the library's read probe over a buffer 32x the L2, best of `reps` (CUDA
+    events). The weight-streaming kernels only read, so this, not a copy, is their ceiling."""
     import torch
+    buf = torch.ones(nbytes, dtype=torch.uint8, device="cuda")
+    sink = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for _ in range(2):
+        moe.moe_read_probe(buf, sink, stream)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    best = float("inf")
+    for _ in range(reps):
+        a.record(stream)
+        moe.moe_read_probe(buf, sink, stream)
+        b.record(stream)
+        b.synchronize()
+        best = min(best, a.elapsed_time(b))
+    del buf
+    return round(nbytes / (best * 1e-3) / 1e9, 1)
 
-    from moe_inputs import CONFIGS, make_config
-    from sparse_mixture_experts_53_b300 import moe
 
-    torch.cuda.set_device(local)
-    moe.moe_set_knob(moe.MOE_KNOB_PDL, args.pdl)
-    moe.moe_set_knob(moe.MOE_KNOB_TILE_CTAS, args.tile_ctas)
-    ranks = Ranks(rank, world, local, backend="nccl")
+def measure_layer(moe, L, cfg: dict, args, ranks, stream, x_dev=None, weights=None, e2e: bool = True) -> dict:
+    """One workload through moe_layer_forward: the timed steps (device-resident inputs, clocks sampled), a
+    second pass with serialised launches and CUDA events around every kernel, the end-to-end steps through
+    the same call with host buffers, and the routing counts of the batch."""
+    import torch
 
     def barrier():
         ranks.barrier()
         torch.cuda.synchronize()
 
-    k = args.config
-    cfg = CONFIGS[k]
-    t0 = time.time()
-    L = make_config(k)
-    gen_s = time.time() - t0
     aux = bool(cfg["aux"])
-    x = L.x.cuda()
-    wg, w1, w3, w2 = L.w_gate.cuda(), L.w1.cuda(), L.w3.cuda(), L.w2.cuda()
+    x = L.x.cuda() if x_dev is None else x_dev
+    wg = L.w_gate.cuda()
+    w1, w3, w2 = weights if weights is not None else (L.w1.cuda(), L.w3.cuda(), L.w2.cuda())
     shape = moe.shape_of(x, w1)
     ws = moe.workspace(shape)
     y = torch.empty_like(x)
     stats = (torch.empty(8, device="cuda"), torch.empty(8, device="cuda"), torch.empty(1, device="cuda")) if aux \
         else None
-    stream = torch.cuda.current_stream()
 
     def step():
         moe.moe_layer_forward(shape, x, wg, w1, w3, w2, y, ws, stats, stream)
 
     for _ in range(args.warmup):
         step()
-    code, detail = moe.moe_get_device_status()
-    if code != moe.MOE_OK:
-        raise RuntimeError(f"device status after warm-up: {moe.status_string(code)} ({detail})")
+    _device_status_ok(moe, "after warm-up")
 
-    # ---- timed region: device-resident inputs
+    # ---- timed region: device-resident inputs, programmatic dependent launch as configured
     sampler = ClockSampler(torch.cuda.current_device())
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
@@ -278,95 +299,145 @@ def run_ours(args, rank, world, local) -> dict | None:
         stop.record(stream)
         barrier()
     ms = start.elapsed_time(stop) / args.steps
-    code, detail = moe.moe_get_device_status()
-    if code != moe.MOE_OK:
-        raise RuntimeError(f"device status after timing: {moe.status_string(code)} ({detail})")
+    _device_status_ok(moe, "after timing")
+    y_out = y.clone()
+    stats_out = tuple(t.clone() for t in stats) if aux else None
 
-    # ---- per-kernel times (CUDA events on the launching stream), same steps
+    # ---- per-kernel times: the same steps with serialised launches (an early-launched kernel's events
+    # would include its wait for the predecessor), CUDA events around every launch on the launching stream
+    moe.moe_set_knob(moe.MOE_KNOB_PDL, 0)
     moe.moe_timing_enable(True)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
     for _ in range(args.steps):
         step()
+    b.record(stream)
     torch.cuda.synchronize()
+    serial_ms = a.elapsed_time(b) / args.steps
     kern = moe.moe_timing_read()
     moe.moe_timing_enable(False)
+    moe.moe_set_knob(moe.MOE_KNOB_PDL, args.pdl)
 
-    # ---- end to end through the public call with host buffers: every step copies its tokens in from
-    # pinned host memory and reads its output back. Input and output copies run on their own streams
-    # (both directions of the link at once) with two device buffers each way, so step i+1's input copy
-    # and step i's output copy overlap neighbouring steps' kernels, as a serving loop would run them.
-    x_host = L.x.pin_memory()
-    y_host = [torch.empty_like(L.x).pin_memory() for _ in range(2)]
-    xb = [torch.empty_like(x) for _ in range(2)]
-    yb = [torch.empty_like(x) for _ in range(2)]
-    cin, cout = torch.cuda.Stream(), torch.cuda.Stream()
-    h2d = [torch.cuda.Event() for _ in range(2)]
-    comp = [torch.cuda.Event() for _ in range(2)]
-    d2h = [torch.cuda.Event() for _ in range(2)]
+    out = dict(ms=ms, serial_ms=serial_ms, kern=kern, clocks=sampler.summary(), y=y_out, stats=stats_out,
+               shape=shape, x=x, wg=wg)
 
-    def e2e_steps(n):
-        for i in range(n):
-            b = i & 1
-            with torch.cuda.stream(cin):
+    if e2e:
+        # ---- end to end through the public call with host buffers: every step copies its tokens in from
+        # pinned host memory and reads its output back. Input and output copies run on their own streams
+        # (both directions of the link at once) with two device buffers each way, so step i+1's input copy
+        # and step i's output copy overlap neighbouring steps' kernels, as a serving loop would run them.
+        x_host = L.x.pin_memory()
+        y_host = [torch.empty_like(L.x).pin_memory() for _ in range(2)]
+        xb = [torch.empty_like(x) for _ in range(2)]
+        yb = [torch.empty_like(x) for _ in range(2)]
+        cin, cout = torch.cuda.Stream(), torch.cuda.Stream()
+        h2d = [torch.cuda.Event() for _ in range(2)]
+        comp = [torch.cuda.Event() for _ in range(2)]
+        d2h = [torch.cuda.Event() for _ in range(2)]
+
+        def e2e_steps(n):
+            for i in range(n):
+                bb = i & 1
+                with torch.cuda.stream(cin):
+                    if i >= 2:
+                        cin.wait_event(comp[bb])  # xb[bb] is free once step i-2 has run
+                    xb[bb].copy_(x_host, non_blocking=True)
+                    h2d[bb].record(cin)
+                stream.wait_event(h2d[bb])
                 if i >= 2:
-                    cin.wait_event(comp[b])  # xb[b] is free once step i-2 has run
-                xb[b].copy_(x_host, non_blocking=True)
-                h2d[b].record(cin)
-            stream.wait_event(h2d[b])
-            if i >= 2:
-                stream.wait_event(d2h[b])  # yb[b] has been read back
-            moe.moe_layer_forward(shape, xb[b], wg, w1, w3, w2, yb[b], ws, stats, stream)
-            comp[b].record(stream)
-            with torch.cuda.stream(cout):
-                cout.wait_event(comp[b])
-                y_host[b].copy_(yb[b], non_blocking=True)
-                d2h[b].record(cout)
-        stream.wait_stream(cout)
+                    stream.wait_event(d2h[bb])  # yb[bb] has been read back
+                moe.moe_layer_forward(shape, xb[bb], wg, w1, w3, w2, yb[bb], ws, stats, stream)
+                comp[bb].record(stream)
+                with torch.cuda.stream(cout):
+                    cout.wait_event(comp[bb])
+                    y_host[bb].copy_(yb[bb], non_blocking=True)
+                    d2h[bb].record(cout)
+            stream.wait_stream(cout)
 
-    e2e_steps(3)
-    barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    cin.wait_stream(stream)
-    cout.wait_stream(stream)
-    e2e_steps(args.steps)
-    e1.record(stream)
-    barrier()
-    e2e_ms = e0.elapsed_time(e1) / args.steps
+        e2e_steps(3)
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        cin.wait_stream(stream)
+        cout.wait_stream(stream)
+        e2e_steps(args.steps)
+        e1.record(stream)
+        barrier()
+        out["e2e_ms"] = e0.elapsed_time(e1) / args.steps
+        out["io_bytes"] = int(L.x.numel() * L.x.element_size())
+        out["y_host_equal"] = bool(torch.equal(y_host[(args.steps - 1) & 1], y_out.cpu()))
 
-    # per-expert counts of this batch (read once, outside every timed region)
+    # routing of this batch (read once, outside every timed region)
     idx = torch.empty((L.T, 2), dtype=torch.int32, device="cuda")
     gw = torch.empty((L.T, 2), dtype=torch.float32, device="cuda")
     moe.moe_route_top2(shape, x, wg, idx, gw)
-    counts = torch.bincount(idx.flatten().long(), minlength=8).cpu().tolist()
+    out["idx"] = idx.cpu()
+    out["counts"] = torch.bincount(idx.flatten().long(), minlength=8).cpu().tolist()
+    _device_status_ok(moe, "after the end-to-end steps")
+    return out
 
-    ms, e2e_ms = ranks.max([ms, e2e_ms])
 
-    work = _algorithmic(cfg, counts)
+def _kernel_ms(kern: dict, name: str) -> float:
+    per = kern.get(name, [1, float("nan")])
+    return per[1] / max(1, per[0])
+
+
+def roofline_tile_up(kern: dict, work: dict, peaks: dict) -> dict:
+    """Dominant kernel of a token-tile step: the up projection (2/3 of the FLOPs), against the dense bf16
+    peak (burst; the sustained figure beside it)."""
+    dom_ms = _kernel_ms(kern, "tile_up_swiglu")
+    achieved = work["up_flops"] / (dom_ms * 1e-3) / 1e12
+    return {"kernel": "tile_up_swiglu", "bound": "tensor", "achieved": round(achieved, 1),
+            "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
+            "peak_source": peaks["source"] + " (burst)",
+            "frac_of_sustained": round(achieved / peaks["bf16_tflops_sustained"], 4),
+            "algorithmic_flops_per_launch": work["up_flops"], "launch_ms": round(dom_ms, 5)}
+
+
+def roofline_stream_up(kern: dict, work: dict, peaks: dict, read_gbs: float | None) -> dict:
+    """Dominant kernel of a decode step: the up projection's weight streaming, against HBM."""
+    dom_ms = _kernel_ms(kern, "stream_up")
+    achieved = work["up_bytes"] / (dom_ms * 1e-3) / 1e9
+    r = {"kernel": "stream_up", "bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+         "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_source": peaks["source"] + " (copy)",
+         "algorithmic_bytes_per_launch": work["up_bytes"], "launch_ms": round(dom_ms, 5)}
+    if read_gbs:
+        r.update(read_peak=read_gbs, frac_of_read_peak=round(achieved / read_gbs, 4),
+                 read_peak_source="moe_read_probe over 4 GiB, best of 10")
+    return r
+
+
+def run_ours(args, rank, world, local) -> dict | None:
+    import torch
+
+    from moe_inputs import CONFIGS, make_config
+    from sparse_mixture_experts_53_b300 import moe
+
+    torch.cuda.set_device(local)
+    moe.moe_set_knob(moe.MOE_KNOB_PDL, args.pdl)
+    moe.moe_set_knob(moe.MOE_KNOB_TILE_CTAS, args.tile_ctas)
+    ranks = Ranks(rank, world, local, backend="nccl")
+    stream = torch.cuda.current_stream()
+
+    k = args.config
+    cfg = CONFIGS[k]
+    t0 = time.time()
+    L = make_config(k)
+    gen_s = time.time() - t0
+    weights = (L.w1.cuda(), L.w3.cuda(), L.w2.cuda())
+    m = measure_layer(moe, L, cfg, args, ranks, stream, weights=weights)
+    ms, e2e_ms = ranks.max([m["ms"], m["e2e_ms"]])
+
     peaks = _peaks()
-    launches_per_step = sum(v[0] for v in kern.values()) / max(1, args.steps)
+    read_gbs = read_peak_gbs(moe, stream) if rank == 0 else None
+    work = _algorithmic(cfg, m["counts"])
+    kern = m["kern"]
     streaming = cfg["T"] <= 64
-    if streaming:
-        dom = "stream_up"
-        per = kern.get(dom, [1, float("nan")])
-        dom_ms = per[1] / max(1, per[0])
-        achieved = work["up_bytes"] / (dom_ms * 1e-3) / 1e9
-        peak = peaks["hbm_gbs"]
-        roof = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "peak_source": peaks["source"],
-                "algorithmic_bytes_per_launch": work["up_bytes"], "launch_ms": round(dom_ms, 5),
-                "traffic": _profile_traffic(dom, cfg["name"])}
-    else:
-        dom = "tile_up_swiglu"
-        per = kern.get(dom, [1, float("nan")])
-        dom_ms = per[1] / max(1, per[0])
-        achieved = work["up_flops"] / (dom_ms * 1e-3) / 1e12
-        peak = peaks["bf16_tflops"]
-        roof = {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
-                "frac": round(achieved / peak, 4), "peak_source": peaks["source"] + " (burst)",
-                "frac_of_sustained": round(achieved / peaks["bf16_tflops_sustained"], 4),
-                "algorithmic_flops_per_launch": work["up_flops"], "launch_ms": round(dom_ms, 5),
-                "traffic": _profile_traffic(dom, cfg["name"])}
+    roof = roofline_stream_up(kern, work, peaks, read_gbs) if streaming else roofline_tile_up(kern, work, peaks)
+    roof["traffic"] = _profile_traffic(roof["kernel"], cfg["name"])
+    roof["timing"] = "CUDA events around each launch on its stream, launches serialised, over the timed steps"
     step_s = ms * 1e-3
+    aux = bool(cfg["aux"])
     line = {
         "metric": METRIC, "value": throughput(cfg["T"], world, ms), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
@@ -374,27 +445,60 @@ def run_ours(args, rank, world, local) -> dict | None:
         "config": {"workload": cfg["name"], "T": cfg["T"], "d": cfg["d"], "ffn": cfg["ffn"], "E": cfg["E"], "k": 2,
                    "aux_stats": aux, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "ffn_path": "weight-streaming (swap-AB)" if streaming else
-                   ("token tiles 256x256, two CTA pairs per cluster sharing the token tile" if args.tile_ctas == 4
-                    else "token tiles 256x256 on CTA pairs" if args.tile_ctas == 2 or (args.tile_ctas == 0 and cfg["T"] > 384)
+                   ("token tiles 256x256 on CTA pairs" if args.tile_ctas == 2 or (args.tile_ctas == 0 and cfg["T"] > 384)
                     else "token tiles 128x256"),
                    "pdl": bool(args.pdl),
                    "l2": "inputs larger than L2: each step reads %.2f GB of expert weights" % (work["weight_bytes"] / 1e9),
                    "experts_touched": work["touched"], "input_gen_s": round(gen_s, 1)},
         "step": {"tflops": round(work["flops"] / step_s / 1e12, 2),
+                 "frac_bf16_burst": round(work["flops"] / step_s / 1e12 / peaks["bf16_tflops"], 4),
+                 "frac_bf16_sustained": round(work["flops"] / step_s / 1e12 / peaks["bf16_tflops_sustained"], 4),
                  "weight_gbs": round(work["weight_bytes"] / step_s / 1e9, 1),
-                 "frac_hbm": round(work["weight_bytes"] / step_s / 1e9 / peaks["hbm_gbs"], 4),
-                 "frac_bf16_sustained": round(work["flops"] / step_s / 1e12 / peaks["bf16_tflops_sustained"], 4)},
+                 "frac_hbm": round(work["weight_bytes"] / step_s / 1e9 / peaks["hbm_gbs"], 4)},
         "roofline": roof,
         "kernels_ms_per_step": {n: round(v[1] / max(1, args.steps), 5) for n, v in kern.items()},
-        "gpu_launches": int(round(launches_per_step * args.steps)),
+        "kernels_timing": {"ms_per_step_serialised": round(m["serial_ms"], 5),
+                           "how": "second pass over the same steps with programmatic dependent launch off and "
+                                  "CUDA events around every launch; the kernels' sum is within that pass's step"},
+        "gpu_launches": int(sum(v[0] for v in kern.values())),
         "e2e": {"value": throughput(cfg["T"], world, e2e_ms), "unit": UNIT,
-                "h2d_bytes_per_step": int(L.x.numel() * L.x.element_size()),
-                "d2h_bytes_per_step": int(L.x.numel() * L.x.element_size()), "ms_per_step": round(e2e_ms, 5),
+                "h2d_bytes_per_step": m["io_bytes"], "d2h_bytes_per_step": m["io_bytes"],
+                "ms_per_step": round(e2e_ms, 5), "output_read_back_equals_device_output": m["y_host_equal"],
                 "copies": "pinned host buffers; input and output copies on two streams overlap neighbouring steps"},
-        "clocks": sampler.summary(),
+        "clocks": m["clocks"],
     }
+    gpu_out = {"cfg": k, "y": m["y"].cpu(), "idx": m["idx"], "stats": [t.cpu() for t in m["stats"]] if aux else None}
+    del m
+
+    if not args.no_decode and k != 1:
+        # the decode batch through the same layer (configs 1-4 share one weight draw), same process
+        c1 = CONFIGS[1]
+        L1 = make_config(1, weights=(L.w1, L.w3, L.w2))
+        d = measure_layer(moe, L1, c1, args, ranks, stream, weights=weights)
+        dms, de2e = ranks.max([d["ms"], d["e2e_ms"]])
+        dwork = _algorithmic(c1, d["counts"])
+        droof = roofline_stream_up(d["kern"], dwork, peaks, read_gbs)
+        droof["traffic"] = _profile_traffic("stream_up", c1["name"])
+        line["decode"] = {
+            "workload": c1["name"], "value": throughput(c1["T"], world, dms), "unit": UNIT,
+            "ms_per_step": round(dms, 5),
+            "weight_gbs": round(dwork["weight_bytes"] / (dms * 1e-3) / 1e9, 1),
+            "frac_hbm_copy_peak": round(dwork["weight_bytes"] / (dms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+            "frac_hbm_read_peak": round(dwork["weight_bytes"] / (dms * 1e-3) / 1e9 / read_gbs, 4) if read_gbs else None,
+            "experts_touched": dwork["touched"], "roofline": droof,
+            "kernels_ms_per_step": {n: round(v[1] / max(1, args.steps), 5) for n, v in d["kern"].items()},
+            "kernels_ms_per_step_serialised": round(d["serial_ms"], 5),
+            "e2e": {"value": throughput(c1["T"], world, de2e), "unit": UNIT, "h2d_bytes_per_step": d["io_bytes"],
+                    "d2h_bytes_per_step": d["io_bytes"], "ms_per_step": round(de2e, 5)},
+            "clocks": d["clocks"]}
+        line["decode"]["gpu_launches"] = int(sum(v[0] for v in d["kern"].values()))
+        gpu_out["decode"] = {"cfg": 1, "y": d["y"].cpu(), "idx": d["idx"]}
+        del d
     ranks.close()
-    return line if rank == 0 else None
+    if rank != 0:
+        return None
+    line["_gpu_out"] = gpu_out
+    return line
 
 
 TRAIN_GEMM_FLOPS = {  # multiples of R*d*ffn (R = 2T slot rows) per launch
@@ -715,29 +819,85 @@ def run_ep(args) -> dict:
                     "it received, the quantity the slowest rank of a real expert-parallel step is bound by"}
 
 
-def cpu_baseline(k: int, max_tokens: int | None = None, budget_s: float = 20.0) -> dict:
-    """The fp64 oracle, as it stands, on a bounded sample of the workload's tokens."""
+def _oracle_cores() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        return max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def _sample_tokens(idx_ref, T: int, n: int, seed: int):
+    """n seeded token indices, led by up to 4 tokens of the least-used expert that has any."""
+    import numpy as np
+    counts = np.bincount(idx_ref.ravel(), minlength=8)
+    used = [e for e in range(8) if counts[e] > 0]
+    rare = min(used, key=lambda e: counts[e])
+    lead = np.nonzero((idx_ref == rare).any(axis=1))[0][:4].tolist()
+    rest = np.random.default_rng(seed).permutation(T).tolist()
+    out = list(dict.fromkeys(lead + rest))
+    return out[:min(n, T)], int(rare)
+
+
+def cpu_baseline(gpu_out: dict, budget_s: float = 20.0, decode_budget_s: float = 6.0) -> tuple[dict, dict]:
+    """The fp64 oracle, as it stands, on a bounded sample of the timed workload's tokens, one oracle call per
+    token (its rate is the CPU baseline). Its results are also the parity check of the GPU's output of the
+    timed steps: routing on every token, y on the sampled tokens, and the statistics when the step has them."""
+    import numpy as np
+
     import oracle
     from moe_inputs import CONFIGS, make_config, to_f64
 
-    try:
-        from threadpoolctl import threadpool_info
-        cores = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
-    except Exception:
-        cores = os.cpu_count() or 1
+    cores = _oracle_cores()
+    k = gpu_out["cfg"]
     cfg = CONFIGS[k]
     L = make_config(k)
     w = tuple(t.float().numpy() for t in (L.w1, L.w3, L.w2))
-    x64, wg64 = to_f64(L.x), to_f64(L.w_gate)
-    n = cfg["T"] if max_tokens is None else min(cfg["T"], max_tokens)
-    done, t0 = 0, time.time()
-    while done < n and (time.time() - t0) < budget_s:
-        oracle.layer_forward_tokens(x64, wg64, *w, [done])
-        done += 1
-    dt = time.time() - t0
-    return {"value": round(done / dt, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{done} of the workload's {cfg['T']} tokens, one oracle call per token "
-                      f"(fp64 router, both experts incl. weight widening), {dt:.1f} s"}
+
+    def check(L, out, budget, n_max, seed):
+        x64, wg64 = to_f64(L.x), to_f64(L.w_gate)
+        logits = oracle.router_logits(x64, wg64)
+        idx_ref, _, _ = oracle.top_k_gates(logits, 2)
+        routing_exact = bool(np.array_equal(out["idx"].numpy().astype(np.int64), idx_ref))
+        tokens, rare = _sample_tokens(idx_ref, L.T, n_max, seed)
+        y_gpu = to_f64(out["y"])
+        refs, done, t0 = [], [], time.time()
+        for t in tokens:
+            if done and (time.time() - t0) >= budget:
+                break
+            refs.append(oracle.layer_forward_tokens(x64, wg64, *w, [t])[0])
+            done.append(t)
+        dt = time.time() - t0
+        ref = np.stack(refs)
+        err = float(np.max(np.abs(y_gpu[done] - ref)) / np.max(np.abs(ref)))
+        par = {"routing_exact": routing_exact, "tokens_routed": int(L.T), "y_tokens_checked": len(done),
+               "y_max_rel_err": err, "tol": 2e-2, "finite": bool(np.all(np.isfinite(y_gpu))),
+               "rarest_expert": rare}
+        aux_ok = True
+        if out.get("stats") is not None:
+            # the statistics' tolerances of the GPU tests: f exact up to one fp32 rounding, P from fp32 scores
+            a = oracle.aux_stats(logits, idx_ref, 8)
+            f, P, l = (t.numpy().astype(np.float64) for t in out["stats"])
+            par["aux"] = {"f_max_abs_err": float(np.max(np.abs(f - a["f"]))),
+                          "P_max_abs_err": float(np.max(np.abs(P - a["P"]))),
+                          "l_aux": float(l[0]), "l_aux_ref": float(a["l_aux"]),
+                          "l_aux_rel_err": abs(float(l[0]) - float(a["l_aux"])) / float(a["l_aux"]),
+                          "tol": {"f": 1e-7, "P": 2e-5, "l_aux_rel": 1e-4}}
+            aux_ok = (par["aux"]["f_max_abs_err"] <= 1e-7 and par["aux"]["P_max_abs_err"] <= 2e-5
+                      and par["aux"]["l_aux_rel_err"] <= 1e-4)
+        par["pass"] = bool(routing_exact and par["finite"] and err <= 2e-2 and aux_ok)
+        return par, len(done), dt
+
+    par, n, dt = check(L, gpu_out, budget_s, 64, 11)
+    base = {"value": round(n / dt, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{n} of the workload's {cfg['T']} tokens, one oracle call per token (fp64 router, both "
+                      f"experts incl. weight widening), {dt:.1f} s"}
+    if "decode" in gpu_out:
+        L1 = make_config(1, weights=(L.w1, L.w3, L.w2))
+        dpar, _, _ = check(L1, gpu_out["decode"], decode_budget_s, 16, 12)
+        par["decode"] = dpar
+        par["pass"] = par["pass"] and dpar["pass"]
+    return base, par
 
 
 def run_reference(args, rank, world) -> dict | None:
@@ -792,8 +952,10 @@ def main():
                     help="time the decoder block around the layer (attention + MoE) at the Mixtral shape")
     ap.add_argument("--block-decode", action="store_true",
                     help="time one decode step of the Mixtral block (16 sequences, 4096-token caches)")
-    ap.add_argument("--tile-ctas", type=int, default=0, choices=[0, 1, 2, 4],
-                    help="token tiles: automatic (0), single CTAs (1), CTA pairs (2), two pairs per cluster (4)")
+    ap.add_argument("--tile-ctas", type=int, default=0, choices=[0, 1, 2],
+                    help="token tiles: automatic (0), single CTAs (1), CTA pairs (2)")
+    ap.add_argument("--no-decode", action="store_true",
+                    help="skip the decode batch that the default line carries beside the headline workload")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -824,8 +986,9 @@ def main():
     line = run_ours(args, rank, world, local)
     if line is None:
         return
+    gpu_out = line.pop("_gpu_out")
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(args.config)
+        line["cpu_baseline"], line["parity"] = cpu_baseline(gpu_out)
     print(json.dumps(line), flush=True)
 
 

@@ -396,6 +396,15 @@ moe_status moe_check_device_status(void* stream);
  * in the status word, as a real stall would; the device stays usable. */
 moe_status moe_selftest_wait_timeout(uint64_t timeout_ns, int32_t* gave_up, void* stream);
 
+/* Read-bandwidth probe (a measurement utility; the pages have no counterpart):
+ * reads `bytes` (a multiple of 16) of device memory at `buf` (16-byte aligned)
+ * once, with streaming loads, and writes nothing but possibly one word to
+ * `sink` (a device uint32, 4-byte aligned). Timed over a buffer much larger
+ * than L2 it gives the HBM read rate, the roofline of the weight-streaming
+ * kernels, which read and do not write. Enqueued on `stream`; argument errors
+ * return MOE_ERR_INVALID_ARG before anything is enqueued. */
+moe_status moe_read_probe(const void* buf, size_t bytes, uint32_t* sink, void* stream);
+
 /* Upper bound, in nanoseconds, on every device-side wait of the tensor-core
  * kernels (default 2e9). A wait that runs out latches MOE_ERR_TIMEOUT and the
  * kernel returns early after its in-flight copies and MMAs have landed. */
@@ -416,9 +425,8 @@ moe_status moe_set_wait_timeout_ns(uint64_t ns);
  *   MOE_KNOB_TILE_CTAS  0 (default) = automatic: 128-token tiles on single
  *                       CTAs up to 384 tokens, 256-token tiles on CTA pairs
  *                       (one tcgen05 MMA spans two SMs) above; 1 = single
- *                       CTAs; 2 = CTA pairs; 4 = two CTA pairs per cluster
- *                       sharing each token tile (loaded once, multicast). The
- *                       single-CTA kernel also runs when no CTA pair fits.
+ *                       CTAs; 2 = CTA pairs. The single-CTA kernel also
+ *                       runs when no CTA pair fits.
  *   MOE_KNOB_DEBUG      1 = debug mode: every launch is followed by a wait on
  *                       its stream and a look at the device status word, so a
  *                       device-side error (timeout, index check) is returned by

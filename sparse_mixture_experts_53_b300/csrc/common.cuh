@@ -344,18 +344,6 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
-// As tma_load_2d_pair, with the tile written to the same shared-memory offset
-// in every CTA of `cta_mask`; each destination's bytes are counted on the
-// barrier at `bar_cluster`'s offset in the even CTA of that destination's pair.
-__device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster, int x,
-                                                    int y, uint16_t cta_mask, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5, %6;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y), "h"(cta_mask), "l"(policy)
-        : "memory");
-}
-
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
                  : "memory");
@@ -430,6 +418,31 @@ __global__ void wait_selftest_kernel(uint64_t timeout_ns, int* gave_up) {
         mbar_arrive(smem_u32(&bar));
     }
     __syncthreads();
+}
+
+// ---------------------------------------------------------------------------
+// Read-bandwidth probe: every thread streams 16-byte words of a device buffer
+// (four loads in flight, cache-streaming hint so the buffer does not displace
+// L2 contents) and folds them into a word that is stored only if it equals a
+// value no input makes likely, so the loads cannot be dropped. It measures the
+// rate at which this GPU reads HBM, the ceiling of a kernel that only streams
+// weights (a copy also writes, so its rate is not that ceiling).
+// ---------------------------------------------------------------------------
+__global__ void read_probe_kernel(const uint4* __restrict__ buf, size_t n16, uint32_t* sink) {
+    pdl_wait();
+    uint32_t acc = 0;
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (; i + 3 * stride < n16; i += 4 * stride) {
+        const uint4 a = __ldcs(buf + i), b = __ldcs(buf + i + stride);
+        const uint4 c = __ldcs(buf + i + 2 * stride), d = __ldcs(buf + i + 3 * stride);
+        acc ^= (a.x ^ a.y ^ a.z ^ a.w) + (b.x ^ b.y ^ b.z ^ b.w) + (c.x ^ c.y ^ c.z ^ c.w) + (d.x ^ d.y ^ d.z ^ d.w);
+    }
+    for (; i < n16; i += stride) {
+        const uint4 a = __ldcs(buf + i);
+        acc ^= a.x ^ a.y ^ a.z ^ a.w;
+    }
+    if (acc == 0x9E3779B9u) sink[0] = acc;
 }
 
 }  // namespace moe

@@ -503,16 +503,11 @@ __device__ __forceinline__ void wgrad_epilogue(uint32_t taddr, bool any_k, int e
     }
 }
 
-// NP CTA pairs per thread-block cluster (launched with cluster size 2 NP). With
-// NP = 2 the two pairs compute neighbouring column tiles of the same token
-// tile: the even pair loads the token rows once and multicasts them into the
-// other pair's shared memory, and both pairs' MMA commits release every CTA's
-// stage (forward modes only).
-template <int MODE, int NP>
+// One CTA pair per thread-block cluster (launched with cluster size 2).
+template <int MODE>
 __global__ void __launch_bounds__(kPairThreads, 1)
     tile_pair_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b0,
                           const __grid_constant__ CUtensorMap map_b1, const TileArgs args) {
-    static_assert(NP == 1 || (NP == 2 && MODE <= PM_DOWN), "token-tile multicast covers the forward modes");
     constexpr bool UP = MODE == PM_UP;
     constexpr bool WG = MODE == PM_WGRAD;
     constexpr bool A_MN = WG;                      // A read as stored with K = token rows
@@ -523,15 +518,12 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     TcControl* ctl = reinterpret_cast<TcControl*>(smem + (size_t)kPairStages * kPairStageBytes);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint32_t crank = cluster_ctarank();
-    const uint32_t rank = crank & 1u;            // CTA of the pair
-    const int pr = (int)(crank >> 1);            // pair of the cluster
-    const uint32_t lead = crank & ~1u;           // the pair's even CTA
+    const uint32_t rank = cluster_ctarank();     // CTA of the pair
+    const uint32_t lead = 0;                     // the pair's even CTA
     const bool leader = rank == 0;
-    const int pair = blockIdx.x / (2 * NP);      // cluster index: the unit sequence
-    const int n_pairs = gridDim.x / (2 * NP);
-    const uint16_t pair_mask = (uint16_t)(0x3u << (2 * pr));
-    const uint16_t all_mask = (uint16_t)((1u << (2 * NP)) - 1u);
+    const int pair = blockIdx.x / 2;             // cluster index: the unit sequence
+    const int n_pairs = gridDim.x / 2;
+    const uint16_t pair_mask = 0x3u;
     const int kid = UP ? K_TILE_UP : (MODE == PM_DOWN ? K_TILE_DOWN : K_TILE_BWD);
     const uint64_t tmo = args.timeout_ns;
     volatile int* abort_flag = &ctl->abort_flag;
@@ -539,7 +531,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < kPairStages; ++s) {
             mbar_init(smem_u32(&ctl->full[s]), 1);
-            mbar_init(smem_u32(&ctl->empty[s]), NP);  // one commit from every pair of the cluster
+            mbar_init(smem_u32(&ctl->empty[s]), 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&ctl->tfull[b]), 1);
@@ -574,7 +566,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             // token modes: 256-token row tiles; weight gradients: fixed row tiles, every expert
             ctl->mt[e] = WG ? args.m_tiles : (c + kPairM - 1) / kPairM;
             ctl->base[e] = tiles;
-            tiles += ctl->mt[e] * (args.n_tiles_n / NP);
+            tiles += ctl->mt[e] * args.n_tiles_n;
         }
         ctl->base[args.E] = tiles;
         ctl->n_work = tiles;
@@ -591,14 +583,13 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     const int E = args.E;
     const int KB = args.K / kBK;
 
-    // unit -> expert, column tile of this pair, row tile
+    // unit -> expert, column tile, row tile
     auto decode = [&](int tile, int& e, int& nt, int& mt) {
         e = 0;
         while (e < E - 1 && tile >= ctl->base[e + 1]) ++e;
         const int rem = tile - ctl->base[e];
-        const int ng = rem / ctl->mt[e];
-        mt = rem - ng * ctl->mt[e];
-        nt = ng * NP + pr;
+        nt = rem / ctl->mt[e];
+        mt = rem - nt * ctl->mt[e];
     };
     // K steps of a tile: fixed, or the expert's padded token count
     auto ksteps = [&](int e) { return WG ? (ctl->koff[e + 1] - ctl->koff[e]) / kBK : KB; };
@@ -643,13 +634,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                         const int ky = ctl->koff[e] + kx;
                         tma_load_2d_pair(sa, &map_a, fb, a0, ky, pol_w);
                         tma_load_2d_pair(sa + kPairHalfBytes / 2, &map_a, fb, a0 + 64, ky, pol_w);
-                    } else if (NP == 1) {
+                    } else {
                         tma_load_2d_pair(sa, &map_a, fb, kx, a0, pol_act);
-                    } else if (pr == 0) {
-                        // the token rows of both pairs: loaded once, written to this CTA and
-                        // to the same CTA of the other pair
-                        tma_load_2d_pair_mc(sa, &map_a, fb, kx, a0, (uint16_t)((1u << crank) | (1u << (crank + 2))),
-                                            pol_act);
                     }
                     if (B_MN) {
                         // two boxes of 64 columns x 64 K rows, read as stored
@@ -719,14 +705,14 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                     for (int kk = 0; kk < kBK / 16; ++kk)
                         mma_bf16_pair(d_tmem, adesc + a_step * kk, bdesc + b_step * kk, idesc, (kb | kk) != 0);
                     any = true;
-                    mma_commit_pair(smem_u32(&ctl->empty[s]), all_mask);
+                    mma_commit_pair(smem_u32(&ctl->empty[s]), pair_mask);
                     if (++s == kPairStages) { s = 0; ph ^= 1; }
                 }
                 if (!ok) break;
                 mma_commit_pair(smem_u32(&ctl->tfull[b]), pair_mask);
             }
             if (any) {
-                mma_commit_pair(smem_u32(&ctl->drain), (uint16_t)(1u << crank));
+                mma_commit_pair(smem_u32(&ctl->drain), (uint16_t)1u);
                 drain_wait(smem_u32(&ctl->drain), 0, tmo, kid);
             }
         }

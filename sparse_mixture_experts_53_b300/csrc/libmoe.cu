@@ -8,6 +8,7 @@
 #include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <utility>
 #include <cstdio>
@@ -71,7 +72,7 @@ struct HostState {
     bool debug = env_flag("MOE_DEBUG");  // synchronise after every launch and report device errors at once
     bool timing = false;
     bool pdl = true;           // programmatic dependent launch between the library's kernels
-    int tile_ctas = 0;         // token tiles: 0 auto, 1 single CTAs, 2 CTA pairs, 4 two pairs per cluster
+    int tile_ctas = 0;         // token tiles: 0 auto, 1 single CTAs, 2 CTA pairs
     int pair_cap[kMaxDevices][8] = {{0}};  // resident clusters per pair kernel (0 = not queried)
     std::vector<TimingRecord> records;
     std::vector<cudaEvent_t> pool;
@@ -516,22 +517,20 @@ int pair_grid(int64_t pairs_upper, int cap) {
     return 2 * pairs;
 }
 
-// Both expert GEMMs on CTA-pair token tiles, NP pairs per cluster.
+// Both expert GEMMs on CTA-pair token tiles.
 // MOE_ERR_UNSUPPORTED (nothing enqueued) when the kernels do not fit.
-template <int NP>
 moe_status run_pair_ffn(const moe_shape& s, const void* x_perm, const int32_t* offsets, const float* perm_w,
                         const void* w1, const void* w3, const void* w2, float* y_slot, __nv_bfloat16* H,
                         __nv_bfloat16* u_out, __nv_bfloat16* v_out, cudaStream_t st) {
     const int64_t R = 2 * s.T;
     const int d = s.d, F = s.ffn, E = s.E;
-    constexpr int CL = 2 * NP;
-    auto kup = tile_pair_gemm_kernel<PM_UP, NP>;
-    auto kdown = tile_pair_gemm_kernel<PM_DOWN, NP>;
-    const int slot = NP == 1 ? 6 : 12;
-    const int cap_slot = NP == 1 ? 0 : 5;  // the backward kernels use slots 2-4
-    const int cap_up = ensure_smem(kup, slot, kPairSmemBytes) ? pair_capacity(kup, kPairSmemBytes, cap_slot, CL) : -1;
+    auto kup = tile_pair_gemm_kernel<PM_UP>;
+    auto kdown = tile_pair_gemm_kernel<PM_DOWN>;
+    const int slot = 6;
+    const int cap_slot = 0;  // the backward kernels use slots 2-4
+    const int cap_up = ensure_smem(kup, slot, kPairSmemBytes) ? pair_capacity(kup, kPairSmemBytes, cap_slot) : -1;
     const int cap_down =
-        ensure_smem(kdown, slot + 1, kPairSmemBytes) ? pair_capacity(kdown, kPairSmemBytes, cap_slot + 1, CL) : -1;
+        ensure_smem(kdown, slot + 1, kPairSmemBytes) ? pair_capacity(kdown, kPairSmemBytes, cap_slot + 1) : -1;
     if (cap_up <= 0 || cap_down <= 0) {
         cudaGetLastError();
         return MOE_ERR_UNSUPPORTED;
@@ -541,18 +540,18 @@ moe_status run_pair_ffn(const moe_shape& s, const void* x_perm, const int32_t* o
         !make_map(&mb1, w3, d, (uint64_t)E * F, 128))
         return MOE_ERR_CUDA;
     TileArgs up{offsets, perm_w, H, E, d, F / kTileM, F, F, g.timeout_ns, u_out, v_out};
-    const int64_t units_up = ((R + kPairM - 1) / kPairM + E) * (F / kTileM / NP);
+    const int64_t units_up = ((R + kPairM - 1) / kPairM + E) * (F / kTileM);
     MOE_TRY(launch("tile_up_swiglu", st, [&] {
-        return klaunch_cluster(kup, CL, CL * (pair_grid(units_up, cap_up) / 2), kPairThreads, kPairSmemBytes, st, ma,
-                               mb0, mb1, up);
+        return klaunch_cluster(kup, 2, pair_grid(units_up, cap_up), kPairThreads, kPairSmemBytes, st, ma, mb0, mb1,
+                               up);
     }));
     CUtensorMap mh, mw2;
     if (!make_map(&mh, H, F, R, 128) || !make_map(&mw2, w2, F, (uint64_t)E * d, 128)) return MOE_ERR_CUDA;
     TileArgs down{offsets, perm_w, y_slot, E, F, d / kTileN, d, d, g.timeout_ns};
-    const int64_t units_down = ((R + kPairM - 1) / kPairM + E) * (d / kTileN / NP);
+    const int64_t units_down = ((R + kPairM - 1) / kPairM + E) * (d / kTileN);
     return launch("tile_down_scale", st, [&] {
-        return klaunch_cluster(kdown, CL, CL * (pair_grid(units_down, cap_down) / 2), kPairThreads, kPairSmemBytes, st,
-                               mh, mw2, mw2, down);
+        return klaunch_cluster(kdown, 2, pair_grid(units_down, cap_down), kPairThreads, kPairSmemBytes, st, mh, mw2,
+                               mw2, down);
     });
 }
 
@@ -581,14 +580,9 @@ moe_status run_ffn(const moe_shape& s, const void* x_perm, const int32_t* offset
     }
     __nv_bfloat16* H = reinterpret_cast<__nv_bfloat16*>(ws + L.h);
     const int tile_ctas = g.tile_ctas != 0 ? g.tile_ctas : (s.T <= kSingleCtaMaxTokens ? 1 : 2);
-    if (L.path == 1 && tile_ctas >= 2) {
-        // CTA pairs: each CTA stages 128 token rows and 128 weight rows per stage;
-        // tile_ctas == 4: two pairs per cluster share each token tile
-        const bool quad = tile_ctas == 4 && (F / kTileM) % 2 == 0 && (d / kTileN) % 2 == 0;
-        moe_status rc = MOE_ERR_UNSUPPORTED;
-        if (quad) rc = run_pair_ffn<2>(s, x_perm, offsets, perm_w, w1, w3, w2, y_slot, H, u_out, v_out, st);
-        if (rc == MOE_ERR_UNSUPPORTED)
-            rc = run_pair_ffn<1>(s, x_perm, offsets, perm_w, w1, w3, w2, y_slot, H, u_out, v_out, st);
+    if (L.path == 1 && tile_ctas == 2) {
+        // CTA pairs: each CTA stages 128 token rows and 128 weight rows per stage
+        const moe_status rc = run_pair_ffn(s, x_perm, offsets, perm_w, w1, w3, w2, y_slot, H, u_out, v_out, st);
         if (rc != MOE_ERR_UNSUPPORTED) return rc;
     }
     if (L.path == 1) {
@@ -758,7 +752,7 @@ moe_status launch_pair(const char* name, int slot, int cap_slot, const CUtensorM
                        const CUtensorMap& mb1, const TileArgs& a, int64_t pairs_upper, cudaStream_t st) {
     // the weight-gradient epilogue stages its stores in 4 warps' arrays after the control block
     const size_t smem = kPairSmemBytes + (MODE == PM_WGRAD ? kWgradStageBytes : 0);
-    auto kern = tile_pair_gemm_kernel<MODE, 1>;
+    auto kern = tile_pair_gemm_kernel<MODE>;
     if (!ensure_smem(kern, slot, smem)) return MOE_ERR_CUDA;
     const int cap = pair_capacity(kern, smem, cap_slot);
     if (cap <= 0) return MOE_ERR_UNSUPPORTED;
@@ -856,21 +850,23 @@ moe_status run_backward(const moe_shape& s, const __nv_bfloat16* x, const __nv_b
 // Scratch of moe_layer_forward_noalloc: a fixed array of static device memory,
 // one copy per device that loads the library, held until the process exits.
 constexpr size_t kNoAllocScratchBytes = size_t(24) << 20;
-__device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 // Device address of the scratch array on the current device. The array's name
 // is only a host-side stand-in in host code, so its address is looked up once
-// per device (with that device current) and cached.
+// per device (with that device current) and cached. Host threads that make
+// their first call on one device at the same time may both look it up; they
+// store the same value, and the atomic slots keep that well defined.
 void* noalloc_scratch() {
-    static void* addr[kMaxDevices] = {nullptr};
+    static std::atomic<void*> addr[kMaxDevices];
     const int dev = current_device();
     if (dev < 0 || dev >= kMaxDevices) return nullptr;
-    if (addr[dev] == nullptr) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
-        addr[dev] = p;
+    void* p = addr[dev].load(std::memory_order_acquire);
+    if (p == nullptr) {
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return nullptr;
+        addr[dev].store(p, std::memory_order_release);
     }
-    return addr[dev];
+    return p;
 }
 
 // ------------------------------------------------------------ decoder block
@@ -1587,6 +1583,16 @@ moe_status moe_selftest_wait_timeout(uint64_t timeout_ns, int32_t* gave_up, void
     });
 }
 
+moe_status moe_read_probe(const void* buf, size_t bytes, uint32_t* sink, void* stream) {
+    if (!ok_ptr(buf) || !ok_ptr(sink) || bytes == 0 || bytes % 16 != 0) return MOE_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t n16 = bytes / 16;
+    const int grid = (int)std::max<size_t>(1, std::min<size_t>((size_t)sm_count() * 4, (n16 + 511) / 512));
+    return launch("read_probe", st, [&] {
+        return klaunch(read_probe_kernel, grid, 512, 0, st, static_cast<const uint4*>(buf), n16, sink);
+    });
+}
+
 moe_status moe_get_device_status(int32_t* code, int32_t* detail) {
     if (code == nullptr) return MOE_ERR_INVALID_ARG;
     if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
@@ -1631,7 +1637,7 @@ moe_status moe_set_knob(int32_t knob, int64_t value) {
             g.pdl = value != 0;
             return MOE_OK;
         case MOE_KNOB_TILE_CTAS:
-            if (value < 0 || value > 4 || value == 3) return MOE_ERR_INVALID_ARG;
+            if (value < 0 || value > 2) return MOE_ERR_INVALID_ARG;
             g.tile_ctas = (int)value;
             return MOE_OK;
         case MOE_KNOB_DEBUG:

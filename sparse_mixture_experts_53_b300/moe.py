@@ -44,6 +44,7 @@ EXPORTED = (
     "moe_check_device_status", "moe_block_workspace_bytes", "moe_block_forward", "moe_rmsnorm", "moe_linear",
     "moe_rope_split", "moe_attention", "moe_residual_add", "moe_block_decode_workspace_bytes", "moe_block_decode",
     "moe_linear_workspace_bytes", "moe_attention_decode_workspace_bytes", "moe_attention_decode",
+    "moe_read_probe",
 )
 
 
@@ -99,6 +100,7 @@ def _load() -> ctypes.CDLL:
         "moe_timing_read": ([ctypes.c_char_p, ctypes.c_size_t], I),
         "moe_gather_rows": ([P, ctypes.c_int64, P, ctypes.c_int64, ctypes.c_int64, P, P], I),
         "moe_selftest_wait_timeout": ([ctypes.c_uint64, P, P], I),
+        "moe_read_probe": ([P, ctypes.c_size_t, P, P], I),
         "moe_check_device_status": ([P], I),
         "moe_train_state_bytes": ([S], ctypes.c_size_t),
         "moe_backward_workspace_bytes": ([S], ctypes.c_size_t),
@@ -265,6 +267,12 @@ def moe_layer_backward(shape, x, w_gate, w1, w3, w2, dy, aux_coef, state, dx, dw
 def moe_selftest_wait_timeout(timeout_ns: int, gave_up, stream=None):
     _check("moe_selftest_wait_timeout", lib.moe_selftest_wait_timeout(int(timeout_ns), _ptr(gave_up),
                                                                       _stream(stream)))
+
+
+def moe_read_probe(buf, sink, stream=None):
+    """Reads every byte of the device tensor `buf` once (HBM read-rate probe); sink: a device int32 tensor."""
+    _check("moe_read_probe", lib.moe_read_probe(_ptr(buf), buf.numel() * buf.element_size(), _ptr(sink),
+                                                _stream(stream)))
 
 
 def moe_check_device_status(stream=None) -> int:

@@ -96,6 +96,7 @@ def test_knobs_and_timeouts():
     assert lib.moe_set_knob(moe.MOE_KNOB_FFN_PATH, 3) == moe.MOE_ERR_INVALID_ARG
     assert lib.moe_set_knob(moe.MOE_KNOB_KSLICE, 100) == moe.MOE_ERR_INVALID_ARG
     assert lib.moe_set_knob(moe.MOE_KNOB_TILE_CTAS, 3) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_set_knob(moe.MOE_KNOB_TILE_CTAS, 4) == moe.MOE_ERR_INVALID_ARG
     assert lib.moe_set_knob(moe.MOE_KNOB_TILE_CTAS, 5) == moe.MOE_ERR_INVALID_ARG
     assert lib.moe_set_knob(moe.MOE_KNOB_PDL, 2) == moe.MOE_ERR_INVALID_ARG
     assert lib.moe_set_wait_timeout_ns(0) == moe.MOE_ERR_INVALID_ARG

@@ -17,6 +17,21 @@ from gpu_harness import TOL, assert_status_ok
 pytestmark = pytest.mark.gpu
 
 
+class _pinned_tiles:
+    """Token-tile expert GEMMs on single CTAs (1) or CTA pairs (2) for every row count."""
+
+    def __init__(self, ctas):
+        self.ctas = ctas
+
+    def __enter__(self):
+        moe.moe_set_knob(moe.MOE_KNOB_FFN_PATH, 1)
+        moe.moe_set_knob(moe.MOE_KNOB_TILE_CTAS, self.ctas)
+
+    def __exit__(self, *exc):
+        moe.moe_set_knob(moe.MOE_KNOB_FFN_PATH, 0)
+        moe.moe_set_knob(moe.MOE_KNOB_TILE_CTAS, 0)
+
+
 def _margin_tokens(T, d, seed, wg, skew=None):
     """Token rows with the 1e-3 router margin for the given router weights."""
     g = torch.Generator().manual_seed(seed)
@@ -92,9 +107,17 @@ def test_emulated_ranks_equal_the_single_gpu_layer(N, T, mode):
     for x, y in zip(xs, ys):
         ref = oracle.layer_forward(to_f64(x.cpu()), to_f64(L.w_gate), to_f64(L.w1), to_f64(L.w3), to_f64(L.w2))["y"]
         assert np.max(np.abs(y.float().cpu().numpy() - ref)) <= TOL["bf16"] * np.max(np.abs(ref))
-        single = moe.layer_forward(x, dev["w_gate"], dev["w1"], dev["w3"], dev["w2"])
-        # same rows, same weights, same K order: the same values as the single-GPU layer
-        assert torch.allclose(y.float(), single.float(), rtol=0, atol=1e-2 * float(single.float().abs().max()))
+    # Same rows, same weights, same K order: with the expert GEMM's kernel pinned (a rank's row
+    # count would otherwise pick its own tile shape or split-K width), every rank's output equals
+    # the single-GPU layer's bit for bit.
+    for ctas in (1, 2):
+        with _pinned_tiles(ctas):
+            ys, _, _ = ep.emulate(xs, dev["w_gate"], dev["w1"], dev["w3"], dev["w2"], owner)
+            for x, y in zip(xs, ys):
+                single = moe.layer_forward(x, dev["w_gate"], dev["w1"], dev["w3"], dev["w2"])
+                torch.cuda.synchronize()
+                assert_status_ok()
+                assert torch.equal(y, single)
 
 
 def test_skewed_routing_is_rebalanced_by_placement():
@@ -118,5 +141,12 @@ def test_skewed_routing_is_rebalanced_by_placement():
                               ep.replicated_placement(load, N, 8 // N + 1))
     assert_status_ok()
     assert p_r.rows_per_rank.max() < p_b.rows_per_rank.max()
-    for y_b, y_r in zip(ys, ys_r):
-        assert torch.allclose(y_b.float(), y_r.float(), rtol=0, atol=1e-2 * float(y_b.float().abs().max()))
+    # the same rows through the same pinned kernel, split differently over the ranks: the same bits
+    with _pinned_tiles(2):
+        ys_b, _, _ = ep.emulate(xs, dev["w_gate"], dev["w1"], dev["w3"], dev["w2"], ep.balanced_owners(load, N))
+        ys_r, _, _ = ep.emulate(xs, dev["w_gate"], dev["w1"], dev["w3"], dev["w2"],
+                                ep.replicated_placement(load, N, 8 // N + 1))
+        torch.cuda.synchronize()
+        assert_status_ok()
+    for y_b, y_r in zip(ys_b, ys_r):
+        assert torch.equal(y_b, y_r)

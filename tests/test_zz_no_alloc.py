@@ -5,9 +5,10 @@ whose host application owns every device allocation through its own pool, or a
 serving loop that must not call cudaMalloc because it can synchronise the
 device). This entry point needs no workspace: its intermediates live in a
 fixed 24 MiB static device array inside the library. Here it is checked
-against moe_layer_forward (caller workspace) on the Mixtral decode batch, on
-two calls in a row with different tokens, so that the second call also shows
-that the scratch left by the first does not leak into its result.
+against moe_layer_forward (caller workspace) on the Mixtral decode batch, bit
+for bit, and against the fp64 oracle within the bf16 tolerance, on two calls
+in a row with different tokens, so that the second call also shows that the
+scratch left by the first does not leak into its result.
 
 This file is collected last (test_zz_*) so that a run that stops at the first
 failure has already run every other test.
@@ -16,10 +17,11 @@ import numpy as np
 import pytest
 import torch
 
-from moe_inputs import CONFIGS, make_config, make_tokens
+import oracle
+from moe_inputs import CONFIGS, make_config, make_tokens, to_f64
 from sparse_mixture_experts_53_b300 import moe
 
-from gpu_harness import TOL, assert_status_ok
+from gpu_harness import TOL, assert_status_ok, host_weights
 
 pytestmark = pytest.mark.gpu
 
@@ -46,9 +48,13 @@ def test_noalloc_matches_workspace_entry_on_two_calls(decode_layer):
         moe.moe_layer_forward_noalloc(shape, x, dev["w_gate"], dev["w1"], dev["w3"], dev["w2"], y)
         torch.cuda.synchronize()
         assert_status_ok()
-        a, b = y.float().cpu().numpy(), ref.float().cpu().numpy()
-        assert np.all(np.isfinite(a))
-        assert np.max(np.abs(a - b)) <= TOL["bf16"] * np.max(np.abs(b))
+        # the same kernels in the same order on the same shape: the same bits
+        assert torch.equal(y, ref)
+        # and, independently of the other entry point, within the bf16 tolerance of the fp64 oracle
+        y_ref = oracle.layer_forward(to_f64(x.cpu()), to_f64(L.w_gate), *host_weights(L))["y"]
+        got = to_f64(y.cpu())
+        assert np.all(np.isfinite(got))
+        assert np.max(np.abs(got - y_ref)) <= TOL["bf16"] * np.max(np.abs(y_ref))
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch(decode_layer):
