@@ -774,6 +774,109 @@ def run_block_decode(args) -> dict:
     }
 
 
+def run_decode_loop(args) -> dict:
+    """Decode-time expert cache (measured experiment): one decode step per sequence of a token stream
+    whose consecutive tokens share experts at the lecture page's rate, through one Mixtral-shape layer or
+    through 32 layers (distinct weight copies, as a model's MoE layers), with and without the weight-
+    streaming path keeping part of each call's expert weights in L2 for the next call."""
+    import torch
+
+    from moe_inputs import CONFIGS, make_token_stream, make_tokens, make_weights
+    from sparse_mixture_experts_53_b300 import moe
+
+    torch.cuda.set_device(0)
+    moe.moe_set_knob(moe.MOE_KNOB_PDL, args.pdl)
+    sched = json.loads((ROOT / "tests" / "golden" / "locality_schedule.json").read_text())
+    c = CONFIGS[1]
+    d, F, E = c["d"], c["ffn"], c["E"]
+    w_host = make_weights(d, F, E, c["dtype"], c["weight_seed"])
+    _, wg_host = make_tokens(1, d, E, c["dtype"], c["seed"])
+    wg = wg_host.cuda()
+    layers_max = 32
+    base = tuple(w.cuda() for w in w_host)
+    del w_host
+    weights = [base] + [tuple(w.clone() for w in base) for _ in range(layers_max - 1)]
+    stream = torch.cuda.current_stream()
+    Bmax = 4
+    streams = {"locality": float(sched["rho"]), "independent": 0.0}
+    n_steps = {1: 64, 32: 12}
+    warm = 4
+    xs = {name: make_token_stream(Bmax, n_steps[1] + warm, d, rho, sched["seed"]).cuda()
+          for name, rho in streams.items()}
+    ws = moe.workspace(moe.make_shape(Bmax, d, F, moe.MOE_BF16))
+    y = torch.empty((Bmax, d), dtype=torch.bfloat16, device="cuda")
+    keep_mb = [0, 32, 64, 96]
+    results = []
+    sampler = ClockSampler(0)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # The evict-last priority may only take hold inside the L2 portion that the context sets aside for
+    # persisting lines (0 unless the application asks for it). This experiment, as an application would,
+    # runs the matrix once as found and once with that context limit raised to the device's maximum;
+    # the limit belongs to this process's context and is put back before the end.
+    from cuda.bindings import runtime as rt
+    err, limit0 = rt.cudaDeviceGetLimit(rt.cudaLimit.cudaLimitPersistingL2CacheSize)
+    err2, prop = rt.cudaGetDeviceProperties(0)
+    set_asides = [int(limit0)]
+    if err == rt.cudaError_t.cudaSuccess and err2 == rt.cudaError_t.cudaSuccess and prop.persistingL2CacheMaxSize > 0:
+        set_asides.append(int(prop.persistingL2CacheMaxSize))
+    with sampler:
+        for aside in set_asides:
+            rt.cudaDeviceSetLimit(rt.cudaLimit.cudaLimitPersistingL2CacheSize, aside)
+            rt.cudaCtxResetPersistingL2Cache()
+            for B in (1, 2, 4):
+                shape = moe.make_shape(B, d, F, moe.MOE_BF16)
+                for sname, x in xs.items():
+                    for L in (1, 32):
+                        S = n_steps[L]
+                        row = {"B": B, "stream": sname, "layers": L, "steps": S,
+                               "l2_set_aside_MB": round(aside / 2**20, 1)}
+                        for kmb in keep_mb:
+                            moe.moe_set_knob(moe.MOE_KNOB_L2_KEEP_KB, kmb * 1024)
+
+                            def run(s0, n):
+                                for s in range(s0, s0 + n):
+                                    for l in range(L):
+                                        w1, w3, w2 = weights[l]
+                                        moe.moe_layer_forward(shape, x[s, :B], wg, w1, w3, w2, y[:B], ws, None, stream)
+
+                            run(0, warm)
+                            torch.cuda.synchronize()
+                            a.record(stream)
+                            run(warm, S)
+                            b.record(stream)
+                            b.synchronize()
+                            row[f"us_per_layer_step_keep{kmb}MB"] = round(a.elapsed_time(b) * 1e3 / (S * L), 2)
+                        moe.moe_set_knob(moe.MOE_KNOB_L2_KEEP_KB, 0)
+                        t0 = row["us_per_layer_step_keep0MB"]
+                        row["best_gain"] = round(t0 / min(row[f"us_per_layer_step_keep{k}MB"] for k in keep_mb) - 1, 4)
+                        results.append(row)
+    rt.cudaCtxResetPersistingL2Cache()
+    rt.cudaDeviceSetLimit(rt.cudaLimit.cudaLimitPersistingL2CacheSize, int(limit0))
+    moe.moe_set_knob(moe.MOE_KNOB_L2_KEEP_KB, 0)
+    _device_status_ok(moe, "after the decode loop")
+    # experts touched per step on the locality stream (routing read once, outside the timed loops)
+    touched = {}
+    for B in (1, 2, 4):
+        shape = moe.make_shape(B, d, F, moe.MOE_BF16)
+        idx = torch.empty((B, 2), dtype=torch.int32, device="cuda")
+        gw = torch.empty((B, 2), dtype=torch.float32, device="cuda")
+        sets = []
+        for s in range(warm, warm + n_steps[1]):
+            moe.moe_route_top2(shape, xs["locality"][s, :B], wg, idx, gw)
+            sets.append(set(idx.flatten().tolist()))
+        touched[B] = {"experts_per_step": round(sum(len(t) for t in sets) / len(sets), 3),
+                      "reused_from_previous_step": round(sum(len(p & q) for p, q in zip(sets, sets[1:]))
+                                                         / max(1, len(sets) - 1), 3)}
+    return {"metric": "decode-time expert cache: microseconds per MoE-layer decode step", "unit": "us",
+            "config": {"workload": "mixtral_decode_stream", "d": d, "ffn": F, "E": E, "k": 2,
+                       "stream_rho": streams, "keep_MB": keep_mb,
+                       "locality_target": "62 % of consecutive tokens share an expert (lecture, layer 15)"},
+            "experts": touched, "results": results, "clocks": sampler.summary(),
+            "l2_set_aside_MB_tried": [round(v / 2**20, 1) for v in set_asides],
+            "note": "32 layers = 32 distinct copies of the expert weights (90 GB), each step runs every layer "
+                    "on the step's tokens; between two calls of one layer the other 31 stream 31 layers' weights"}
+
+
 def run_ep(args) -> dict:
     """Expert parallelism emulated on one GPU: the workload's tokens split over N ranks, each rank's
     expert FFNs timed, for the contiguous, the load-balanced and the replicated expert placement
@@ -954,6 +1057,9 @@ def main():
                     help="time one decode step of the Mixtral block (16 sequences, 4096-token caches)")
     ap.add_argument("--tile-ctas", type=int, default=0, choices=[0, 1, 2],
                     help="token tiles: automatic (0), single CTAs (1), CTA pairs (2)")
+    ap.add_argument("--decode-loop", action="store_true",
+                    help="decode-time expert cache experiment: a locality token stream through 1 or 32 layers "
+                         "with and without part of each call's expert weights kept in L2")
     ap.add_argument("--no-decode", action="store_true",
                     help="skip the decode batch that the default line carries beside the headline workload")
     args = ap.parse_args()
@@ -962,6 +1068,11 @@ def main():
     rank, world, local = _dist_env()
     if args.ep:
         print(json.dumps(run_ep(args)), flush=True)
+        return
+    if args.decode_loop:
+        if args.impl != "ours" or world != 1:
+            raise SystemExit("--decode-loop times this library's decode steps on one GPU")
+        print(json.dumps(run_decode_loop(args)), flush=True)
         return
     if args.block_decode:
         if args.impl != "ours" or world != 1:

@@ -427,6 +427,17 @@ moe_status moe_set_wait_timeout_ns(uint64_t ns);
  *                       (one tcgen05 MMA spans two SMs) above; 1 = single
  *                       CTAs; 2 = CTA pairs. The single-CTA kernel also
  *                       runs when no CTA pair fits.
+ *   MOE_KNOB_L2_KEEP_KB decode-time expert cache of the weight-streaming path
+ *                       (0 .. 131072 KiB; default 0 = off): about this many
+ *                       KiB of each call's expert weights are loaded with the
+ *                       L2 evict-last priority so that a following call that
+ *                       routes to the same experts finds them in L2 (the
+ *                       router's choices of consecutive tokens repeat more
+ *                       often than chance: "Mixtral of Experts" lecture,
+ *                       router walkthrough). The budget is spread evenly over
+ *                       the experts a call touches, each keeping the leading
+ *                       rows of W1, W3 (two thirds) and W2 (one third); the
+ *                       rest is loaded evict-first. Results do not change.
  *   MOE_KNOB_DEBUG      1 = debug mode: every launch is followed by a wait on
  *                       its stream and a look at the device status word, so a
  *                       device-side error (timeout, index check) is returned by
@@ -436,7 +447,7 @@ moe_status moe_set_wait_timeout_ns(uint64_t ns);
  * Environment, read when the library loads: MOE_DEBUG=1 starts in debug mode;
  * MOE_WAIT_TIMEOUT_NS sets the initial wait limit (as moe_set_wait_timeout_ns). */
 enum { MOE_KNOB_FFN_PATH = 1, MOE_KNOB_KSLICE = 2, MOE_KNOB_GRID = 3, MOE_KNOB_PDL = 4, MOE_KNOB_TILE_CTAS = 5,
-       MOE_KNOB_DEBUG = 6 };
+       MOE_KNOB_DEBUG = 6, MOE_KNOB_L2_KEEP_KB = 7 };
 moe_status moe_set_knob(int32_t knob, int64_t value);
 
 /* Per-kernel timing with CUDA events recorded on the launching stream.

@@ -16,6 +16,7 @@ from .gen import (  # noqa: F401
     make_layer,
     make_weights,
     make_tokens,
+    make_token_stream,
     redraw_token_row,
     load_schedule,
     to_f64,

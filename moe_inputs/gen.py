@@ -45,6 +45,7 @@ STREAM_ATTN_NORM = 8
 STREAM_WQKV = 9
 STREAM_WO = 10
 STREAM_FFN_NORM = 11
+STREAM_DECODE = 12
 
 SCHEDULE_PATH = Path(__file__).resolve().parent.parent / "tests" / "golden" / "input_schedule.json"
 
@@ -157,6 +158,25 @@ def make_tokens(T: int, d: int, E: int, dtype: str, seed: int,
             x[t] = redraw_token_row(seed, t, attempt, d, skew_c)
     wg = _gate_f32(seed, E, d, skew_c is not None)
     return _store(x, dtype), _store(wg, dtype)
+
+
+def make_token_stream(B: int, S: int, d: int, rho: float, seed: int, dtype: str = "bf16") -> torch.Tensor:
+    """Decode-time token stream: x [S][B][d], B independent sequences of S steps whose consecutive rows
+    are correlated, so that the router's choices of consecutive tokens repeat more often than chance.
+
+    Each sequence is a first-order autoregression in float64, rounded once to the stored type:
+    x_0 = z_0, x_s = rho * x_{s-1} + sqrt(1 - rho^2) * z_s with z ~ N(0, 1) i.i.d. (its own stream), so
+    every row is N(0, 1) like the layer workloads' tokens and the correlation of rows s and s+1 is rho
+    (rho = 0: independent tokens). The value of rho that matches the pages' locality figures is
+    decided by a calibration script under tests/golden; this function only draws.
+    """
+    z = normal_f32(seed, STREAM_DECODE, S * B * d, 1.0).reshape(S, B, d).astype(np.float64)
+    x = np.empty_like(z)
+    x[0] = z[0]
+    c = float(np.sqrt(max(0.0, 1.0 - rho * rho)))
+    for i in range(1, S):
+        x[i] = rho * x[i - 1] + c * z[i]
+    return _store(x.astype(np.float32), dtype)
 
 
 @dataclass

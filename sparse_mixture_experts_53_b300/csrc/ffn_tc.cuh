@@ -785,6 +785,10 @@ struct StreamArgs {
     uint32_t stage_bytes;
     uint64_t timeout_ns;
     int dense_rows;  // plain linear layer (offsets == nullptr, E == 1): one group of this many rows
+    // Weight bytes of this call that should stay in L2 for the next call (decode-time expert cache,
+    // 0 = none): spread evenly over the experts the call touches, each keeps the leading 128-row
+    // blocks of its matrices.
+    uint64_t keep_bytes;
 };
 
 inline size_t stream_smem_bytes(int nb, int stages) {
@@ -875,9 +879,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     if (warp == 0) {
         if (lane == 0) {
+            // Weights are read once per call: evict-first, except the leading row blocks that an expert
+            // cache keeps for the next call (the router's choices of consecutive tokens repeat more often
+            // than chance: lecture, router walkthrough), which are loaded with the evict-last priority.
             const uint64_t pol_w = policy_evict_first();
+            const uint64_t pol_keep = policy_evict_last();
             const uint64_t pol_x = policy_evict_last();
             const uint32_t x_bytes = (uint32_t)args.nb * 128u;
+            int keep_rb = 0;
+            if (args.keep_bytes > 0 && ctl->n_act > 0) {
+                const uint64_t blk = 128ull * (uint64_t)args.kslice * (uint64_t)S * 2ull;  // one row block of one matrix
+                const uint64_t per = args.keep_bytes / (blk * (uint64_t)ctl->n_act * (uint64_t)args.nmat);
+                keep_rb = (int)(per < (uint64_t)RB ? per : (uint64_t)RB);
+            }
             uint32_t s = 0, ph = 0;
             uint32_t issued_mask = 0, issued_ph = 0;
             bool ok = true;
@@ -897,7 +911,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const uint32_t sa = smem_u32(smem + (size_t)s * args.stage_bytes);
                     const int kx = ks * args.kslice + kb * kBK;
                     mbar_arrive_expect_tx(fb, kStreamABytes + x_bytes);
-                    tma_load_2d(sa, mw, fb, kx, wrow, pol_w);
+                    tma_load_2d(sa, mw, fb, kx, wrow, rb < keep_rb ? pol_keep : pol_w);
                     tma_load_2d(sa + kStreamABytes, &map_x, fb, kx, xrow, pol_x);
                     issued_mask |= 1u << s;
                     issued_ph = (issued_ph & ~(1u << s)) | (ph << s);

@@ -73,6 +73,7 @@ struct HostState {
     bool timing = false;
     bool pdl = true;           // programmatic dependent launch between the library's kernels
     int tile_ctas = 0;         // token tiles: 0 auto, 1 single CTAs, 2 CTA pairs
+    uint64_t l2_keep_bytes = 0;  // weight-streaming path: bytes per call kept in L2 for the next call
     int pair_cap[kMaxDevices][8] = {{0}};  // resident clusters per pair kernel (0 = not queried)
     std::vector<TimingRecord> records;
     std::vector<cudaEvent_t> pool;
@@ -630,6 +631,7 @@ moe_status run_ffn(const moe_shape& s, const void* x_perm, const int32_t* offset
     if (!ensure_smem(stream_gemm_kernel<true>, 4, kSmemBudget)) return MOE_ERR_CUDA;
     StreamArgs up{offsets, part_up, E, (int)R, L.ks_up, L.S_up, F / 128, 2, F, L.nb, stages, stage_bytes,
                   g.timeout_ns};
+    up.keep_bytes = g.l2_keep_bytes / 3 * 2;  // W1 and W3 hold two thirds of an expert's bytes
     MOE_TRY(launch("stream_up", st, [&] {
         return klaunch(stream_gemm_kernel<true>, grid_up, kTcThreads, smem, st, mw1, mw3, mx, up);
     }));
@@ -642,6 +644,7 @@ moe_status run_ffn(const moe_shape& s, const void* x_perm, const int32_t* offset
     if (!ensure_smem(stream_gemm_kernel<false>, 5, kSmemBudget)) return MOE_ERR_CUDA;
     StreamArgs down{offsets, part_down, E, (int)R, L.ks_down, L.S_down, d / 128, 1, d, L.nb, stages_down,
                     stage_bytes, g.timeout_ns};
+    down.keep_bytes = g.l2_keep_bytes / 3;
     MOE_TRY(launch("stream_down", st, [&] {
         return klaunch(stream_gemm_kernel<false>, grid_down, kTcThreads, smem_down, st, mw2, mw2, mh, down);
     }));
@@ -1639,6 +1642,10 @@ moe_status moe_set_knob(int32_t knob, int64_t value) {
         case MOE_KNOB_TILE_CTAS:
             if (value < 0 || value > 2) return MOE_ERR_INVALID_ARG;
             g.tile_ctas = (int)value;
+            return MOE_OK;
+        case MOE_KNOB_L2_KEEP_KB:
+            if (value < 0 || value > 128 * 1024) return MOE_ERR_INVALID_ARG;
+            g.l2_keep_bytes = (uint64_t)value * 1024u;
             return MOE_OK;
         case MOE_KNOB_DEBUG:
             if (value < 0 || value > 1) return MOE_ERR_INVALID_ARG;

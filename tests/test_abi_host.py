@@ -99,6 +99,10 @@ def test_knobs_and_timeouts():
     assert lib.moe_set_knob(moe.MOE_KNOB_TILE_CTAS, 4) == moe.MOE_ERR_INVALID_ARG
     assert lib.moe_set_knob(moe.MOE_KNOB_TILE_CTAS, 5) == moe.MOE_ERR_INVALID_ARG
     assert lib.moe_set_knob(moe.MOE_KNOB_PDL, 2) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_set_knob(moe.MOE_KNOB_L2_KEEP_KB, -1) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_set_knob(moe.MOE_KNOB_L2_KEEP_KB, 128 * 1024 + 1) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_set_knob(moe.MOE_KNOB_L2_KEEP_KB, 64 * 1024) == moe.MOE_OK
+    assert lib.moe_set_knob(moe.MOE_KNOB_L2_KEEP_KB, 0) == moe.MOE_OK
     assert lib.moe_set_wait_timeout_ns(0) == moe.MOE_ERR_INVALID_ARG
     try:
         moe.moe_set_knob(moe.MOE_KNOB_FFN_PATH, 2)
