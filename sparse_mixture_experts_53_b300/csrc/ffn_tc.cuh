@@ -112,6 +112,11 @@ struct TileArgs {
     int64_t out_estride;   // elements per expert in each gradient matrix
     // plain linear layer (pair kernel, PM_DOWN with offsets == nullptr): one group of this many rows
     int dense_rows;
+    // pair kernel: order of an expert's tiles. 0 = row tiles fastest: the tiles running at one time share
+    // a block of B, and all of the expert's A stays in L2 across B's blocks (right when A is the smaller
+    // operand); 1 = column tiles fastest: they share a block of A and all of B stays in L2 (right when B
+    // is the smaller one). The order does not change any tile's arithmetic.
+    int n_fast;
 };
 
 // Epilogue of one token tile for one thread (one row): reads the row's 256
@@ -588,8 +593,13 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         e = 0;
         while (e < E - 1 && tile >= ctl->base[e + 1]) ++e;
         const int rem = tile - ctl->base[e];
-        nt = rem / ctl->mt[e];
-        mt = rem - nt * ctl->mt[e];
+        if (args.n_fast) {
+            mt = rem / args.n_tiles_n;
+            nt = rem - mt * args.n_tiles_n;
+        } else {
+            nt = rem / ctl->mt[e];
+            mt = rem - nt * ctl->mt[e];
+        }
     };
     // K steps of a tile: fixed, or the expert's padded token count
     auto ksteps = [&](int e) { return WG ? (ctl->koff[e + 1] - ctl->koff[e]) / kBK : KB; };
