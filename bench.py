@@ -148,13 +148,20 @@ class ClockSampler:
 CSRC = ROOT / "sparse_mixture_experts_53_b300" / "csrc"
 
 
-def _source_digest() -> str:
-    """Digest of the kernels and their launch code (ncu figures go stale when any of it changes)."""
+# The sources that define each profiled kernel and its launch: its own file, the shared device helpers
+# and the launch code (ncu figures go stale when any of them changes, not when another kernel does).
+KERNEL_SOURCES = {
+    "tile_up_swiglu": ("ffn_tc.cuh", "common.cuh", "libmoe.cu"),
+    "tile_down_scale": ("ffn_tc.cuh", "common.cuh", "libmoe.cu"),
+    "stream_up": ("ffn_tc.cuh", "common.cuh", "libmoe.cu"),
+}
+
+
+def _source_digest(kernel: str) -> str:
     h = hashlib.sha256()
-    for f in sorted(CSRC.iterdir()):
-        if f.suffix in (".cu", ".cuh"):
-            h.update(f.name.encode())
-            h.update(f.read_bytes())
+    for name in KERNEL_SOURCES[kernel]:
+        h.update(name.encode())
+        h.update((CSRC / name).read_bytes())
     return h.hexdigest()[:16]
 
 
@@ -167,7 +174,7 @@ def _profile_traffic(kernel: str, workload: str):
         d = json.loads(f.read_text())
     except Exception:
         return None
-    if d.get("source_digest") != _source_digest():
+    if kernel not in KERNEL_SOURCES or d.get("source_digest") != _source_digest(kernel):
         return None
     return d.get("dram_bytes_per_launch")
 
