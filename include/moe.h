@@ -361,12 +361,13 @@ moe_status moe_attention(const moe_block_shape* s, const void* q, const void* k,
  * bf16 against the head-major caches ([B][n_kv_heads][cache_max][head_dim],
  * the token's own key and value already stored at position cache_len[b]),
  * cache_len[b] + 1 keys; o [B][n_heads head_dim] bf16. Splits each
- * sequence's keys over a few CTAs per KV head (each streams its share in
- * steps of 64 keys through shared memory by TMA, S = Q K^T and O += P V on
- * the tensor cores, a running softmax) and merges the partials; advances
- * cache_len[b] by one (up to cache_max). ws:
+ * sequence's keys over CTAs per KV head (each streams its share in steps of
+ * 128 keys through shared memory by TMA, S^T = K Q^T and O^T += V^T P^T on
+ * the tensor cores, a running softmax with one key per thread) and merges the
+ * partials; advances cache_len[b] by one (up to cache_max). Cache rows at or
+ * past a sequence's key count are never used, whatever they hold. ws:
  * moe_attention_decode_workspace_bytes. head_dim 128, n_heads / n_kv_heads
- * <= 32. */
+ * <= 16. */
 size_t moe_attention_decode_workspace_bytes(const moe_block_shape* s);
 moe_status moe_attention_decode(const moe_block_shape* s, const void* q, const void* k_cache, const void* v_cache,
                                 int32_t* cache_len, void* o, void* ws, size_t ws_bytes, void* stream);

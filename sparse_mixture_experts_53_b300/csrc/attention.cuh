@@ -693,40 +693,58 @@ __global__ void __launch_bounds__(kAttnPairThreads, 1)
 // Decode: one new token per sequence against its key/value cache. The cache
 // is head-major, [B][Hkv][cache_max][128] bf16, so a KV head's keys are one
 // contiguous run. CTA (split s, KV head, sequence) takes an equal share of the
-// n = len + 1 valid keys (the new token's were appended by the RoPE step), 64
-// keys per step, for the G query heads that share the KV head:
-//   S = Q K^T     tcgen05.mma M = 128 (rows 0 .. G-1 are the heads; the other
-//                 rows are not read), N = 64 keys, K = 128 channels; Q held in
-//                 tensor memory (A operand), K by TMA (128-byte swizzle), S in
-//                 tensor memory
-//   softmax       warp 0, one row per lane: running maximum and sum, O
-//                 rescaled in place when the maximum grows, P (bf16) written
-//                 over S
-//   O += P V      tcgen05.mma M = 128, N = 128 channels, K = 64 keys, P from
-//                 tensor memory, V as stored (MN-major)
-// Keys and values stream through three shared-memory stages, so the tensor
-// core only waits on HBM. Each CTA writes one unnormalised partial (O, m, l) per
-// head; a second kernel merges the splits in order (flash decoding).
+// n = len + 1 valid keys (the new token's were appended by the RoPE step), 128
+// keys per step, for the G <= 16 query heads that share the KV head. The keys
+// sit on the MMA's 128-row side and the G heads on its N = 16 side, so the
+// softmax runs one key per thread and computes only G exponentials per key:
+//   S^T = K Q^T     tcgen05.mma M = 128 keys, N = 16 (heads G .. 15 are zero
+//                   rows of Q), K = 128 channels; K by TMA (128-byte swizzle,
+//                   K-major), Q K-major in shared memory; S^T in tensor
+//                   memory, two buffers, so the scores of step i + 1 are
+//                   computed while the softmax of step i runs
+//   softmax         warps 0-3, thread t = key t of the step: each head's
+//                   maximum over the 128 keys (warp butterflies, then the four
+//                   warps' values through shared memory behind a bounded
+//                   mbarrier wait), p = 2^(s - m), a per-thread partial sum
+//                   rescaled with the running maximum; P^T (bf16, heads x
+//                   keys, K-major) into shared memory, two buffers
+//   O^T += V^T P^T  M = 128 channels, N = 16 heads, K = 128 keys: V read as
+//                   stored ([key][channel] is the MN-major A), O^T in tensor
+//                   memory (16 columns), rescaled in place when a maximum grows
+// Keys and values stream through three 64 KB stages. Key rows past the valid
+// ones in the last step are masked (score -inf) and their value rows are
+// zeroed in shared memory before P V, so whatever the cache holds past its
+// length cannot reach the result. Each CTA writes one unnormalised partial
+// (O, m, l) per head; a second kernel merges the splits in order (flash
+// decoding).
 // ---------------------------------------------------------------------------
-constexpr int kDecChunk = 64;                        // keys per step
-constexpr int kDecThreads = 96;                      // warp 0 softmax, warp 1 TMA, warp 2 MMA
-constexpr int kDecMaxGroup = 32;                     // query heads per KV head (one row per lane)
-constexpr int kDecCtasPerSm = 2;
+constexpr int kDecChunk = 128;                       // keys per step
+constexpr int kDecN = 16;                            // MMA N: the group's query heads, zero-padded
+constexpr int kDecThreads = 192;                     // warps 0-3 softmax, warp 4 TMA, warp 5 MMA
+constexpr int kDecMaxGroup = kDecN;                  // query heads per KV head
+constexpr int kDecCtasPerSm = 1;
 constexpr int kDecStages = 3;
-constexpr uint32_t kDecBox = 64 * 64 * 2;            // 8 KB: 64 keys x 64 channels
+constexpr uint32_t kDecBox = 128 * 64 * 2;           // 16 KB: 128 keys x 64 channels
 constexpr uint32_t kDecStageBytes = 4 * kDecBox;     // keys (two boxes) + values (two boxes)
+constexpr uint32_t kDecQBytes = 2 * kDecN * 128;     // Q: two 64-channel blocks of 16 rows x 128 bytes
+constexpr uint32_t kDecPBytes = 2 * kDecN * 128;     // one P^T buffer: two 64-key blocks of 16 rows
 
 struct DecControl {
     uint64_t q_ready;
     uint64_t kv_full[kDecStages];
     uint64_t kv_empty[kDecStages];
-    uint64_t s_full, p_full, o_full, drain;
+    uint64_t s_full[2], p_full[2], red_full[2], o_ready[2];
+    uint64_t o_full, fin_full, drain;
+    float red[2][4][kDecN];                          // per step parity, per softmax warp, per head
+    float fin[4][kDecN];
     uint32_t tmem_base;
     int abort_flag;
 };
 
-// stages | control
-constexpr size_t kDecSmemBytes = 1024 + (size_t)kDecStages * kDecStageBytes + sizeof(DecControl);
+// stages | Q | P^T x 2 | control
+constexpr size_t kDecSmemBytes =
+    1024 + (size_t)kDecStages * kDecStageBytes + kDecQBytes + 2 * (size_t)kDecPBytes + sizeof(DecControl);
+static_assert(kDecSmemBytes <= 227 * 1024, "decode attention CTA exceeds the shared memory of a CTA");
 
 struct DecodeArgs {
     const __nv_bfloat16* q;       // [B][Hq hd]
@@ -744,14 +762,23 @@ __device__ __forceinline__ void dec_abort(DecControl* c, int where) {
     *reinterpret_cast<volatile int*>(&c->abort_flag) = 1;
 }
 
+// Bounded wait on an mbarrier by a whole warp; true when every lane saw the phase complete.
+__device__ __forceinline__ bool dec_wait_warp(uint32_t bar, uint32_t parity, uint64_t tmo, volatile int* abort_flag) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, tmo, abort_flag));
+}
+
 // map_k, map_v: the caches viewed as [B Hkv cache_max][128], boxes of 64
-// channels x 64 keys.
+// channels x 128 keys. GP: the group size rounded up to a power of two
+// (1 .. 16); the softmax's per-head loops run GP times, heads G .. GP-1 are
+// zero rows of Q whose results are dropped.
+template <int GP>
 __global__ void __launch_bounds__(kDecThreads, 1)
     attention_decode_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
                             const DecodeArgs a) {
     extern __shared__ unsigned char dec_smem_raw[];
     unsigned char* smem = align1024(dec_smem_raw);
-    DecControl* ctl = reinterpret_cast<DecControl*>(smem + (size_t)kDecStages * kDecStageBytes);
+    DecControl* ctl = reinterpret_cast<DecControl*>(smem + (size_t)kDecStages * kDecStageBytes + kDecQBytes +
+                                                    2 * (size_t)kDecPBytes);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const uint64_t tmo = a.timeout_ns;
@@ -761,25 +788,32 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     const uint32_t sbase = smem_u32(smem);
     auto sK = [&](int st) { return sbase + (uint32_t)st * kDecStageBytes; };
     auto sV = [&](int st) { return sK(st) + 2 * kDecBox; };
+    const uint32_t sQ = sbase + kDecStages * kDecStageBytes;
+    auto sP = [&](int buf) { return sQ + kDecQBytes + (uint32_t)buf * kDecPBytes; };
 
     if (threadIdx.x == 0) {
-        mbar_init(smem_u32(&ctl->q_ready), 1);
+        mbar_init(smem_u32(&ctl->q_ready), 4);
         for (int s = 0; s < kDecStages; ++s) {
             mbar_init(smem_u32(&ctl->kv_full[s]), 1);
             mbar_init(smem_u32(&ctl->kv_empty[s]), 1);
         }
-        mbar_init(smem_u32(&ctl->s_full), 1);
-        mbar_init(smem_u32(&ctl->p_full), 1);
+        for (int p = 0; p < 2; ++p) {
+            mbar_init(smem_u32(&ctl->s_full[p]), 1);
+            mbar_init(smem_u32(&ctl->p_full[p]), 4);
+            mbar_init(smem_u32(&ctl->red_full[p]), 4);
+            mbar_init(smem_u32(&ctl->o_ready[p]), 1);
+        }
         mbar_init(smem_u32(&ctl->o_full), 1);
+        mbar_init(smem_u32(&ctl->fin_full), 4);
         mbar_init(smem_u32(&ctl->drain), 1);
         ctl->abort_flag = 0;
         fence_mbar_init();
     }
     if (warp == 0) {
-        tmem_alloc(smem_u32(&ctl->tmem_base), 256);
+        tmem_alloc(smem_u32(&ctl->tmem_base), 64);
         tmem_relinquish();
     }
-    if (warp == 1 && lane == 0) {
+    if (warp == 4 && lane == 0) {
         tma_prefetch_desc(&map_k);
         tma_prefetch_desc(&map_v);
     }
@@ -788,9 +822,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tS = ctl->tmem_base;         // columns 0-63: scores (P over columns 0-31)
-    const uint32_t tQ = ctl->tmem_base + 64;    // columns 64-127: the queries, two bf16 per column
-    const uint32_t tO = ctl->tmem_base + 128;   // columns 128-255: output accumulator
+    const uint32_t tS = ctl->tmem_base;          // columns 0-15 and 16-31: S^T of even and odd steps
+    const uint32_t tO = ctl->tmem_base + 32;     // columns 32-47: O^T
 
     const int64_t n_all = (int64_t)a.len[b] + 1;
     const int64_t n = n_all < a.cache_max ? n_all : a.cache_max;
@@ -801,7 +834,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     const int steps = c_end > c_begin ? (int)(c_end - c_begin) : 0;
     const int64_t row0 = ((int64_t)b * a.Hkv + kvh) * a.cache_max;
 
-    if (warp == 1) {
+    if (warp == 4) {
         // ------------------------------------------------------------ TMA
         if (lane == 0 && steps > 0) {
             const uint64_t pol = policy_evict_first();
@@ -827,43 +860,61 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                 if (issued & (1u << st)) drain_wait(smem_u32(&ctl->kv_full[st]), (issued_ph >> st) & 1u, tmo, K_ATTN);
         }
         __syncwarp();
-    } else if (warp == 2) {
+    } else if (warp == 5) {
         // ------------------------------------------------------------ MMA
         if (lane == 0 && steps > 0) {
-            constexpr uint32_t idesc_s = idesc_bf16_f32(128, kDecChunk);
-            constexpr uint32_t idesc_o = idesc_bf16_f32(128, 128, false, true);
+            constexpr uint32_t idesc_s = idesc_bf16_f32(128, kDecN);
+            constexpr uint32_t idesc_o = idesc_bf16_f32(128, kDecN, true, false);
             bool ok = mbar_wait(smem_u32(&ctl->q_ready), 0, tmo, abort_flag);
             if (!ok) dec_abort(ctl, W_MMA);
             bool any = false;
+            // O^T += V^T P^T of step j, once the softmax has written P^T_j
+            auto pv = [&](int j) -> bool {
+                if (!mbar_wait(smem_u32(&ctl->p_full[j & 1]), (uint32_t)(j >> 1) & 1u, tmo, abort_flag)) return false;
+                tc_fence_after();
+                const int st = j % kDecStages;
+#pragma unroll
+                for (int kk = 0; kk < kDecChunk / 16; ++kk) {
+                    const uint64_t ad = sw128_mnmajor_desc(sV(st), kDecBox) + 128ull * kk;
+                    const uint64_t bd = sw128_kmajor_desc(sP(j & 1) + (uint32_t)(kk >> 2) * (kDecN * 128)) +
+                                        2ull * (kk & 3);
+                    mma_bf16(tO, ad, bd, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+                }
+                mma_commit(smem_u32(&ctl->kv_empty[st]));
+                mma_commit(smem_u32(&ctl->o_ready[j & 1]));
+                return true;
+            };
             for (int i = 0; ok && i < steps; ++i) {
                 const int st = i % kDecStages;
                 if (!mbar_wait(smem_u32(&ctl->kv_full[st]), (uint32_t)(i / kDecStages) & 1u, tmo, abort_flag)) {
                     dec_abort(ctl, W_MMA);
+                    ok = false;
                     break;
                 }
                 tc_fence_after();
-                // S = Q K^T (issued after the previous P V, which read P from these columns)
+                // S^T_i = K_i Q^T into buffer i & 1 (its scores of step i - 2 were read before P^T_{i-2},
+                // whose P V was issued before this)
 #pragma unroll
                 for (int kk = 0; kk < kAttnHD / 16; ++kk) {
-                    const uint32_t off = (uint32_t)(kk >> 2);
-                    const uint64_t bd = sw128_kmajor_desc(sK(st) + off * kDecBox) + 2ull * (kk & 3);
-                    mma_bf16_ts(tS, tQ + 8u * (uint32_t)kk, bd, idesc_s, kk > 0);
+                    const uint32_t blk = (uint32_t)(kk >> 2);
+                    const uint64_t ad = sw128_kmajor_desc(sK(st) + blk * kDecBox) + 2ull * (kk & 3);
+                    const uint64_t bd = sw128_kmajor_desc(sQ + blk * (kDecN * 128)) + 2ull * (kk & 3);
+                    mma_bf16(tS + kDecN * (uint32_t)(i & 1), ad, bd, idesc_s, kk > 0);
                 }
                 any = true;
-                mma_commit(smem_u32(&ctl->s_full));
-                if (!mbar_wait(smem_u32(&ctl->p_full), (uint32_t)i & 1u, tmo, abort_flag)) {
+                mma_commit(smem_u32(&ctl->s_full[i & 1]));
+                if (i > 0 && !pv(i - 1)) {
                     dec_abort(ctl, W_MMA);
+                    ok = false;
                     break;
                 }
-                tc_fence_after();
-                // O += P V
-#pragma unroll
-                for (int kk = 0; kk < kDecChunk / 16; ++kk) {
-                    const uint64_t bd = sw128_mnmajor_desc(sV(st), kDecBox) + 128ull * kk;
-                    mma_bf16_ts(tO, tS + 8u * (uint32_t)kk, bd, idesc_o, (i > 0 || kk > 0) ? 1u : 0u);
+            }
+            if (ok) {
+                if (pv(steps - 1)) {
+                    mma_commit(smem_u32(&ctl->o_full));
+                } else {
+                    dec_abort(ctl, W_MMA);
                 }
-                mma_commit(smem_u32(&ctl->kv_empty[st]));
-                if (i + 1 == steps) mma_commit(smem_u32(&ctl->o_full));
             }
             if (any) {
                 mma_commit(smem_u32(&ctl->drain));
@@ -872,116 +923,182 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------------------ softmax + partial (warp 0: lanes = rows)
-        const int row = lane;
+        // ------------------------------------------------------------ softmax + partial (warps 0-3: t = key / channel)
+        const int t = threadIdx.x;                               // 0 .. 127
+        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;   // this warp's tensor-memory lane quarter
         const float sl2 = a.scale_log2;
-        float m_run = -INFINITY, l_run = 0.f;
+        float m_run[GP], l_part[GP];
+#pragma unroll
+        for (int h = 0; h < GP; ++h) {
+            m_run[h] = -INFINITY;
+            l_part[h] = 0.f;
+        }
         bool ok = true;
         if (steps > 0) {
-            // the group's queries into tensor memory, one head per lane (rows G .. 31 zero)
-            const uint4* qr = reinterpret_cast<const uint4*>(a.q + ((int64_t)b * a.Hq + kvh * G + row) * kAttnHD);
+            // Q (the group's heads, zero rows past G) and both P^T buffers (rows past G stay zero) into
+            // shared memory, K-major in the 128-byte swizzle: thread t writes row t / 8, 16-byte chunk t % 8
+            // of both 64-channel blocks, and zeroes the same chunks of both P^T buffers
+            const int hq = t >> 3, c = t & 7;
+            const uint32_t off = (uint32_t)hq * 128u + ((uint32_t)(c ^ (hq & 7)) << 4);
+            const uint4* qr = reinterpret_cast<const uint4*>(a.q + ((int64_t)b * a.Hq + kvh * G + hq) * kAttnHD);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t w[16];
+            for (int blk = 0; blk < 2; ++blk) {
+                const uint4 u = hq < G ? qr[blk * 8 + c] : make_uint4(0u, 0u, 0u, 0u);
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sQ + blk * (kDecN * 128) + off),
+                             "r"(u.x), "r"(u.y), "r"(u.z), "r"(u.w)
+                             : "memory");
 #pragma unroll
-                for (int v4 = 0; v4 < 4; ++v4) {
-                    const uint4 u = row < G ? qr[4 * c + v4] : make_uint4(0u, 0u, 0u, 0u);
-                    w[4 * v4] = u.x;
-                    w[4 * v4 + 1] = u.y;
-                    w[4 * v4 + 2] = u.z;
-                    w[4 * v4 + 3] = u.w;
-                }
-                tmem_st16(tQ + 16 * c, w);
+                for (int pb = 0; pb < 2; ++pb)
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(sP(pb) + blk * (kDecN * 128) + off),
+                                 "r"(0u)
+                                 : "memory");
             }
-            tmem_wait_st();
-            tc_fence_before();
+            fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&ctl->q_ready));
         }
         for (int i = 0; i < steps; ++i) {
-            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->s_full), (uint32_t)i & 1u, tmo, abort_flag))) {
+            const int par = i & 1;
+            if (!dec_wait_warp(smem_u32(&ctl->s_full[par]), (uint32_t)(i >> 1) & 1u, tmo, abort_flag)) {
                 dec_abort(ctl, W_EPILOGUE);
                 ok = false;
                 break;
             }
             tc_fence_after();
-            uint32_t sv[kDecChunk];
-            tmem_ld32(tS, &sv[0]);
-            tmem_ld32(tS + 32, &sv[32]);
+            uint32_t sv[kDecN];
+            tmem_ld16(tS + kDecN * (uint32_t)par + lane_off, sv);
             tmem_wait_ld();
-            const int64_t k0 = (c_begin + i) * kDecChunk;
-            float mx = -INFINITY;
+            const int64_t key = (c_begin + i) * kDecChunk + t;
+            const bool valid = key < n;
+            float sc[GP], wmax[GP];
 #pragma unroll
-            for (int c = 0; c < kDecChunk; ++c) {
-                if (k0 + c >= n) sv[c] = __float_as_uint(-INFINITY);
-                mx = fmaxf(mx, __uint_as_float(sv[c]));
+            for (int h = 0; h < GP; ++h) {
+                sc[h] = valid ? __uint_as_float(sv[h]) * sl2 : -INFINITY;
+                wmax[h] = sc[h];
             }
-            const float m_new = fmaxf(m_run, mx * sl2);
-            const float m_use = m_new == -INFINITY ? 0.f : m_new;
-            const float alpha = m_run == -INFINITY ? 0.f : fast_exp2(m_run - m_use);
-            if (i > 0 && __any_sync(0xffffffffu, alpha < 1.f)) {
-                // O holds P_{i-1} V_{i-1} (the MMA that wrote S_i ran after it): rescale it in place
-#pragma unroll 1
-                for (int c = 0; c < 8; ++c) {
-                    uint32_t o[16];
-                    tmem_ld16(tO + 16 * c, o);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+                for (int h = 0; h < GP; ++h) wmax[h] = fmaxf(wmax[h], __shfl_xor_sync(0xffffffffu, wmax[h], o));
+            if (lane == 0) {
+#pragma unroll
+                for (int h = 0; h < GP; ++h) ctl->red[par][warp][h] = wmax[h];
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&ctl->red_full[par]));
+            if (!dec_wait_warp(smem_u32(&ctl->red_full[par]), (uint32_t)(i >> 1) & 1u, tmo, abort_flag)) {
+                dec_abort(ctl, W_EPILOGUE);
+                ok = false;
+                break;
+            }
+            if (i >= 2) {
+                // P V of step i - 2 has finished reading this P^T buffer
+                if (!dec_wait_warp(smem_u32(&ctl->o_ready[par]), (uint32_t)((i - 2) >> 1) & 1u, tmo, abort_flag)) {
+                    dec_abort(ctl, W_EPILOGUE);
+                    ok = false;
+                    break;
+                }
+            }
+            float alpha[GP];
+            bool grow = false;
+            // P^T[h][t]: block t / 64, row h, 16-byte chunk (t % 64) / 8 swizzled by h % 8
+            const uint32_t prow = sP(par) + (uint32_t)(t >> 6) * (kDecN * 128) + (uint32_t)(t & 7) * 2u;
+            const uint32_t pchunk = (uint32_t)((t & 63) >> 3);
+#pragma unroll
+            for (int h = 0; h < GP; ++h) {
+                const float mc = fmax3f(fmaxf(ctl->red[par][0][h], ctl->red[par][1][h]), ctl->red[par][2][h],
+                                        ctl->red[par][3][h]);
+                const float m_new = fmaxf(m_run[h], mc);
+                const float m_use = m_new == -INFINITY ? 0.f : m_new;
+                alpha[h] = m_run[h] == -INFINITY ? 0.f : fast_exp2(m_run[h] - m_use);
+                grow |= alpha[h] < 1.f;
+                const float p = fast_exp2(sc[h] - m_use);
+                l_part[h] = fmaf(l_part[h], alpha[h], p);
+                m_run[h] = m_new;
+                const uint32_t addr = prow + (uint32_t)h * 128u + ((pchunk ^ (uint32_t)(h & 7)) << 4);
+                const __nv_bfloat16 pb = __float2bfloat16_rn(p);
+                asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"(*reinterpret_cast<const uint16_t*>(&pb))
+                             : "memory");
+            }
+            if (!valid) {
+                // the value row of a key past the valid ones is zeroed, so it cannot reach O
+                const uint32_t vrow = sV((int)(i % kDecStages)) + (uint32_t)t * 128u;
+#pragma unroll
+                for (int blk = 0; blk < 2; ++blk)
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(vrow + blk * kDecBox + q * 16u),
+                                     "r"(0u)
+                                     : "memory");
+            }
+            if (i > 0 && grow) {
+                // a maximum grew: once P V of the previous step has finished with O, rescale O in place
+                // (with no growth O needs no change, and P V of this step may follow the previous one at once)
+                if (!dec_wait_warp(smem_u32(&ctl->o_ready[par ^ 1]), (uint32_t)((i - 1) >> 1) & 1u, tmo,
+                                   abort_flag)) {
+                    dec_abort(ctl, W_EPILOGUE);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                {
+                    uint32_t o[kDecN];
+                    tmem_ld16(tO + lane_off, o);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int q = 0; q < 16; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * alpha);
-                    tmem_st16(tO + 16 * c, o);
+                    for (int h = 0; h < GP; ++h) o[h] = __float_as_uint(__uint_as_float(o[h]) * alpha[h]);
+                    tmem_st16(tO + lane_off, o);
+                    tmem_wait_st();
                 }
             }
-            float sum = 0.f;
-            uint32_t pk[kDecChunk / 2];
-#pragma unroll
-            for (int c = 0; c < kDecChunk / 2; ++c) {
-                const float p0 = fast_exp2(fmaf(__uint_as_float(sv[2 * c]), sl2, -m_use));
-                const float p1 = fast_exp2(fmaf(__uint_as_float(sv[2 * c + 1]), sl2, -m_use));
-                sum += p0 + p1;
-                pk[c] = pack_bf16x2(p0, p1);
-            }
-            l_run = l_run * alpha + sum;
-            m_run = m_new;
-            tmem_st16(tS, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
-            tmem_st16(tS + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
-            tmem_wait_st();
+            fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&ctl->p_full));
+            if (lane == 0) mbar_arrive(smem_u32(&ctl->p_full[par]));
         }
-        const int64_t part = ((int64_t)b * a.Hq + kvh * G + row) * a.splits + split;
-        if (ok && steps > 0 &&
-            __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->o_full), 0, tmo, abort_flag))) {
-            tc_fence_after();
-#pragma unroll 1
-            for (int c = 0; c < 8; ++c) {
-                uint32_t o[16];
-                tmem_ld16(tO + 16 * c, o);
-                tmem_wait_ld();
-                if (row < G) {
-                    float4* dst = reinterpret_cast<float4*>(a.part_o + part * kAttnHD + 16 * c);
+        // each head's sum over the keys: the threads' partial sums, warp by warp, then the four warps
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        dst[q] = make_float4(__uint_as_float(o[4 * q]), __uint_as_float(o[4 * q + 1]),
-                                             __uint_as_float(o[4 * q + 2]), __uint_as_float(o[4 * q + 3]));
-                }
-            }
-        } else if (ok && steps > 0) {
-            dec_abort(ctl, W_EPILOGUE);
-        } else if (steps == 0 && row < G) {
-            // no keys for this split: an empty partial
-            for (int c = 0; c < kAttnHD; c += 4)
-                *reinterpret_cast<float4*>(a.part_o + part * kAttnHD + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+            for (int h = 0; h < GP; ++h) l_part[h] += __shfl_xor_sync(0xffffffffu, l_part[h], o);
+        if (lane == 0) {
+#pragma unroll
+            for (int h = 0; h < GP; ++h) ctl->fin[warp][h] = l_part[h];
         }
-        if (row < G) {
-            a.part_ml[2 * part] = m_run;
-            a.part_ml[2 * part + 1] = l_run;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&ctl->fin_full));
+        const bool fin_ok = dec_wait_warp(smem_u32(&ctl->fin_full), 0, tmo, abort_flag);
+        const int64_t part0 = ((int64_t)b * a.Hq + kvh * G) * a.splits + split;
+        if (ok && fin_ok && steps > 0 && dec_wait_warp(smem_u32(&ctl->o_full), 0, tmo, abort_flag)) {
+            tc_fence_after();
+            uint32_t o[kDecN];
+            tmem_ld16(tO + lane_off, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int h = 0; h < GP; ++h)
+                if (h < G) a.part_o[(part0 + (int64_t)h * a.splits) * kAttnHD + t] = __uint_as_float(o[h]);
+        } else if (steps > 0) {
+            dec_abort(ctl, W_EPILOGUE);
+        } else {
+            // no keys for this split: an empty partial
+#pragma unroll
+            for (int h = 0; h < GP; ++h)
+                if (h < G) a.part_o[(part0 + (int64_t)h * a.splits) * kAttnHD + t] = 0.f;
+        }
+        if (t < G) {
+            const float l = fin_ok ? ctl->fin[0][t] + ctl->fin[1][t] + ctl->fin[2][t] + ctl->fin[3][t] : 0.f;
+            float m = -INFINITY;
+#pragma unroll
+            for (int h = 0; h < GP; ++h)
+                if (h == t) m = m_run[h];
+            a.part_ml[2 * (part0 + (int64_t)t * a.splits)] = m;
+            a.part_ml[2 * (part0 + (int64_t)t * a.splits) + 1] = l;
         }
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 0) tmem_dealloc(ctl->tmem_base, 256);
+    if (warp == 0) tmem_dealloc(ctl->tmem_base, 64);
 }
 
 // out[b][h] = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c over the splits c

@@ -78,7 +78,7 @@ struct HostState {
     std::vector<TimingRecord> records;
     std::vector<cudaEvent_t> pool;
     int sms[kMaxDevices] = {0};
-    bool attr_set[kMaxDevices][16] = {{false}};
+    bool attr_set[kMaxDevices][32] = {{false}};
 };
 HostState g;
 
@@ -1108,7 +1108,6 @@ moe_status run_attention_decode(const moe_block_shape& s, const void* q, const v
     const uint64_t cache_rows = (uint64_t)s.B * s.n_kv_heads * s.cache_max;
     if (!make_map(&mk, kc, kAttnHD, cache_rows, kDecChunk) || !make_map(&mv, vc, kAttnHD, cache_rows, kDecChunk))
         return MOE_ERR_CUDA;
-    (void)group;
     DecodeArgs a{};
     a.q = static_cast<const __nv_bfloat16*>(q);
     a.len = len;
@@ -1120,10 +1119,18 @@ moe_status run_attention_decode(const moe_block_shape& s, const void* q, const v
     a.splits = splits;
     a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)s.head_dim));
     a.timeout_ns = g.timeout_ns;
-    if (!ensure_smem(attention_decode_kernel, 15, kDecSmemBytes)) return MOE_ERR_CUDA;
+    // the softmax's per-head loops are unrolled for the group size rounded up to a power of two
+    const int gp = group <= 1 ? 1 : group <= 2 ? 2 : group <= 4 ? 4 : group <= 8 ? 8 : 16;
+    auto kern = gp == 1 ? attention_decode_kernel<1>
+                : gp == 2 ? attention_decode_kernel<2>
+                : gp == 4 ? attention_decode_kernel<4>
+                : gp == 8 ? attention_decode_kernel<8>
+                          : attention_decode_kernel<16>;
+    const int slot = gp == 1 ? 20 : gp == 2 ? 21 : gp == 4 ? 22 : gp == 8 ? 23 : 24;
+    if (!ensure_smem(kern, slot, kDecSmemBytes)) return MOE_ERR_CUDA;
     MOE_TRY(launch("attention_decode", st, [&] {
-        return klaunch(attention_decode_kernel, dim3((unsigned)splits, (unsigned)s.n_kv_heads, (unsigned)s.B),
-                       dim3(kDecThreads), kDecSmemBytes, st, mk, mv, a);
+        return klaunch(kern, dim3((unsigned)splits, (unsigned)s.n_kv_heads, (unsigned)s.B), dim3(kDecThreads),
+                       kDecSmemBytes, st, mk, mv, a);
     }));
     return launch("attention_decode_merge", st, [&] {
         return klaunch(attention_decode_merge_kernel, dim3((unsigned)s.n_heads, (unsigned)s.B), dim3(kAttnHD), 0, st,

@@ -195,9 +195,9 @@ def test_block_decode_validation_codes():
     assert call(_block(S=1, B=16, cache_max=0)) == moe.MOE_ERR_INVALID_ARG       # no cache
     assert call(dec, cache_len=None) == moe.MOE_ERR_INVALID_ARG
     assert call(dec, ws_bytes=n - 1) == moe.MOE_ERR_WORKSPACE
-    # the decode attention keeps one query head per lane of its softmax warp: up to 32 per KV head
-    assert moe.moe_block_decode_workspace_bytes(_block(S=1, n_heads=64, n_kv_heads=1, cache_max=64)) == 0
-    assert moe.moe_block_decode_workspace_bytes(_block(S=1, n_heads=32, n_kv_heads=1, cache_max=64)) > 0
+    # the decode attention takes up to 16 query heads per KV head
+    assert moe.moe_block_decode_workspace_bytes(_block(S=1, n_heads=32, n_kv_heads=1, cache_max=64)) == 0
+    assert moe.moe_block_decode_workspace_bytes(_block(S=1, n_heads=16, n_kv_heads=1, cache_max=64)) > 0
     assert moe.moe_block_decode_workspace_bytes(_block(S=1, n_heads=24, n_kv_heads=8, cache_max=64)) > 0
     # one partial (128 channels, maximum, sum) per query head and split; splits fill the SMs once
     att = moe.moe_attention_decode_workspace_bytes(dec)

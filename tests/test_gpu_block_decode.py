@@ -82,7 +82,8 @@ def test_rope_split_writes_the_caches_at_their_positions():
 
 @pytest.mark.parametrize("lens,Hq,Hkv,cmax", [((0, 1, 255, 256, 700), 32, 8, 1000), ((4095,), 8, 2, 4096),
                                                ((10, 300), 4, 4, 333), ((127, 128, 129), 16, 8, 300),
-                                               ((50, 999), 16, 2, 1000)])
+                                               ((50, 999), 16, 2, 1000), ((3, 2000), 32, 2, 2048),
+                                               tuple([tuple(range(0, 3200, 100)), 8, 8, 3300])])
 def test_attention_decode_on_ragged_caches(lens, Hq, Hkv, cmax):
     B = len(lens)
     s = moe.make_block_shape(B, 1, 256, Hq, Hkv, 256, cache_max=cmax)
@@ -103,6 +104,38 @@ def test_attention_decode_on_ragged_caches(lens, Hq, Hkv, cmax):
         keys = to_f64(kc[b, :, :n + 1].permute(1, 0, 2))
         vals = to_f64(vc[b, :, :n + 1].permute(1, 0, 2))
         ref = oracle.attention_one_query(to_f64(q[b]).reshape(Hq, HD), keys, vals)
+        assert np.max(np.abs(out[b] - ref)) <= 1e-2 * np.max(np.abs(ref)), (b, n)
+
+
+def test_attention_decode_ignores_what_the_cache_holds_past_its_length():
+    """Cache rows past a sequence's keys (never written: here NaN and Inf) must not reach the output;
+    the result equals the one with zeros there, bit for bit, and the oracle's."""
+    lens, Hq, Hkv, cmax = (5, 130, 255), 8, 2, 384
+    B = len(lens)
+    s = moe.make_block_shape(B, 1, 256, Hq, Hkv, 256, cache_max=cmax)
+    g = _gen(31)
+    q = torch.randn((B, Hq * HD), generator=g).to(torch.bfloat16).cuda()
+    kc = torch.randn((B, Hkv, cmax, HD), generator=g).to(torch.bfloat16)
+    vc = torch.randn((B, Hkv, cmax, HD), generator=g).to(torch.bfloat16)
+    outs = []
+    for fill in (0.0, float("nan"), float("inf")):
+        k2, v2 = kc.clone(), vc.clone()
+        for b, n in enumerate(lens):
+            k2[b, :, n + 1:] = fill
+            v2[b, :, n + 1:] = fill
+        ws = torch.empty(moe.moe_attention_decode_workspace_bytes(s), dtype=torch.uint8, device="cuda")
+        o = torch.empty((B, Hq * HD), dtype=torch.bfloat16, device="cuda")
+        moe.moe_attention_decode(s, q, k2.cuda(), v2.cuda(), torch.tensor(lens, dtype=torch.int32).cuda(), o, ws)
+        torch.cuda.synchronize()
+        assert_status_ok()
+        outs.append(o.cpu())
+    assert torch.isfinite(outs[0].float()).all()
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+    out = to_f64(outs[0]).reshape(B, Hq, HD)
+    for b, n in enumerate(lens):
+        keys = to_f64(kc[b, :, :n + 1].permute(1, 0, 2))
+        vals = to_f64(vc[b, :, :n + 1].permute(1, 0, 2))
+        ref = oracle.attention_one_query(to_f64(q[b].cpu()).reshape(Hq, HD), keys, vals)
         assert np.max(np.abs(out[b] - ref)) <= 1e-2 * np.max(np.abs(ref)), (b, n)
 
 
