@@ -129,31 +129,40 @@ __global__ void __launch_bounds__(256)
 
 // Load-balancing statistics (tokentrails.org "Mixtral", step "Load balancing"):
 // f_i = counts_i / (2T), P_i = mean_t softmax(l_t)_i over all E scores,
-// L_aux = E * sum_i f_i P_i. One CTA; fixed-order tree reduction.
+// L_aux = E * sum_i f_i P_i. One cluster of kAuxCtas CTAs: CTA r takes the
+// r-th of kAuxCtas equal blocks of tokens and reduces its softmax rows in a
+// fixed order (threads, warps); CTA 0 then adds the CTAs' sums in rank order
+// through distributed shared memory. The order depends only on T.
 constexpr int kAuxThreads = 1024;
+constexpr int kAuxCtas = 8;
 __global__ void __launch_bounds__(kAuxThreads)
     aux_stats_kernel(const float* __restrict__ logits, const int32_t* __restrict__ counts, int64_t T_tokens,
                      int E, float* __restrict__ f, float* __restrict__ P, float* __restrict__ l_aux) {
     __shared__ float red[kAuxThreads / 32][kMaxExperts];
+    __shared__ float part[kMaxExperts];
     pdl_trigger();
     pdl_wait();
+    const uint32_t rank = cluster_ctarank();
+    const int64_t per = (T_tokens + kAuxCtas - 1) / kAuxCtas;
+    const int64_t t_begin = (int64_t)rank * per;
+    const int64_t t_end = t_begin + per < T_tokens ? t_begin + per : T_tokens;
     float acc[kMaxExperts];
 #pragma unroll
     for (int e = 0; e < kMaxExperts; ++e) acc[e] = 0.f;
-    // a thread's tokens t = tid, tid + 1024, ... in order; the score rows of
+    // a thread's tokens t = t_begin + tid, + 1024, ... in order; the score rows of
     // four of them are loaded before any is used
     constexpr int G = 4;
-    for (int64_t t0 = threadIdx.x; t0 < T_tokens; t0 += (int64_t)G * kAuxThreads) {
+    for (int64_t t0 = t_begin + threadIdx.x; t0 < t_end; t0 += (int64_t)G * kAuxThreads) {
         float lv[G][kMaxExperts];
 #pragma unroll
         for (int g = 0; g < G; ++g) {
             const int64_t t = t0 + (int64_t)g * kAuxThreads;
 #pragma unroll
-            for (int e = 0; e < kMaxExperts; ++e) lv[g][e] = (t < T_tokens && e < E) ? logits[t * E + e] : 0.f;
+            for (int e = 0; e < kMaxExperts; ++e) lv[g][e] = (t < t_end && e < E) ? logits[t * E + e] : 0.f;
         }
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-            if (t0 + (int64_t)g * kAuxThreads >= T_tokens) break;
+            if (t0 + (int64_t)g * kAuxThreads >= t_end) break;
             float m = lv[g][0];
 #pragma unroll
             for (int e = 1; e < kMaxExperts; ++e)
@@ -185,20 +194,33 @@ __global__ void __launch_bounds__(kAuxThreads)
             float v = red[lane][e];
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-            acc[e] = v;
-        }
-        if (lane == 0) {
-            float L = 0.f;
-            for (int e = 0; e < E; ++e) {
-                const float fe = (float)counts[e] / (float)(2 * T_tokens);
-                const float pe = acc[e] / (float)T_tokens;
-                f[e] = fe;
-                P[e] = pe;
-                L += fe * pe;
-            }
-            l_aux[0] = (float)E * L;
+            if (lane == 0) part[e] = v;
         }
     }
+    // every CTA's sums are in its shared memory before CTA 0 reads them
+    cluster_sync();
+    if (rank == 0 && threadIdx.x == 0) {
+        float L = 0.f;
+        for (int e = 0; e < E; ++e) {
+            float v = 0.f;
+            for (int r = 0; r < kAuxCtas; ++r) {
+                float pr;
+                asm volatile("ld.shared::cluster.f32 %0, [%1];"
+                             : "=f"(pr)
+                             : "r"(mapa_shared(smem_u32(&part[e]), (uint32_t)r))
+                             : "memory");
+                v += pr;
+            }
+            const float fe = (float)counts[e] / (float)(2 * T_tokens);
+            const float pe = v / (float)T_tokens;
+            f[e] = fe;
+            P[e] = pe;
+            L += fe * pe;
+        }
+        l_aux[0] = (float)E * L;
+    }
+    // no CTA leaves while CTA 0 may still read its shared memory
+    cluster_sync();
 }
 
 }  // namespace moe

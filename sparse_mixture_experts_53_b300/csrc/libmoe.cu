@@ -696,7 +696,8 @@ moe_status run_aux(const moe_shape& s, const float* logits, const int32_t* count
         return MOE_OK;
     }
     return launch("aux_stats", st, [&] {
-        return klaunch(aux_stats_kernel, 1, kAuxThreads, 0, st, logits, counts, s.T, s.E, f, P, l_aux);
+        return klaunch_cluster(aux_stats_kernel, kAuxCtas, kAuxCtas, kAuxThreads, 0, st, logits, counts, s.T, s.E, f,
+                               P, l_aux);
     });
 }
 

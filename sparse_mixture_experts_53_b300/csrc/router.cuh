@@ -51,6 +51,7 @@ __device__ __forceinline__ void load_vec(const T* p, float (&v)[Vec16<T>::N]) {
 
 constexpr int kRouterGroup = 8;  // 16-byte chunks each thread loads before storing them (W_g staging)
 constexpr int kRouterTokensPerWarp = 4;  // tokens a warp scores together (large batches)
+constexpr int kRouterChunks = 2;         // 16-byte chunks of each token a lane loads before using them
 
 // Top-2 selection and the two-way softmax from the E scores of one token.
 __device__ __forceinline__ void top2_softmax(const float (&acc)[kMaxExperts], int E, int32_t* idx, float* w) {
@@ -130,10 +131,10 @@ __global__ void __launch_bounds__(kRouterWarps * 32, 2)
             for (int k = 0; k < TPW; ++k)
 #pragma unroll
                 for (int e = 0; e < kMaxExperts; ++e) acc[k][e] = 0.f;
-            for (int c0 = lane; c0 < nchunks; c0 += 64) {
-                uint4 xg[2][TPW];
+            for (int c0 = lane; c0 < nchunks; c0 += 32 * kRouterChunks) {
+                uint4 xg[kRouterChunks][TPW];
 #pragma unroll
-                for (int u = 0; u < 2; ++u)
+                for (int u = 0; u < kRouterChunks; ++u)
 #pragma unroll
                     for (int k = 0; k < TPW; ++k) {
                         const int c = c0 + 32 * u;
@@ -142,7 +143,7 @@ __global__ void __launch_bounds__(kRouterWarps * 32, 2)
                                        : make_uint4(0, 0, 0, 0);
                     }
 #pragma unroll
-                for (int u = 0; u < 2; ++u) {
+                for (int u = 0; u < kRouterChunks; ++u) {
                     const int c = c0 + 32 * u;
                     if (c < nchunks) {
                         float xv[TPW][V];
