@@ -148,20 +148,37 @@ class ClockSampler:
 CSRC = ROOT / "sparse_mixture_experts_53_b300" / "csrc"
 
 
-# The sources that define each profiled kernel and its launch: its own file, the shared device helpers
-# and the launch code (ncu figures go stale when any of them changes, not when another kernel does).
+# The sources that define each profiled kernel and its launch: its own file, the shared device helpers and
+# the launch functions in the ABI file (ncu figures go stale when any of them changes, not when another
+# kernel or another launch does).
 KERNEL_SOURCES = {
-    "tile_up_swiglu": ("ffn_tc.cuh", "common.cuh", "libmoe.cu"),
-    "tile_down_scale": ("ffn_tc.cuh", "common.cuh", "libmoe.cu"),
-    "stream_up": ("ffn_tc.cuh", "common.cuh", "libmoe.cu"),
+    "tile_up_swiglu": (("ffn_tc.cuh", "common.cuh"), ("run_pair_ffn", "make_map", "pair_capacity", "pair_grid")),
+    "tile_down_scale": (("ffn_tc.cuh", "common.cuh"), ("run_pair_ffn", "make_map", "pair_capacity", "pair_grid")),
+    "stream_up": (("ffn_tc.cuh", "common.cuh"), ("run_ffn", "make_map", "pick_kslice", "ffn_layout")),
 }
 
 
+def _function_text(src: str, name: str) -> str:
+    """The definition of a top-level function of a C++ source: from its signature line to the closing brace
+    at column 0."""
+    import re
+    m = re.search(r"^[^\n]*\b" + re.escape(name) + r"\(", src, re.M)
+    if m is None:
+        return ""
+    end = src.find("\n}\n", m.start())
+    return src[m.start():end + 3 if end >= 0 else len(src)]
+
+
 def _source_digest(kernel: str) -> str:
+    files, functions = KERNEL_SOURCES[kernel]
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES[kernel]:
+    for name in files:
         h.update(name.encode())
         h.update((CSRC / name).read_bytes())
+    abi = (CSRC / "libmoe.cu").read_text()
+    for fn in functions:
+        h.update(fn.encode())
+        h.update(_function_text(abi, fn).encode())
     return h.hexdigest()[:16]
 
 
