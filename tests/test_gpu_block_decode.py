@@ -83,7 +83,8 @@ def test_rope_split_writes_the_caches_at_their_positions():
 @pytest.mark.parametrize("lens,Hq,Hkv,cmax", [((0, 1, 255, 256, 700), 32, 8, 1000), ((4095,), 8, 2, 4096),
                                                ((10, 300), 4, 4, 333), ((127, 128, 129), 16, 8, 300),
                                                ((50, 999), 16, 2, 1000), ((3, 2000), 32, 2, 2048),
-                                               tuple([tuple(range(0, 3200, 100)), 8, 8, 3300])])
+                                               tuple([tuple(range(0, 3200, 100)), 8, 8, 3300]),
+                                               ((100, 1000), 12, 4, 1100), ((77,), 24, 4, 200)])
 def test_attention_decode_on_ragged_caches(lens, Hq, Hkv, cmax):
     B = len(lens)
     s = moe.make_block_shape(B, 1, 256, Hq, Hkv, 256, cache_max=cmax)
