@@ -63,6 +63,7 @@ struct TcControl {
     int base[kMaxExperts + 1];
     int act[kMaxExperts];
     int koff[kMaxExperts + 1];  // expert groups padded to multiples of 64 rows
+    int half_ok;                // pair kernel, forward modes: last tiles of <= 128 rows run as half tiles
 };
 
 constexpr size_t kTileSmemBytes = 1024 + (size_t)kTileStages * kTileStageBytes + sizeof(TcControl);
@@ -119,24 +120,27 @@ struct TileArgs {
     int n_fast;
 };
 
-// Epilogue of one token tile for one thread (one row): reads the row's 256
+// Epilogue of one token tile for one thread (one row): reads the row's
 // accumulator columns from tensor memory and writes
-//   up:   h = SiLU(u) * v in bf16 (u = columns 0-127, v = columns 128-255),
+//   up:   h = SiLU(u) * v in bf16 (u in columns j, v in columns v_off + j),
 //   down: perm_w[r] * acc in fp32.
 // Every thread of the warp must call it (tcgen05.ld is warp-collective);
 // `valid` only predicates the stores.
-// [j_begin, j_end): the columns this thread handles (up: of the 128 u, v
-// pairs; down: of the 256 columns), multiples of 16.
+// [j_begin, j_end): the columns this thread handles (up: of the u, v pairs;
+// down: of the accumulator columns), multiples of 16; col0: the output column
+// of j = 0 (up: in H, down: in y_slot).
 template <bool UP>
 __device__ __forceinline__ void tile_epilogue(uint32_t taddr, bool valid, int64_t r, int nt, const TileArgs& args,
-                                              int j_begin = 0, int j_end = UP ? kTileM : kTileN) {
+                                              int j_begin = 0, int j_end = UP ? kTileM : kTileN,
+                                              int v_off = kTileM, int col0 = -1) {
+    if (col0 < 0) col0 = nt * (UP ? kTileM : kTileN);
     if (UP) {
-        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(args.out) + r * args.ldo + nt * kTileM;
+        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(args.out) + r * args.ldo + col0;
 #pragma unroll 1
         for (int j = j_begin; j < j_end; j += 16) {
             uint32_t u[16], v[16];
             tmem_ld16(taddr + j, u);
-            tmem_ld16(taddr + kTileM + j, v);
+            tmem_ld16(taddr + v_off + j, v);
             tmem_wait_ld();
             uint32_t pk[8];
 #pragma unroll
@@ -151,7 +155,7 @@ __device__ __forceinline__ void tile_epilogue(uint32_t taddr, bool valid, int64_
                 dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
                 if (args.u_out != nullptr) {
                     // training forward: keep u and v (bf16) for the backward pass
-                    const int64_t at = r * args.ldo + nt * kTileM + j;
+                    const int64_t at = r * args.ldo + col0 + j;
 #pragma unroll
                     for (int i = 0; i < 8; ++i) pk[i] = pack_bf16x2(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1]));
                     uint4* du = reinterpret_cast<uint4*>(args.u_out + at);
@@ -167,7 +171,7 @@ __device__ __forceinline__ void tile_epilogue(uint32_t taddr, bool valid, int64_
         }
     } else {
         const float pw = valid ? (args.perm_w != nullptr ? args.perm_w[r] : 1.0f) : 0.f;
-        float* out = reinterpret_cast<float*>(args.out) + r * args.ldo + nt * kTileN;
+        float* out = reinterpret_cast<float*>(args.out) + r * args.ldo + col0;
 #pragma unroll 1
         for (int j = j_begin; j < j_end; j += 16) {
             uint32_t a[16];
@@ -509,10 +513,20 @@ __device__ __forceinline__ void wgrad_epilogue(uint32_t taddr, bool any_k, int e
 }
 
 // One CTA pair per thread-block cluster (launched with cluster size 2).
+//
+// Half tiles (forward modes): an expert's last row tile with at most 128 real
+// rows runs one M = 128 MMA across the pair instead of M = 256, at about half
+// the tensor-core time. Each CTA then supplies 64 token rows (from row
+// 64 * rank of the tile), and its accumulator holds those 64 rows twice over
+// the lanes: lanes 0-63 carry the tile's columns 0-127, lanes 64-127 columns
+// 128-255. For the up projection each CTA's 128 weight rows are 64 rows of W1
+// followed by the same 64 rows of W3 (map_b0h / map_b1h: boxes of 64 rows),
+// so a lane still finds u and v of the same f, 64 columns apart.
 template <int MODE>
 __global__ void __launch_bounds__(kPairThreads, 1)
     tile_pair_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b0,
-                          const __grid_constant__ CUtensorMap map_b1, const TileArgs args) {
+                          const __grid_constant__ CUtensorMap map_b1, const __grid_constant__ CUtensorMap map_b0h,
+                          const __grid_constant__ CUtensorMap map_b1h, const TileArgs args) {
     constexpr bool UP = MODE == PM_UP;
     constexpr bool WG = MODE == PM_WGRAD;
     constexpr bool A_MN = WG;                      // A read as stored with K = token rows
@@ -549,7 +563,11 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&map_a);
         tma_prefetch_desc(&map_b0);
-        if (UP) tma_prefetch_desc(&map_b1);
+        if (UP) {
+            tma_prefetch_desc(&map_b1);
+            tma_prefetch_desc(&map_b0h);
+            tma_prefetch_desc(&map_b1h);
+        }
     }
     if (warp == 1) {
         tmem_alloc_pair(smem_u32(&ctl->tmem_base), 2 * kTileAccCols);
@@ -577,6 +595,18 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         ctl->n_work = tiles;
         ctl->koff[0] = 0;
         for (int e = 0; e < args.E; ++e) ctl->koff[e + 1] = ctl->koff[e] + (ctl->cnt[e] + kBK - 1) / kBK * kBK;
+        // Half tiles pay when they save a large share of the MMA work (few row tiles per expert): a
+        // half tile finishes early, which puts its pair out of step with the pairs that share its
+        // weight tiles. Measured at the Mixtral shape: 5.6 % of the MMA rows saved (T = 4096) made the
+        // expert GEMMs 0.5-4 % faster; 2.9 % (the skewed T = 8192 batch) made the up projection 1 %
+        // slower; 1.9 % (T = 16384) changed nothing measurable. So they run from 4 % on.
+        int rows = 0, saved = 0;
+        for (int e = 0; e < args.E; ++e) {
+            rows += ctl->mt[e] * kPairM;
+            const int tail = ctl->cnt[e] - (ctl->mt[e] - 1) * kPairM;
+            if (ctl->mt[e] > 0 && tail <= 128) saved += 128;
+        }
+        ctl->half_ok = MODE <= PM_DOWN && saved * 25 >= rows;
     }
     // both CTAs' barriers are initialised and both halves of tensor memory are
     // allocated before any CTA signals the other
@@ -603,6 +633,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     };
     // K steps of a tile: fixed, or the expert's padded token count
     auto ksteps = [&](int e) { return WG ? (ctl->koff[e + 1] - ctl->koff[e]) / kBK : KB; };
+    // a forward tile with at most 128 real rows runs as a half tile (M = 128)
+    auto is_half = [&](int e, int mt) { return MODE <= PM_DOWN && ctl->half_ok && ctl->cnt[e] - mt * kPairM <= 128; };
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer (both CTAs)
@@ -620,9 +652,11 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             for (int tile = pair; ok && tile < n_work; tile += n_pairs) {
                 int e, nt, mt;
                 decode(tile, e, nt, mt);
-                // this CTA's 128 rows (K-major) or 128 columns (MN-major) of each operand
+                // this CTA's 128 rows (K-major) or 128 columns (MN-major) of each operand; a half tile's
+                // CTA supplies 64 token rows
+                const bool half = is_half(e, mt);
                 const int a0 = WG ? mt * kPairM + 128 * (int)rank
-                                  : (A_PAD ? ctl->koff[e] : ctl->off[e]) + mt * kPairM + 128 * (int)rank;
+                                  : (A_PAD ? ctl->koff[e] : ctl->off[e]) + mt * kPairM + (half ? 64 : 128) * (int)rank;
                 const int b0 = UP ? e * args.w_rows + nt * kTileM
                                   : (B_MN ? nt * kTileN + 128 * (int)rank
                                           : e * args.w_rows + nt * kTileN + 128 * (int)rank);
@@ -661,6 +695,11 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                         }
                         tma_load_2d_pair(sb, mb, fb, b0, ky, pol_w);
                         tma_load_2d_pair(sb + kPairHalfBytes / 2, mb, fb, b0 + 64, ky, pol_w);
+                    } else if (UP && half) {
+                        // 64 rows of W1, then the same 64 rows of W3
+                        const int bh = e * args.w_rows + nt * kTileM + 64 * (int)rank;
+                        tma_load_2d_pair(sb, &map_b0h, fb, kx, bh, pol_w);
+                        tma_load_2d_pair(sb + kPairHalfBytes / 2, &map_b1h, fb, kx, bh, pol_w);
                     } else {
                         tma_load_2d_pair(sb, map_b, fb, kx, b0, pol_w);
                     }
@@ -679,7 +718,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer (even CTA only)
         if (lane == 0 && leader) {
-            constexpr uint32_t idesc = idesc_bf16_f32(kPairM, kTileN, A_MN, B_MN);
+            constexpr uint32_t idesc_full = idesc_bf16_f32(kPairM, kTileN, A_MN, B_MN);
+            constexpr uint32_t idesc_half = idesc_bf16_f32(kPairM / 2, kTileN, A_MN, B_MN);
             // descriptor start advance per K step of 16, in 16-byte units:
             // 32 bytes inside a K-major swizzle row, two 1 KB atoms MN-major
             constexpr uint64_t a_step = A_MN ? 128 : 2;
@@ -691,6 +731,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                 int e, nt, mt;
                 decode(tile, e, nt, mt);
                 const int nk = ksteps(e);
+                const uint32_t idesc = is_half(e, mt) ? idesc_half : idesc_full;
                 const int b = it & 1;
                 const uint32_t aph = (it >> 1) & 1;
                 if (!mbar_wait_cluster(smem_u32(&ctl->tempty[b]), aph ^ 1, tmo, abort_flag)) {
@@ -754,6 +795,18 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                                (warp - 2) * kWgradStageFloats;
                 wgrad_epilogue(taddr, ksteps(e) > 0, e, mt * kPairM + row_in_tile - lane, nt, lane, stage, args,
                                j_begin, j_end);
+            } else if (is_half(e, mt)) {
+                // half tile: lane l holds row l mod 64 of this CTA's 64 rows, the tile's columns
+                // 128 (l / 64) .. 128 (l / 64) + 127 (up: u and v of f = 64 (l / 64) + j at j, 64 + j)
+                const int gl = sub * 32 + lane;
+                const int grow = mt * kPairM + 64 * (int)rank + (gl & 63);
+                const bool valid = grow < ctl->cnt[e];
+                const int64_t r = ctl->off[e] + grow;
+                const int hb = half * (UP ? 32 : 64);
+                if (UP)
+                    tile_epilogue<true>(taddr, valid, r, nt, args, hb, hb + 32, 64, nt * kTileM + 64 * (gl >> 6));
+                else
+                    tile_epilogue<false>(taddr, valid, r, nt, args, hb, hb + 64, 0, nt * kTileN + 128 * (gl >> 6));
             } else {
                 const int grow = mt * kPairM + row_in_tile;
                 const bool valid = grow < ctl->cnt[e];

@@ -536,15 +536,16 @@ moe_status run_pair_ffn(const moe_shape& s, const void* x_perm, const int32_t* o
         cudaGetLastError();
         return MOE_ERR_UNSUPPORTED;
     }
-    CUtensorMap ma, mb0, mb1;
+    CUtensorMap ma, mb0, mb1, mb0h, mb1h;
     if (!make_map(&ma, x_perm, d, R, 128) || !make_map(&mb0, w1, d, (uint64_t)E * F, 128) ||
-        !make_map(&mb1, w3, d, (uint64_t)E * F, 128))
+        !make_map(&mb1, w3, d, (uint64_t)E * F, 128) || !make_map(&mb0h, w1, d, (uint64_t)E * F, 64) ||
+        !make_map(&mb1h, w3, d, (uint64_t)E * F, 64))
         return MOE_ERR_CUDA;
     TileArgs up{offsets, perm_w, H, E, d, F / kTileM, F, F, g.timeout_ns, u_out, v_out};
     const int64_t units_up = ((R + kPairM - 1) / kPairM + E) * (F / kTileM);
     MOE_TRY(launch("tile_up_swiglu", st, [&] {
         return klaunch_cluster(kup, 2, pair_grid(units_up, cap_up), kPairThreads, kPairSmemBytes, st, ma, mb0, mb1,
-                               up);
+                               mb0h, mb1h, up);
     }));
     CUtensorMap mh, mw2;
     if (!make_map(&mh, H, F, R, 128) || !make_map(&mw2, w2, F, (uint64_t)E * d, 128)) return MOE_ERR_CUDA;
@@ -552,7 +553,7 @@ moe_status run_pair_ffn(const moe_shape& s, const void* x_perm, const int32_t* o
     const int64_t units_down = ((R + kPairM - 1) / kPairM + E) * (d / kTileN);
     return launch("tile_down_scale", st, [&] {
         return klaunch_cluster(kdown, 2, pair_grid(units_down, cap_down), kPairThreads, kPairSmemBytes, st, mh, mw2,
-                               mw2, down);
+                               mw2, mw2, mw2, down);
     });
 }
 
@@ -761,7 +762,8 @@ moe_status launch_pair(const char* name, int slot, int cap_slot, const CUtensorM
     const int cap = pair_capacity(kern, smem, cap_slot);
     if (cap <= 0) return MOE_ERR_UNSUPPORTED;
     return launch(name, st, [&] {
-        return klaunch_cluster(kern, 2, pair_grid(pairs_upper, cap), kPairThreads, smem, st, ma, mb0, mb1, a);
+        return klaunch_cluster(kern, 2, pair_grid(pairs_upper, cap), kPairThreads, smem, st, ma, mb0, mb1, mb0, mb1,
+                               a);
     });
 }
 
