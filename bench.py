@@ -440,6 +440,7 @@ def run_ours(args, rank, world, local) -> dict | None:
     torch.cuda.set_device(local)
     moe.moe_set_knob(moe.MOE_KNOB_PDL, args.pdl)
     moe.moe_set_knob(moe.MOE_KNOB_TILE_CTAS, args.tile_ctas)
+    moe.moe_set_knob(moe.MOE_KNOB_TILE_SCHED, args.tile_sched)
     ranks = Ranks(rank, world, local, backend="nccl")
     stream = torch.cuda.current_stream()
 
@@ -471,7 +472,7 @@ def run_ours(args, rank, world, local) -> dict | None:
                    "ffn_path": "weight-streaming (swap-AB)" if streaming else
                    ("token tiles 256x256 on CTA pairs" if args.tile_ctas == 2 or (args.tile_ctas == 0 and cfg["T"] > 384)
                     else "token tiles 128x256"),
-                   "pdl": bool(args.pdl),
+                   "pdl": bool(args.pdl), "tile_units": tile_units_note(args.tile_sched),
                    "l2": "inputs larger than L2: each step reads %.2f GB of expert weights" % (work["weight_bytes"] / 1e9),
                    "experts_touched": work["touched"], "input_gen_s": round(gen_s, 1)},
         "step": {"tflops": round(work["flops"] / step_s / 1e12, 2),
@@ -530,6 +531,14 @@ TRAIN_GEMM_FLOPS = {  # multiples of R*d*ffn (R = 2T slot rows) per launch
 }
 
 
+def tile_units_note(sched: int) -> str:
+    """How the CTA-pair kernels took their units (MOE_KNOB_TILE_SCHED)."""
+    if sched == 8:
+        return "automatic: the up projection claims units from a counter at >= 32 units per pair, else fixed"
+    return "claimed from a counter: " + (", ".join(n for b, n in ((1, "up"), (2, "down"), (4, "backward"))
+                                                  if sched & b) or "none")
+
+
 def run_training(args) -> dict:
     """One training step of the layer: forward that keeps its state, then the backward pass."""
     import torch
@@ -539,6 +548,7 @@ def run_training(args) -> dict:
 
     torch.cuda.set_device(0)
     moe.moe_set_knob(moe.MOE_KNOB_PDL, args.pdl)
+    moe.moe_set_knob(moe.MOE_KNOB_TILE_SCHED, args.tile_sched)
     k = args.config
     cfg = CONFIGS[k]
     L = make_config(k)
@@ -1081,6 +1091,9 @@ def main():
                     help="time one decode step of the Mixtral block (16 sequences, 4096-token caches)")
     ap.add_argument("--tile-ctas", type=int, default=0, choices=[0, 1, 2],
                     help="token tiles: automatic (0), single CTAs (1), CTA pairs (2)")
+    ap.add_argument("--tile-sched", type=int, default=8, choices=range(9),
+                    help="CTA-pair GEMMs claiming their units from a counter: bit 0 up, bit 1 down, "
+                         "bit 2 the backward's four (0: static units per pair); 8 (default): automatic")
     ap.add_argument("--decode-loop", action="store_true",
                     help="decode-time expert cache experiment: a locality token stream through 1 or 32 layers "
                          "with and without part of each call's expert weights kept in L2")

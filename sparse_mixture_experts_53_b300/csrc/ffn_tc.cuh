@@ -47,6 +47,8 @@ constexpr int kStreamAcc = 4;
 constexpr int kStreamMaxNB = 64;
 constexpr uint32_t kStreamABytes = 128 * kBK * 2;     // 16 KB of weights per stage
 
+constexpr int kUnitRing = 8;
+
 struct TcControl {
     uint64_t full[kMaxStreamStages];
     uint64_t empty[kMaxStreamStages];
@@ -64,6 +66,11 @@ struct TcControl {
     int act[kMaxExperts];
     int koff[kMaxExperts + 1];  // expert groups padded to multiples of 64 rows
     int half_ok;                // pair kernel, forward modes: last tiles of <= 128 rows run as half tiles
+    // pair kernel with a shared unit counter: the even CTA's producer claims each unit and passes it
+    // to every other role of both CTAs through this ring
+    uint64_t ring_full[kUnitRing];   // the slot holds a claimed unit (-1: no more)
+    uint64_t ring_empty[kUnitRing];  // (even CTA) every reader of both CTAs has taken the slot
+    int ring_unit[kUnitRing];
 };
 
 constexpr size_t kTileSmemBytes = 1024 + (size_t)kTileStages * kTileStageBytes + sizeof(TcControl);
@@ -118,6 +125,10 @@ struct TileArgs {
     // operand); 1 = column tiles fastest: they share a block of A and all of B stays in L2 (right when B
     // is the smaller one). The order does not change any tile's arithmetic.
     int n_fast;
+    // pair kernel: nullptr = pair p takes units p, p + pairs, ...; otherwise a counter, zero at launch,
+    // from which the pairs claim units in order as they become free (any pair may compute any unit: the
+    // results do not depend on the assignment)
+    int* sched;
 };
 
 // Epilogue of one token tile for one thread (one row): reads the row's
@@ -399,6 +410,8 @@ constexpr int kPairThreads = 320;
 constexpr int kPairEpiWarps = 8;
 constexpr uint32_t kPairHalfBytes = 128 * kBK * 2;          // 16 KB: one CTA's half of A or of B
 constexpr uint32_t kPairStageBytes = 2 * kPairHalfBytes;     // 32 KB per CTA and stage
+// readers of a unit-ring slot: the MMA issuer, the odd CTA's producer and the epilogue warps of both CTAs
+constexpr int kRingReaders = 2 + 2 * kPairEpiWarps;
 constexpr size_t kPairSmemBytes = 1024 + (size_t)kPairStages * kPairStageBytes + sizeof(TcControl);
 // the weight-gradient epilogue's staging arrays, one per epilogue warp, after the control block
 constexpr size_t kWgradStageBytes = 16 + (size_t)kPairEpiWarps * 32 * 33 * sizeof(float);
@@ -557,6 +570,10 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             mbar_init(smem_u32(&ctl->tempty[b]), 2 * kPairEpiWarps);  // the epilogue warps of both CTAs
         }
         mbar_init(smem_u32(&ctl->drain), 1);
+        for (int q = 0; q < kUnitRing; ++q) {
+            mbar_init(smem_u32(&ctl->ring_full[q]), 1);
+            mbar_init(smem_u32(&ctl->ring_empty[q]), kRingReaders);
+        }
         ctl->abort_flag = 0;
         fence_mbar_init();
     }
@@ -636,6 +653,36 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     // a forward tile with at most 128 real rows runs as a half tile (M = 128)
     auto is_half = [&](int e, int mt) { return MODE <= PM_DOWN && ctl->half_ok && ctl->cnt[e] - mt * kPairM <= 128; };
 
+    // The pair's it-th unit (-1: none left). Static: pair + it * n_pairs. With a counter: the even CTA's
+    // producer claims it (claim_unit) and every other role of both CTAs takes it from the ring slot
+    // (take_unit, one thread per role or warp), then frees the slot (give_back).
+    const bool shared_counter = args.sched != nullptr;
+    // `claimed`: the unit the even CTA's producer took from the counter one iteration ahead, so that the
+    // atomic's round trip overlaps the previous unit's loads
+    auto claim_unit = [&](int it, int& claimed, int& tile) -> bool {
+        const int q = it & (kUnitRing - 1);
+        const uint32_t rph = (uint32_t)(it / kUnitRing) & 1u;
+        if (!mbar_wait_cluster(smem_u32(&ctl->ring_empty[q]), rph ^ 1u, tmo, abort_flag)) return false;
+        int u = claimed < n_work ? claimed : -1;
+        if (u >= 0) claimed = atomicAdd(args.sched, 1);
+        ctl->ring_unit[q] = u;
+        st_cluster_s32(mapa_shared(smem_u32(&ctl->ring_unit[q]), 1), u);
+        mbar_arrive(smem_u32(&ctl->ring_full[q]));
+        mbar_arrive_cluster(mapa_shared(smem_u32(&ctl->ring_full[q]), 1));
+        tile = u;
+        return true;
+    };
+    auto take_unit = [&](int it, int& tile) -> bool {
+        const int q = it & (kUnitRing - 1);
+        const uint32_t rph = (uint32_t)(it / kUnitRing) & 1u;
+        if (!mbar_wait_cluster(smem_u32(&ctl->ring_full[q]), rph, tmo, abort_flag)) return false;
+        tile = *reinterpret_cast<volatile int*>(&ctl->ring_unit[q]);
+        return true;
+    };
+    auto give_back = [&](int it) {
+        mbar_arrive_cluster(mapa_shared(smem_u32(&ctl->ring_empty[it & (kUnitRing - 1)]), lead));
+    };
+
     if (warp == 0) {
         // ------------------------------------------------ TMA producer (both CTAs)
         if (lane == 0) {
@@ -649,7 +696,18 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             uint32_t s = 0, ph = 0;
             uint32_t issued_mask = 0, issued_ph = 0;
             bool ok = true;
-            for (int tile = pair; ok && tile < n_work; tile += n_pairs) {
+            int claimed = (shared_counter && leader) ? atomicAdd(args.sched, 1) : 0;
+            for (int it = 0; ok; ++it) {
+                int tile = pair + it * n_pairs;
+                if (shared_counter) {
+                    if (!(leader ? claim_unit(it, claimed, tile) : take_unit(it, tile))) {
+                        raise_abort(ctl, kid, W_PRODUCER);
+                        ok = false;
+                        break;
+                    }
+                    if (!leader) give_back(it);
+                }
+                if (tile < 0 || tile >= n_work) break;
                 int e, nt, mt;
                 decode(tile, e, nt, mt);
                 // this CTA's 128 rows (K-major) or 128 columns (MN-major) of each operand; a half tile's
@@ -726,8 +784,17 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             constexpr uint64_t b_step = B_MN ? 128 : 2;
             uint32_t s = 0, ph = 0;
             bool ok = true, any = false;
-            int it = 0;
-            for (int tile = pair; ok && tile < n_work; tile += n_pairs, ++it) {
+            for (int it = 0; ok; ++it) {
+                int tile = pair + it * n_pairs;
+                if (shared_counter) {
+                    if (!take_unit(it, tile)) {
+                        raise_abort(ctl, kid, W_MMA);
+                        ok = false;
+                        break;
+                    }
+                    give_back(it);
+                }
+                if (tile < 0 || tile >= n_work) break;
                 int e, nt, mt;
                 decode(tile, e, nt, mt);
                 const int nk = ksteps(e);
@@ -777,8 +844,21 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         const int j_begin = half * (ncols / 2), j_end = j_begin + ncols / 2;
         uint32_t tempty_leader[2];
         for (int b = 0; b < 2; ++b) tempty_leader[b] = mapa_shared(smem_u32(&ctl->tempty[b]), lead);
-        int it = 0;
-        for (int tile = pair; tile < n_work; tile += n_pairs, ++it) {
+        for (int it = 0;; ++it) {
+            int tile = pair + it * n_pairs;
+            if (shared_counter) {
+                int got = 1;
+                if (lane == 0) got = take_unit(it, tile) ? 1 : 0;
+                got = __shfl_sync(0xffffffffu, got, 0);
+                tile = __shfl_sync(0xffffffffu, tile, 0);
+                if (!got) {
+                    if (lane == 0) raise_abort(ctl, kid, W_EPILOGUE);
+                    break;
+                }
+                __syncwarp();
+                if (lane == 0) give_back(it);
+            }
+            if (tile < 0 || tile >= n_work) break;
             int e, nt, mt;
             decode(tile, e, nt, mt);
             const int b = it & 1;

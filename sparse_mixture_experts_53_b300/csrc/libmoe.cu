@@ -64,6 +64,11 @@ bool env_flag(const char* name) {
     return v != nullptr && v[0] != '\0' && std::strcmp(v, "0") != 0;
 }
 
+// MOE_KNOB_TILE_SCHED: 0 .. 7 a bit mask, kTileSchedAuto the automatic choice
+constexpr int kTileSchedAuto = 8;
+// automatic choice: the up projection claims its units from this many units per pair on
+constexpr int kClaimMinUnitsPerPair = 32;
+
 struct HostState {
     int ffn_path = 0;          // 0 auto, 1 token tiles, 2 weight streaming
     int64_t kslice = 0;        // 0 auto
@@ -73,6 +78,7 @@ struct HostState {
     bool timing = false;
     bool pdl = true;           // programmatic dependent launch between the library's kernels
     int tile_ctas = 0;         // token tiles: 0 auto, 1 single CTAs, 2 CTA pairs
+    int tile_sched = kTileSchedAuto;  // CTA-pair GEMMs claiming units from a counter: bit 0 up, 1 down, 2 backward
     uint64_t l2_keep_bytes = 0;  // weight-streaming path: bytes per call kept in L2 for the next call
     int pair_cap[kMaxDevices][8] = {{0}};  // resident clusters per pair kernel (0 = not queried)
     std::vector<TimingRecord> records;
@@ -324,7 +330,7 @@ size_t permute_ws_bytes(const moe_shape& s) {
 struct FfnLayout {
     int path = 0;
     int nb = 0, ks_up = 0, ks_down = 0, S_up = 0, S_down = 0;
-    size_t h = 0, part_up = 0, part_down = 0, total = 0;
+    size_t h = 0, part_up = 0, part_down = 0, sched = 0, total = 0;
 };
 
 FfnLayout ffn_layout(const moe_shape& s) {
@@ -346,6 +352,10 @@ FfnLayout ffn_layout(const moe_shape& s) {
             off = align_up(off + (size_t)L.S_up * 2 * R * s.ffn * 4, kAlign);
             L.part_down = off;
             off = align_up(off + (size_t)L.S_down * R * s.d * 4, kAlign);
+        } else if (L.path == 1) {
+            // the unit counters of the CTA-pair kernels (up, down), on separate lines
+            L.sched = off;
+            off = align_up(off + 256, kAlign);
         }
     }
     L.total = off;
@@ -522,7 +532,7 @@ int pair_grid(int64_t pairs_upper, int cap) {
 // MOE_ERR_UNSUPPORTED (nothing enqueued) when the kernels do not fit.
 moe_status run_pair_ffn(const moe_shape& s, const void* x_perm, const int32_t* offsets, const float* perm_w,
                         const void* w1, const void* w3, const void* w2, float* y_slot, __nv_bfloat16* H,
-                        __nv_bfloat16* u_out, __nv_bfloat16* v_out, cudaStream_t st) {
+                        __nv_bfloat16* u_out, __nv_bfloat16* v_out, int* sched, cudaStream_t st) {
     const int64_t R = 2 * s.T;
     const int d = s.d, F = s.ffn, E = s.E;
     auto kup = tile_pair_gemm_kernel<PM_UP>;
@@ -543,13 +553,25 @@ moe_status run_pair_ffn(const moe_shape& s, const void* x_perm, const int32_t* o
         return MOE_ERR_CUDA;
     TileArgs up{offsets, perm_w, H, E, d, F / kTileM, F, F, g.timeout_ns, u_out, v_out};
     const int64_t units_up = ((R + kPairM - 1) / kPairM + E) * (F / kTileM);
+    const int grid_up = pair_grid(units_up, cap_up);
+    // Automatic: the up projection claims its units when each pair has many of them (T = 16384: about 200).
+    // The pairs' drift then no longer spreads the readers of a weight tile over several waves, and the
+    // launch reads each operand from DRAM about once instead of twice; with few units per pair
+    // (T = 4096: 8) the fixed assignment keeps the pairs in step and was the faster of the two.
+    const int sched_bits = g.tile_sched != kTileSchedAuto ? g.tile_sched
+                                                          : (units_up >= (int64_t)kClaimMinUnitsPerPair * (grid_up / 2) ? 1 : 0);
+    if (sched_bits & 3) {
+        // the kernels claim their units from counters that start at zero
+        if (cudaMemsetAsync(sched, 0, 256, st) != cudaSuccess) return MOE_ERR_CUDA;
+        if (sched_bits & 1) up.sched = sched;
+    }
     MOE_TRY(launch("tile_up_swiglu", st, [&] {
-        return klaunch_cluster(kup, 2, pair_grid(units_up, cap_up), kPairThreads, kPairSmemBytes, st, ma, mb0, mb1,
-                               mb0h, mb1h, up);
+        return klaunch_cluster(kup, 2, grid_up, kPairThreads, kPairSmemBytes, st, ma, mb0, mb1, mb0h, mb1h, up);
     }));
     CUtensorMap mh, mw2;
     if (!make_map(&mh, H, F, R, 128) || !make_map(&mw2, w2, F, (uint64_t)E * d, 128)) return MOE_ERR_CUDA;
     TileArgs down{offsets, perm_w, y_slot, E, F, d / kTileN, d, d, g.timeout_ns};
+    if (sched_bits & 2) down.sched = sched + 32;
     const int64_t units_down = ((R + kPairM - 1) / kPairM + E) * (d / kTileN);
     return launch("tile_down_scale", st, [&] {
         return klaunch_cluster(kdown, 2, pair_grid(units_down, cap_down), kPairThreads, kPairSmemBytes, st, mh, mw2,
@@ -584,7 +606,8 @@ moe_status run_ffn(const moe_shape& s, const void* x_perm, const int32_t* offset
     const int tile_ctas = g.tile_ctas != 0 ? g.tile_ctas : (s.T <= kSingleCtaMaxTokens ? 1 : 2);
     if (L.path == 1 && tile_ctas == 2) {
         // CTA pairs: each CTA stages 128 token rows and 128 weight rows per stage
-        const moe_status rc = run_pair_ffn(s, x_perm, offsets, perm_w, w1, w3, w2, y_slot, H, u_out, v_out, st);
+        const moe_status rc = run_pair_ffn(s, x_perm, offsets, perm_w, w1, w3, w2, y_slot, H, u_out, v_out,
+                                           reinterpret_cast<int*>(ws + L.sched), st);
         if (rc != MOE_ERR_UNSUPPORTED) return rc;
     }
     if (L.path == 1) {
@@ -723,7 +746,7 @@ TrainLayout train_layout(const moe_shape& s) {
 // Workspace of the backward pass. dYs and dUV rows are in the padded group
 // order (each expert's rows from a multiple of 64, zero rows between groups).
 struct BwdLayout {
-    size_t dg, dl, dys, duv, dxp, dwg, total;
+    size_t dg, dl, dys, duv, dxp, dwg, sched, total;
     int64_t rp;   // padded rows: 2T + 64 E, rounded up to 64
     int nchunks;  // token chunks of the router's weight gradient
 };
@@ -745,6 +768,7 @@ BwdLayout bwd_layout(const moe_shape& s) {
     L.duv = take((size_t)L.rp * 2 * F * 2);
     L.dxp = take(R * d * 4);
     L.dwg = take((size_t)std::max(L.nchunks, 1) * E * d * 4);
+    L.sched = take(512);  // unit counters of the four CTA-pair GEMMs, on separate lines
     L.total = off;
     return L;
 }
@@ -795,6 +819,8 @@ moe_status run_backward(const moe_shape& s, const __nv_bfloat16* x, const __nv_b
     float* dxp = reinterpret_cast<float*>(ws + B.dxp);
     float* part = reinterpret_cast<float*>(ws + B.dwg);
     const int sms = sm_count();
+    int* sched = (g.tile_sched != kTileSchedAuto && (g.tile_sched & 4)) ? reinterpret_cast<int*>(ws + B.sched) : nullptr;
+    if (sched != nullptr && cudaMemsetAsync(sched, 0, 512, st) != cudaSuccess) return MOE_ERR_CUDA;
 
     // per slot: dYs = g dy (padded order, pad rows of dYs and dUV zeroed),
     // dg = <dy, E(x)>; per token: the scores' gradient
@@ -814,12 +840,14 @@ moe_status run_backward(const moe_shape& s, const __nv_bfloat16* x, const __nv_b
     TileArgs a_dh{offsets, nullptr, duv, E, d, F / kTileN, d, 2 * F, g.timeout_ns};
     a_dh.u_in = U;
     a_dh.v_in = V;
+    if (sched != nullptr) a_dh.sched = sched;
     MOE_TRY(launch_pair<PM_BWD_DH>("bwd_dh_swiglu", 8, 2, ma, mb0, mb0, a_dh, token_tiles * (F / kTileN), st));
     // dXp = [du dv] [W1; W3] (W1, W3 read as stored)
     if (!make_map(&ma, duv, 2 * F, (uint64_t)B.rp, 128) || !make_map(&mb0, w1, d, (uint64_t)E * F, 64) ||
         !make_map(&mb1, w3, d, (uint64_t)E * F, 64))
         return MOE_ERR_CUDA;
     TileArgs a_dx{offsets, nullptr, dxp, E, 2 * F, d / kTileN, F, d, g.timeout_ns};
+    if (sched != nullptr) a_dx.sched = sched + 32;
     MOE_TRY(launch_pair<PM_BWD_DX>("bwd_dx", 9, 3, ma, mb0, mb1, a_dx, token_tiles * (d / kTileN), st));
     // dx = both slots + the router's part
     MOE_TRY(launch("bwd_combine", st, [&] {
@@ -840,6 +868,7 @@ moe_status run_backward(const moe_shape& s, const __nv_bfloat16* x, const __nv_b
     a_w2.m_tiles = d / kPairM;
     a_w2.split_rows = d;
     a_w2.out_estride = (int64_t)d * F;
+    if (sched != nullptr) a_w2.sched = sched + 64;
     MOE_TRY(launch_pair<PM_WGRAD>("bwd_dw2", 10, 4, ma, mb0, mb0, a_w2, (int64_t)E * (d / kPairM) * (F / kTileN), st));
     // [dW1; dW3][e] = [du dv]_e^T Xp_e
     if (!make_map(&ma, duv, 2 * (uint64_t)F, (uint64_t)B.rp, 64) || !make_map(&mb0, x_perm, d, R, 64))
@@ -853,6 +882,7 @@ moe_status run_backward(const moe_shape& s, const __nv_bfloat16* x, const __nv_b
     // 256-column blocks is shared by the tiles running at one time and x_perm (d columns) stays in L2
     // (DRAM reads per launch at T = 4096: 4.07 GB row tiles fastest, 0.55 GB column tiles fastest)
     a_w13.n_fast = 1;
+    if (sched != nullptr) a_w13.sched = sched + 96;
     return launch_pair<PM_WGRAD>("bwd_dw13", 10, 4, ma, mb0, mb0, a_w13,
                                  (int64_t)E * (2 * F / kPairM) * (d / kTileN), st);
 }
@@ -1656,6 +1686,10 @@ moe_status moe_set_knob(int32_t knob, int64_t value) {
         case MOE_KNOB_TILE_CTAS:
             if (value < 0 || value > 2) return MOE_ERR_INVALID_ARG;
             g.tile_ctas = (int)value;
+            return MOE_OK;
+        case MOE_KNOB_TILE_SCHED:
+            if (value < 0 || value > kTileSchedAuto) return MOE_ERR_INVALID_ARG;
+            g.tile_sched = (int)value;
             return MOE_OK;
         case MOE_KNOB_L2_KEEP_KB:
             if (value < 0 || value > 128 * 1024) return MOE_ERR_INVALID_ARG;
