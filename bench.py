@@ -533,10 +533,9 @@ TRAIN_GEMM_FLOPS = {  # multiples of R*d*ffn (R = 2T slot rows) per launch
 
 def tile_units_note(sched: int) -> str:
     """How the CTA-pair kernels took their units (MOE_KNOB_TILE_SCHED)."""
-    if sched == 8:
-        return "automatic: the up projection claims units from a counter at >= 32 units per pair, else fixed"
-    return "claimed from a counter: " + (", ".join(n for b, n in ((1, "up"), (2, "down"), (4, "backward"))
-                                                  if sched & b) or "none")
+    if sched == 0:
+        return "static: pair p takes units p, p + pairs, ..."
+    return "claimed from a counter: " + ", ".join(n for b, n in ((1, "up"), (2, "down"), (4, "backward")) if sched & b)
 
 
 def run_training(args) -> dict:
@@ -1091,9 +1090,9 @@ def main():
                     help="time one decode step of the Mixtral block (16 sequences, 4096-token caches)")
     ap.add_argument("--tile-ctas", type=int, default=0, choices=[0, 1, 2],
                     help="token tiles: automatic (0), single CTAs (1), CTA pairs (2)")
-    ap.add_argument("--tile-sched", type=int, default=8, choices=range(9),
+    ap.add_argument("--tile-sched", type=int, default=0, choices=range(8),
                     help="CTA-pair GEMMs claiming their units from a counter: bit 0 up, bit 1 down, "
-                         "bit 2 the backward's four (0: static units per pair); 8 (default): automatic")
+                         "bit 2 the backward's four (0, the default: static units per pair)")
     ap.add_argument("--decode-loop", action="store_true",
                     help="decode-time expert cache experiment: a locality token stream through 1 or 32 layers "
                          "with and without part of each call's expert weights kept in L2")

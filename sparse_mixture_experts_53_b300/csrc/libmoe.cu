@@ -64,11 +64,6 @@ bool env_flag(const char* name) {
     return v != nullptr && v[0] != '\0' && std::strcmp(v, "0") != 0;
 }
 
-// MOE_KNOB_TILE_SCHED: 0 .. 7 a bit mask, kTileSchedAuto the automatic choice
-constexpr int kTileSchedAuto = 8;
-// automatic choice: the up projection claims its units from this many units per pair on
-constexpr int kClaimMinUnitsPerPair = 32;
-
 struct HostState {
     int ffn_path = 0;          // 0 auto, 1 token tiles, 2 weight streaming
     int64_t kslice = 0;        // 0 auto
@@ -78,7 +73,7 @@ struct HostState {
     bool timing = false;
     bool pdl = true;           // programmatic dependent launch between the library's kernels
     int tile_ctas = 0;         // token tiles: 0 auto, 1 single CTAs, 2 CTA pairs
-    int tile_sched = kTileSchedAuto;  // CTA-pair GEMMs claiming units from a counter: bit 0 up, 1 down, 2 backward
+    int tile_sched = 0;        // CTA-pair GEMMs claiming units from a counter: bit 0 up, 1 down, 2 backward
     uint64_t l2_keep_bytes = 0;  // weight-streaming path: bytes per call kept in L2 for the next call
     int pair_cap[kMaxDevices][8] = {{0}};  // resident clusters per pair kernel (0 = not queried)
     std::vector<TimingRecord> records;
@@ -554,12 +549,7 @@ moe_status run_pair_ffn(const moe_shape& s, const void* x_perm, const int32_t* o
     TileArgs up{offsets, perm_w, H, E, d, F / kTileM, F, F, g.timeout_ns, u_out, v_out};
     const int64_t units_up = ((R + kPairM - 1) / kPairM + E) * (F / kTileM);
     const int grid_up = pair_grid(units_up, cap_up);
-    // Automatic: the up projection claims its units when each pair has many of them (T = 16384: about 200).
-    // The pairs' drift then no longer spreads the readers of a weight tile over several waves, and the
-    // launch reads each operand from DRAM about once instead of twice; with few units per pair
-    // (T = 4096: 8) the fixed assignment keeps the pairs in step and was the faster of the two.
-    const int sched_bits = g.tile_sched != kTileSchedAuto ? g.tile_sched
-                                                          : (units_up >= (int64_t)kClaimMinUnitsPerPair * (grid_up / 2) ? 1 : 0);
+    const int sched_bits = g.tile_sched;
     if (sched_bits & 3) {
         // the kernels claim their units from counters that start at zero
         if (cudaMemsetAsync(sched, 0, 256, st) != cudaSuccess) return MOE_ERR_CUDA;
@@ -819,7 +809,7 @@ moe_status run_backward(const moe_shape& s, const __nv_bfloat16* x, const __nv_b
     float* dxp = reinterpret_cast<float*>(ws + B.dxp);
     float* part = reinterpret_cast<float*>(ws + B.dwg);
     const int sms = sm_count();
-    int* sched = (g.tile_sched != kTileSchedAuto && (g.tile_sched & 4)) ? reinterpret_cast<int*>(ws + B.sched) : nullptr;
+    int* sched = (g.tile_sched & 4) ? reinterpret_cast<int*>(ws + B.sched) : nullptr;
     if (sched != nullptr && cudaMemsetAsync(sched, 0, 512, st) != cudaSuccess) return MOE_ERR_CUDA;
 
     // per slot: dYs = g dy (padded order, pad rows of dYs and dUV zeroed),
@@ -1688,7 +1678,7 @@ moe_status moe_set_knob(int32_t knob, int64_t value) {
             g.tile_ctas = (int)value;
             return MOE_OK;
         case MOE_KNOB_TILE_SCHED:
-            if (value < 0 || value > kTileSchedAuto) return MOE_ERR_INVALID_ARG;
+            if (value < 0 || value > 7) return MOE_ERR_INVALID_ARG;
             g.tile_sched = (int)value;
             return MOE_OK;
         case MOE_KNOB_L2_KEEP_KB:

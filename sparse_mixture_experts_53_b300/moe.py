@@ -35,7 +35,6 @@ MOE_KNOB_TILE_CTAS = 5
 MOE_KNOB_DEBUG = 6
 MOE_KNOB_L2_KEEP_KB = 7
 MOE_KNOB_TILE_SCHED = 8
-MOE_TILE_SCHED_AUTO = 8  # the default value of MOE_KNOB_TILE_SCHED
 
 EXPORTED = (
     "moe_version", "moe_status_string", "moe_workspace_bytes", "moe_ffn_workspace_bytes",

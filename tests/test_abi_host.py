@@ -104,10 +104,9 @@ def test_knobs_and_timeouts():
     assert lib.moe_set_knob(moe.MOE_KNOB_L2_KEEP_KB, 64 * 1024) == moe.MOE_OK
     assert lib.moe_set_knob(moe.MOE_KNOB_L2_KEEP_KB, 0) == moe.MOE_OK
     assert lib.moe_set_knob(moe.MOE_KNOB_TILE_SCHED, -1) == moe.MOE_ERR_INVALID_ARG
-    assert lib.moe_set_knob(moe.MOE_KNOB_TILE_SCHED, 9) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_set_knob(moe.MOE_KNOB_TILE_SCHED, 8) == moe.MOE_ERR_INVALID_ARG
     assert lib.moe_set_knob(moe.MOE_KNOB_TILE_SCHED, 7) == moe.MOE_OK
     assert lib.moe_set_knob(moe.MOE_KNOB_TILE_SCHED, 0) == moe.MOE_OK
-    assert lib.moe_set_knob(moe.MOE_KNOB_TILE_SCHED, moe.MOE_TILE_SCHED_AUTO) == moe.MOE_OK
     assert lib.moe_set_wait_timeout_ns(0) == moe.MOE_ERR_INVALID_ARG
     try:
         moe.moe_set_knob(moe.MOE_KNOB_FFN_PATH, 2)

@@ -25,8 +25,7 @@ def _pair_tiles():
     moe.moe_set_knob(moe.MOE_KNOB_TILE_CTAS, 2)
     moe.moe_get_device_status()
     yield
-    for k, v in ((moe.MOE_KNOB_FFN_PATH, 0), (moe.MOE_KNOB_TILE_CTAS, 0),
-                 (moe.MOE_KNOB_TILE_SCHED, moe.MOE_TILE_SCHED_AUTO),
+    for k, v in ((moe.MOE_KNOB_FFN_PATH, 0), (moe.MOE_KNOB_TILE_CTAS, 0), (moe.MOE_KNOB_TILE_SCHED, 0),
                  (moe.MOE_KNOB_GRID, 0), (moe.MOE_KNOB_PDL, 1)):
         moe.moe_set_knob(k, v)
 
@@ -55,7 +54,7 @@ def _both(dev, calls=2):
     moe.moe_set_knob(moe.MOE_KNOB_TILE_SCHED, 0)
     ref = _forward(dev)
     outs = []
-    for sched in (1, 2, 3, moe.MOE_TILE_SCHED_AUTO):
+    for sched in (1, 2, 3):
         moe.moe_set_knob(moe.MOE_KNOB_TILE_SCHED, sched)
         outs += [_forward(dev) for _ in range(calls)]
     assert_status_ok()
