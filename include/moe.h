@@ -450,6 +450,13 @@ moe_status moe_set_wait_timeout_ns(uint64_t ns);
  *                       shape with T = 16384 this halves the up projection's
  *                       DRAM reads but takes 0.4 % longer (T = 4096: 2 %; the
  *                       backward's GEMMs: 2-7 %). Results do not change.
+ *   MOE_KNOB_ROUTER_TC  1 (default) = bf16 batches of more than 256 tokens
+ *                       compute the router's scores on the tensor cores (fp32
+ *                       accumulation in tensor memory, 128 tokens per tile);
+ *                       0 = on the CUDA cores (the fixed per-lane order with a
+ *                       butterfly, as for small batches). The two sum the d
+ *                       products in different orders, so scores can differ in
+ *                       the last bits.
  *   MOE_KNOB_DEBUG      1 = debug mode: every launch is followed by a wait on
  *                       its stream and a look at the device status word, so a
  *                       device-side error (timeout, index check) is returned by
@@ -459,7 +466,7 @@ moe_status moe_set_wait_timeout_ns(uint64_t ns);
  * Environment, read when the library loads: MOE_DEBUG=1 starts in debug mode;
  * MOE_WAIT_TIMEOUT_NS sets the initial wait limit (as moe_set_wait_timeout_ns). */
 enum { MOE_KNOB_FFN_PATH = 1, MOE_KNOB_KSLICE = 2, MOE_KNOB_GRID = 3, MOE_KNOB_PDL = 4, MOE_KNOB_TILE_CTAS = 5,
-       MOE_KNOB_DEBUG = 6, MOE_KNOB_L2_KEEP_KB = 7, MOE_KNOB_TILE_SCHED = 8 };
+       MOE_KNOB_DEBUG = 6, MOE_KNOB_L2_KEEP_KB = 7, MOE_KNOB_TILE_SCHED = 8, MOE_KNOB_ROUTER_TC = 9 };
 moe_status moe_set_knob(int32_t knob, int64_t value);
 
 /* Per-kernel timing with CUDA events recorded on the launching stream.

@@ -74,6 +74,7 @@ struct HostState {
     bool pdl = true;           // programmatic dependent launch between the library's kernels
     int tile_ctas = 0;         // token tiles: 0 auto, 1 single CTAs, 2 CTA pairs
     int tile_sched = 0;        // CTA-pair GEMMs claiming units from a counter: bit 0 up, 1 down, 2 backward
+    bool router_tc = true;     // bf16 router above the small-batch size on the tensor cores
     uint64_t l2_keep_bytes = 0;  // weight-streaming path: bytes per call kept in L2 for the next call
     int pair_cap[kMaxDevices][8] = {{0}};  // resident clusters per pair kernel (0 = not queried)
     std::vector<TimingRecord> records;
@@ -415,6 +416,19 @@ moe_status run_router(const moe_shape& s, const void* x, const void* wg, int32_t
         return launch("router_top2", st, [&] {
             return klaunch(router_top2_split_kernel<float>, sgrid, kRouterWarps * 32, 0, st, 
                 static_cast<const float*>(x), static_cast<const float*>(wg), s.T, s.d, s.E, idx, w, logits);
+        });
+    }
+    if (s.dtype == MOE_BF16 && vec && s.d % kBK == 0 && g.router_tc) {
+        // tensor cores: 128-token tiles, one CTA per SM
+        CUtensorMap mx, mw;
+        if (!make_map(&mx, x, (uint64_t)s.d, (uint64_t)s.T, kRtM) || !make_map(&mw, wg, (uint64_t)s.d, (uint64_t)s.E, 8))
+            return MOE_ERR_CUDA;
+        if (!ensure_smem(router_tc_kernel, 25, kRtSmemBytes)) return MOE_ERR_CUDA;
+        const int tiles = (int)((s.T + kRtM - 1) / kRtM);
+        const int tgrid = std::max(1, std::min(tiles, sm_count()));
+        return launch("router_top2", st, [&] {
+            return klaunch(router_tc_kernel, tgrid, kRtThreads, kRtSmemBytes, st, mx, mw, s.T, s.d, s.E,
+                           g.timeout_ns, idx, w, logits);
         });
     }
     if (s.dtype == MOE_BF16) {
@@ -1680,6 +1694,10 @@ moe_status moe_set_knob(int32_t knob, int64_t value) {
         case MOE_KNOB_TILE_SCHED:
             if (value < 0 || value > 7) return MOE_ERR_INVALID_ARG;
             g.tile_sched = (int)value;
+            return MOE_OK;
+        case MOE_KNOB_ROUTER_TC:
+            if (value < 0 || value > 1) return MOE_ERR_INVALID_ARG;
+            g.router_tc = value != 0;
             return MOE_OK;
         case MOE_KNOB_L2_KEEP_KB:
             if (value < 0 || value > 128 * 1024) return MOE_ERR_INVALID_ARG;

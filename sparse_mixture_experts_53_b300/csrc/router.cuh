@@ -8,9 +8,16 @@
 // E experts in fp32, then a butterfly of warp shuffles leaves the E totals in
 // every lane. Small batches split one token over a CTA. The reduction order
 // of a token's scores is fixed, so the result does not depend on the grid.
+//
+// bf16 batches above the small-batch size run on the tensor cores instead
+// (router_tc_kernel): the scores of 128 tokens are one M = 128, N = 16, K = d
+// tcgen05 product of the token tile and W_g (rows E..15 zero), accumulated in
+// fp32 in tensor memory; the epilogue's thread for a token reads its E scores
+// and makes the top-2 choice. That leaves the kernel bound by reading x.
 #pragma once
 
 #include "common.cuh"
+#include "ffn_tc.cuh"
 
 namespace moe {
 
@@ -279,6 +286,203 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
         }
         __syncthreads();
     }
+}
+
+// ---------------------------------------------------------------------------
+// Router on the tensor cores (bf16, d a multiple of 64). Persistent CTAs take
+// 128-token tiles; warp 0 streams the tile's x (TMA, 64 K x 128 rows) and the
+// matching 64 K x 8 rows of W_g into a stage, warp 1 issues four M = 128,
+// N = 16, K = 16 MMAs per stage into one of two 16-column accumulators, and
+// warps 2-5 (one token per thread) read the scores back, choose the top two
+// and write idx, w and the scores. Rows 8..15 of each stage's W_g slot are
+// zero (written once before the first copy), and TMA fills W_g rows >= E and
+// token rows >= T with zeros, so those scores and rows are never used.
+// ---------------------------------------------------------------------------
+constexpr int kRtStages = 8;
+constexpr int kRtM = 128;                                  // tokens per tile
+constexpr int kRtN = 16;                                   // MMA columns (E <= 8 used)
+constexpr uint32_t kRtABytes = kRtM * kBK * 2;             // 16 KB of x per stage
+constexpr uint32_t kRtBBytes = kRtN * kBK * 2;             // 2 KB slot of W_g per stage
+constexpr uint32_t kRtBLoad = 8 * kBK * 2;                 // the 1 KB TMA writes (rows 0-7)
+constexpr uint32_t kRtStageBytes = kRtABytes + kRtBBytes;  // 18 KB, a multiple of 1 KB
+constexpr int kRtThreads = 192;
+
+struct RouterTcControl {
+    uint64_t full[kRtStages];
+    uint64_t empty[kRtStages];
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+constexpr size_t kRtSmemBytes = 1024 + (size_t)kRtStages * kRtStageBytes + sizeof(RouterTcControl);
+
+__device__ __forceinline__ void rt_abort(RouterTcControl* c, int where) {
+    report_error(MOE_ERR_TIMEOUT, K_ROUTER, where);
+    *reinterpret_cast<volatile int*>(&c->abort_flag) = 1;
+}
+
+__global__ void __launch_bounds__(kRtThreads, 1)
+    router_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
+                     int64_t T_tokens, int d, int E, uint64_t timeout_ns, int32_t* __restrict__ topk_idx,
+                     float* __restrict__ topk_w, float* __restrict__ logits) {
+    extern __shared__ unsigned char rt_smem_raw[];
+    unsigned char* smem = align1024(rt_smem_raw);
+    RouterTcControl* ctl = reinterpret_cast<RouterTcControl*>(smem + (size_t)kRtStages * kRtStageBytes);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint64_t tmo = timeout_ns;
+    volatile int* abort_flag = &ctl->abort_flag;
+    const int n_tiles = (int)((T_tokens + kRtM - 1) / kRtM);
+    const int KB = d / kBK;
+
+    // rows 8..15 of every W_g slot: zeros the tensor core reads (async proxy)
+    for (int i = threadIdx.x; i < kRtStages * (int)(kRtBBytes - kRtBLoad) / 16; i += blockDim.x) {
+        const int st = i / ((kRtBBytes - kRtBLoad) / 16), j = i % ((kRtBBytes - kRtBLoad) / 16);
+        reinterpret_cast<uint4*>(smem + (size_t)st * kRtStageBytes + kRtABytes + kRtBLoad)[j] = make_uint4(0, 0, 0, 0);
+    }
+    fence_proxy_async_smem();
+    if (threadIdx.x == 0) {
+        for (int q = 0; q < kRtStages; ++q) {
+            mbar_init(smem_u32(&ctl->full[q]), 1);
+            mbar_init(smem_u32(&ctl->empty[q]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&ctl->tfull[b]), 1);
+            mbar_init(smem_u32(&ctl->tempty[b]), 4);
+        }
+        mbar_init(smem_u32(&ctl->drain), 1);
+        ctl->abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&map_x);
+        tma_prefetch_desc(&map_w);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&ctl->tmem_base), 2 * kRtN);
+        tmem_relinquish();
+    }
+    pdl_trigger();
+    pdl_wait();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = ctl->tmem_base;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            const uint64_t pol_x = policy_evict_first();   // each token row is read once
+            const uint64_t pol_w = policy_evict_last();    // W_g is read by every tile
+            uint32_t s = 0, ph = 0;
+            uint32_t issued_mask = 0, issued_ph = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x) {
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!mbar_wait(smem_u32(&ctl->empty[s]), ph ^ 1, tmo, abort_flag)) {
+                        rt_abort(ctl, W_PRODUCER);
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = smem_u32(&ctl->full[s]);
+                    const uint32_t sa = smem_u32(smem + (size_t)s * kRtStageBytes);
+                    mbar_arrive_expect_tx(fb, kRtABytes + kRtBLoad);
+                    tma_load_2d(sa, &map_x, fb, kb * kBK, tile * kRtM, pol_x);
+                    tma_load_2d(sa + kRtABytes, &map_w, fb, kb * kBK, 0, pol_w);
+                    issued_mask |= 1u << s;
+                    issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
+                    if (++s == kRtStages) { s = 0; ph ^= 1; }
+                }
+            }
+            if (!ok) {
+                for (int q = 0; q < kRtStages; ++q)
+                    if (issued_mask & (1u << q))
+                        drain_wait(smem_u32(&ctl->full[q]), (issued_ph >> q) & 1u, tmo, K_ROUTER);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16_f32(kRtM, kRtN);
+            uint32_t s = 0, ph = 0;
+            bool ok = true, any = false;
+            int it = 0;
+            for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x, ++it) {
+                const int b = it & 1;
+                const uint32_t aph = (it >> 1) & 1;
+                if (!mbar_wait(smem_u32(&ctl->tempty[b]), aph ^ 1, tmo, abort_flag)) {
+                    rt_abort(ctl, W_MMA);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + b * kRtN;
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!mbar_wait(smem_u32(&ctl->full[s]), ph, tmo, abort_flag)) {
+                        rt_abort(ctl, W_MMA);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(smem + (size_t)s * kRtStageBytes);
+                    const uint64_t adesc = sw128_kmajor_desc(sa);
+                    const uint64_t bdesc = sw128_kmajor_desc(sa + kRtABytes);
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk)
+                        mma_bf16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (kb | kk) != 0);
+                    any = true;
+                    mma_commit(smem_u32(&ctl->empty[s]));
+                    if (++s == kRtStages) { s = 0; ph ^= 1; }
+                }
+                if (!ok) break;
+                mma_commit(smem_u32(&ctl->tfull[b]));
+            }
+            if (any) {
+                mma_commit(smem_u32(&ctl->drain));
+                drain_wait(smem_u32(&ctl->drain), 0, tmo, K_ROUTER);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------ epilogue (warps 2-5): one token per thread
+        const int sub = warp & 3;   // tensor-memory lanes 32 sub .. 32 sub + 31
+        int it = 0;
+        for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
+            const int b = it & 1;
+            const uint32_t aph = (it >> 1) & 1;
+            if (!mbar_wait(smem_u32(&ctl->tfull[b]), aph, tmo, abort_flag)) {
+                rt_abort(ctl, W_EPILOGUE);
+                break;
+            }
+            tc_fence_after();
+            uint32_t v[16];
+            tmem_ld16(tmem_base + b * kRtN + ((uint32_t)(sub * 32) << 16), v);
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[b]));
+            const int64_t t = (int64_t)tile * kRtM + sub * 32 + lane;
+            if (t < T_tokens) {
+                float acc[kMaxExperts];
+#pragma unroll
+                for (int e = 0; e < kMaxExperts; ++e) acc[e] = __uint_as_float(v[e]);
+                if (logits != nullptr) {
+#pragma unroll
+                    for (int e = 0; e < kMaxExperts; ++e)
+                        if (e < E) logits[t * E + e] = acc[e];
+                }
+                top2_softmax(acc, E, topk_idx + 2 * t, topk_w + 2 * t);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, 2 * kRtN);
 }
 
 }  // namespace moe
