@@ -457,6 +457,15 @@ moe_status moe_set_wait_timeout_ns(uint64_t ns);
  *                       butterfly, as for small batches). The two sum the d
  *                       products in different orders, so scores can differ in
  *                       the last bits.
+ *   MOE_KNOB_FUSE_COMBINE 1 (default) = moe_layer_forward on CTA-pair token
+ *                       tiles runs the combine inside the down projection: the
+ *                       slot of a token in the higher-numbered of its two
+ *                       experts waits for the unit holding the other slot,
+ *                       adds that slot's y_slot row to its own and writes the
+ *                       token's row of y (bf16), so y_slot is written only for
+ *                       the other slots and the separate combine pass is
+ *                       skipped; 0 = y_slot for every slot, then the combine.
+ *                       Results are bit-identical.
  *   MOE_KNOB_DEBUG      1 = debug mode: every launch is followed by a wait on
  *                       its stream and a look at the device status word, so a
  *                       device-side error (timeout, index check) is returned by
@@ -466,7 +475,8 @@ moe_status moe_set_wait_timeout_ns(uint64_t ns);
  * Environment, read when the library loads: MOE_DEBUG=1 starts in debug mode;
  * MOE_WAIT_TIMEOUT_NS sets the initial wait limit (as moe_set_wait_timeout_ns). */
 enum { MOE_KNOB_FFN_PATH = 1, MOE_KNOB_KSLICE = 2, MOE_KNOB_GRID = 3, MOE_KNOB_PDL = 4, MOE_KNOB_TILE_CTAS = 5,
-       MOE_KNOB_DEBUG = 6, MOE_KNOB_L2_KEEP_KB = 7, MOE_KNOB_TILE_SCHED = 8, MOE_KNOB_ROUTER_TC = 9 };
+       MOE_KNOB_DEBUG = 6, MOE_KNOB_L2_KEEP_KB = 7, MOE_KNOB_TILE_SCHED = 8, MOE_KNOB_ROUTER_TC = 9,
+       MOE_KNOB_FUSE_COMBINE = 10 };
 moe_status moe_set_knob(int32_t knob, int64_t value);
 
 /* Per-kernel timing with CUDA events recorded on the launching stream.

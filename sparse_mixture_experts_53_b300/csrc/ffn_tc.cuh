@@ -125,6 +125,14 @@ struct TileArgs {
     // operand); 1 = column tiles fastest: they share a block of A and all of B stays in L2 (right when B
     // is the smaller one). The order does not change any tile's arithmetic.
     int n_fast;
+    // down projection with the combine (pair kernel, PM_DOWN, y non-null): a slot whose token's other slot
+    // lies in a lower-numbered expert adds that slot's y_slot row to its own and writes the token's row of
+    // y (bf16); every other slot writes y_slot. done[unit] (zero at launch) counts the epilogue warps that
+    // have finished the unit's stores.
+    const int32_t* perm_token;
+    const int32_t* slot_row;
+    __nv_bfloat16* y;
+    int* done;
     // pair kernel: nullptr = pair p takes units p, p + pairs, ...; otherwise a counter, zero at launch,
     // from which the pairs claim units in order as they become free (any pair may compute any unit: the
     // results do not depend on the assignment)
@@ -197,6 +205,58 @@ __device__ __forceinline__ void tile_epilogue(uint32_t taddr, bool valid, int64_
             }
         }
     }
+}
+
+// Down-projection epilogue with the combine fused in, for one thread (one slot row r); every thread of
+// the warp calls it with the same columns (tcgen05.ld is warp-collective: the per-thread choice below
+// only selects which stores it makes). A slot that finishes its token (`finish`) adds the same columns
+// of the token's other slot (row pr of y_slot, already written; pr < 0: no other slot) to its own value
+// (the accumulator scaled by its gate weight, rounded once as in y_slot), sums in fp32 and rounds once
+// to bf16 into row t of y; any other slot writes its y_slot row as tile_epilogue<false> does. Two fp32
+// operands add the same in either order, so y equals the separate combine pass bit for bit.
+__device__ __forceinline__ void down_combine_epilogue(uint32_t taddr, bool valid, bool finish, int64_t r, int64_t pr,
+                                                      int64_t t, const TileArgs& args, int j_begin, int j_end,
+                                                      int col0) {
+    const float pw = valid ? (args.perm_w != nullptr ? args.perm_w[r] : 1.0f) : 0.f;
+    float* ys = reinterpret_cast<float*>(args.out) + r * args.ldo + col0;
+    const float* other = reinterpret_cast<const float*>(args.out) + (pr >= 0 ? pr : 0) * args.ldo + col0;
+    __nv_bfloat16* yo = args.y + t * args.ldo + col0;
+    const bool read_other = valid && finish && pr >= 0;
+#pragma unroll 1
+    for (int j = j_begin; j < j_end; j += 16) {
+        float4 o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            o[i] = read_other ? reinterpret_cast<const float4*>(other + j)[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+        uint32_t a[16];
+        __syncwarp();
+        tmem_ld16(taddr + j, a);
+        tmem_wait_ld();
+        float v[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) v[c] = __fmul_rn(pw, __uint_as_float(a[c]));
+        if (valid && finish) {
+            uint32_t pk[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                pk[2 * i] = pack_bf16x2(__fadd_rn(v[4 * i], o[i].x), __fadd_rn(v[4 * i + 1], o[i].y));
+                pk[2 * i + 1] = pack_bf16x2(__fadd_rn(v[4 * i + 2], o[i].z), __fadd_rn(v[4 * i + 3], o[i].w));
+            }
+            uint4* dst = reinterpret_cast<uint4*>(yo + j);
+            dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        } else if (valid) {
+            float4* dst = reinterpret_cast<float4*>(ys + j);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+        }
+    }
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+    int v;
+    asm volatile("ld.global.acquire.gpu.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
 }
 
 // UP = true: SwiGLU up-projection; UP = false: W2 down-projection + gate scale.
@@ -875,26 +935,60 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                                (warp - 2) * kWgradStageFloats;
                 wgrad_epilogue(taddr, ksteps(e) > 0, e, mt * kPairM + row_in_tile - lane, nt, lane, stage, args,
                                j_begin, j_end);
-            } else if (is_half(e, mt)) {
+            } else {
                 // half tile: lane l holds row l mod 64 of this CTA's 64 rows, the tile's columns
                 // 128 (l / 64) .. 128 (l / 64) + 127 (up: u and v of f = 64 (l / 64) + j at j, 64 + j)
+                const bool hf = is_half(e, mt);
                 const int gl = sub * 32 + lane;
-                const int grow = mt * kPairM + 64 * (int)rank + (gl & 63);
+                const int grow = hf ? mt * kPairM + 64 * (int)rank + (gl & 63) : mt * kPairM + row_in_tile;
                 const bool valid = grow < ctl->cnt[e];
                 const int64_t r = ctl->off[e] + grow;
                 const int hb = half * (UP ? 32 : 64);
-                if (UP)
-                    tile_epilogue<true>(taddr, valid, r, nt, args, hb, hb + 32, 64, nt * kTileM + 64 * (gl >> 6));
-                else
-                    tile_epilogue<false>(taddr, valid, r, nt, args, hb, hb + 64, 0, nt * kTileN + 128 * (gl >> 6));
-            } else {
-                const int grow = mt * kPairM + row_in_tile;
-                const bool valid = grow < ctl->cnt[e];
-                const int64_t r = ctl->off[e] + grow;
-                if (MODE == PM_BWD_DH)
+                const int jb = hf ? hb : j_begin, je = hf ? hb + (UP ? 32 : 64) : j_end;
+                const int col0 = hf ? nt * (UP ? kTileM : kTileN) + (UP ? 64 : 128) * (gl >> 6) : -1;
+                if (MODE == PM_DOWN && args.y != nullptr) {
+                    // the combine fused in: does this slot finish its token? (the token's other slot lies
+                    // in a lower-numbered expert, whose units come first; wait until that unit is stored)
+                    int64_t t = 0, pr = -1;
+                    bool finish = false;
+                    if (valid) {
+                        t = args.perm_token[r];
+                        const int s0 = args.slot_row[2 * t], s1 = args.slot_row[2 * t + 1];
+                        pr = s0 == r ? s1 : s0;
+                        int pe = -1;
+                        if (pr >= 0)
+                            for (int q = 0; q < E; ++q)
+                                if (pr >= ctl->off[q] && pr < ctl->off[q + 1]) pe = q;
+                        finish = pr < 0 || pe < e;
+                        if (pr >= 0 && pe == e) report_error(MOE_ERR_DEVICE_CHECK, kid, W_INDEX);
+                        if (finish && pr >= 0) {
+                            const int pm = (int)(pr - ctl->off[pe]) / kPairM;
+                            const int* flag = args.done + ctl->base[pe] + nt * ctl->mt[pe] + pm;
+                            const uint64_t t0 = global_ns();
+                            while (ld_acquire_gpu(flag) < 2 * kPairEpiWarps) {
+                                if (global_ns() - t0 > tmo) {
+                                    raise_abort(ctl, kid, W_EPILOGUE);
+                                    break;
+                                }
+                            }
+                        }
+                    }
+                    __syncwarp();
+                    down_combine_epilogue(taddr, valid, finish, r, pr, t, args, jb, je, col0 < 0 ? nt * kTileN : col0);
+                    // the unit's y_slot rows are visible to every SM before the warp counts itself done
+                    __threadfence();
+                    __syncwarp();
+                    if (lane == 0) atomicAdd(args.done + tile, 1);
+                } else if (hf) {
+                    if (UP)
+                        tile_epilogue<true>(taddr, valid, r, nt, args, hb, hb + 32, 64, col0);
+                    else
+                        tile_epilogue<false>(taddr, valid, r, nt, args, hb, hb + 64, 0, col0);
+                } else if (MODE == PM_BWD_DH) {
                     bwd_dh_epilogue(taddr, valid, r, (int64_t)ctl->koff[e] + grow, nt, args, j_begin, j_end);
-                else
+                } else {
                     tile_epilogue<UP>(taddr, valid, r, nt, args, j_begin, j_end);
+                }
             }
             tc_fence_before();
             __syncwarp();

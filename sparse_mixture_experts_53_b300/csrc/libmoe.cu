@@ -75,6 +75,7 @@ struct HostState {
     int tile_ctas = 0;         // token tiles: 0 auto, 1 single CTAs, 2 CTA pairs
     int tile_sched = 0;        // CTA-pair GEMMs claiming units from a counter: bit 0 up, 1 down, 2 backward
     bool router_tc = true;     // bf16 router above the small-batch size on the tensor cores
+    bool fuse_combine = true;  // whole-layer call on CTA pairs: the combine runs in the down projection
     uint64_t l2_keep_bytes = 0;  // weight-streaming path: bytes per call kept in L2 for the next call
     int pair_cap[kMaxDevices][8] = {{0}};  // resident clusters per pair kernel (0 = not queried)
     std::vector<TimingRecord> records;
@@ -326,7 +327,7 @@ size_t permute_ws_bytes(const moe_shape& s) {
 struct FfnLayout {
     int path = 0;
     int nb = 0, ks_up = 0, ks_down = 0, S_up = 0, S_down = 0;
-    size_t h = 0, part_up = 0, part_down = 0, sched = 0, total = 0;
+    size_t h = 0, part_up = 0, part_down = 0, sched = 0, done = 0, total = 0;
 };
 
 FfnLayout ffn_layout(const moe_shape& s) {
@@ -352,6 +353,9 @@ FfnLayout ffn_layout(const moe_shape& s) {
             // the unit counters of the CTA-pair kernels (up, down), on separate lines
             L.sched = off;
             off = align_up(off + 256, kAlign);
+            // the down projection's per-unit completion counts (combine fused in)
+            L.done = off;
+            off = align_up(off + (size_t)((R + 255) / 256 + s.E) * (s.d / 256) * sizeof(int), kAlign);
         }
     }
     L.total = off;
@@ -541,7 +545,8 @@ int pair_grid(int64_t pairs_upper, int cap) {
 // MOE_ERR_UNSUPPORTED (nothing enqueued) when the kernels do not fit.
 moe_status run_pair_ffn(const moe_shape& s, const void* x_perm, const int32_t* offsets, const float* perm_w,
                         const void* w1, const void* w3, const void* w2, float* y_slot, __nv_bfloat16* H,
-                        __nv_bfloat16* u_out, __nv_bfloat16* v_out, int* sched, cudaStream_t st) {
+                        __nv_bfloat16* u_out, __nv_bfloat16* v_out, int* sched, const int32_t* perm_token,
+                        const int32_t* slot_row, __nv_bfloat16* y, int* done, cudaStream_t st) {
     const int64_t R = 2 * s.T;
     const int d = s.d, F = s.ffn, E = s.E;
     auto kup = tile_pair_gemm_kernel<PM_UP>;
@@ -577,6 +582,14 @@ moe_status run_pair_ffn(const moe_shape& s, const void* x_perm, const int32_t* o
     TileArgs down{offsets, perm_w, y_slot, E, F, d / kTileN, d, d, g.timeout_ns};
     if (sched_bits & 2) down.sched = sched + 32;
     const int64_t units_down = ((R + kPairM - 1) / kPairM + E) * (d / kTileN);
+    if (y != nullptr) {
+        // the combine fused into the down projection's epilogue: per-unit completion counts from zero
+        if (cudaMemsetAsync(done, 0, (size_t)units_down * sizeof(int), st) != cudaSuccess) return MOE_ERR_CUDA;
+        down.perm_token = perm_token;
+        down.slot_row = slot_row;
+        down.y = y;
+        down.done = done;
+    }
     return launch("tile_down_scale", st, [&] {
         return klaunch_cluster(kdown, 2, pair_grid(units_down, cap_down), kPairThreads, kPairSmemBytes, st, mh, mw2,
                                mw2, mw2, mw2, down);
@@ -584,12 +597,14 @@ moe_status run_pair_ffn(const moe_shape& s, const void* x_perm, const int32_t* o
 }
 
 // With slot_row and y given (the whole-layer call), the weight-streaming path
-// finishes with the fused K-slice sum + gate scale + combine and sets
-// *combined; otherwise it writes y_slot.
+// finishes with the fused K-slice sum + gate scale + combine, and the CTA-pair
+// path (given perm_token too) with the combine fused into the down
+// projection, and both set *combined; otherwise the expert FFN writes y_slot.
 moe_status run_ffn(const moe_shape& s, const void* x_perm, const int32_t* offsets, const float* perm_w,
                    const void* w1, const void* w3, const void* w2, float* y_slot, unsigned char* ws,
                    const FfnLayout& L, cudaStream_t st, const int32_t* slot_row = nullptr, void* y = nullptr,
-                   bool* combined = nullptr, __nv_bfloat16* u_out = nullptr, __nv_bfloat16* v_out = nullptr) {
+                   bool* combined = nullptr, __nv_bfloat16* u_out = nullptr, __nv_bfloat16* v_out = nullptr,
+                   const int32_t* perm_token = nullptr) {
     if (s.T == 0) return MOE_OK;
     const int64_t R = 2 * s.T;
     const int d = s.d, F = s.ffn, E = s.E;
@@ -610,8 +625,14 @@ moe_status run_ffn(const moe_shape& s, const void* x_perm, const int32_t* offset
     const int tile_ctas = g.tile_ctas != 0 ? g.tile_ctas : (s.T <= kSingleCtaMaxTokens ? 1 : 2);
     if (L.path == 1 && tile_ctas == 2) {
         // CTA pairs: each CTA stages 128 token rows and 128 weight rows per stage
-        const moe_status rc = run_pair_ffn(s, x_perm, offsets, perm_w, w1, w3, w2, y_slot, H, u_out, v_out,
-                                           reinterpret_cast<int*>(ws + L.sched), st);
+        const bool fuse = perm_token != nullptr && slot_row != nullptr && y != nullptr && combined != nullptr &&
+                          g.fuse_combine;
+        const moe_status rc =
+            run_pair_ffn(s, x_perm, offsets, perm_w, w1, w3, w2, y_slot, H, u_out, v_out,
+                         reinterpret_cast<int*>(ws + L.sched), fuse ? perm_token : nullptr,
+                         fuse ? slot_row : nullptr, fuse ? static_cast<__nv_bfloat16*>(y) : nullptr,
+                         reinterpret_cast<int*>(ws + L.done), st);
+        if (rc == MOE_OK && fuse) *combined = true;
         if (rc != MOE_ERR_UNSUPPORTED) return rc;
     }
     if (L.path == 1) {
@@ -1346,7 +1367,8 @@ moe_status moe_layer_forward(const moe_shape* s, const void* x, const void* w_ga
     MOE_TRY(run_permute(*s, idx, gw, x, counts, offsets, perm_token, slot_row, perm_w, x_perm, w + L.perm_ws,
                         permute_ws_bytes(*s), st));
     bool combined = false;
-    MOE_TRY(run_ffn(*s, x_perm, offsets, perm_w, w1, w3, w2, y_slot, w + L.ffn, L.f, st, slot_row, y, &combined));
+    MOE_TRY(run_ffn(*s, x_perm, offsets, perm_w, w1, w3, w2, y_slot, w + L.ffn, L.f, st, slot_row, y, &combined,
+                    nullptr, nullptr, perm_token));
     if (!combined) MOE_TRY(run_combine(*s, y_slot, slot_row, y, st));
     if (aux) MOE_TRY(run_aux(*s, logits, counts, aux_f, aux_P, aux_l_aux, st));
     return MOE_OK;
@@ -1694,6 +1716,10 @@ moe_status moe_set_knob(int32_t knob, int64_t value) {
         case MOE_KNOB_TILE_SCHED:
             if (value < 0 || value > 7) return MOE_ERR_INVALID_ARG;
             g.tile_sched = (int)value;
+            return MOE_OK;
+        case MOE_KNOB_FUSE_COMBINE:
+            if (value < 0 || value > 1) return MOE_ERR_INVALID_ARG;
+            g.fuse_combine = value != 0;
             return MOE_OK;
         case MOE_KNOB_ROUTER_TC:
             if (value < 0 || value > 1) return MOE_ERR_INVALID_ARG;

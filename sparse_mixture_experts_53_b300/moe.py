@@ -36,6 +36,7 @@ MOE_KNOB_DEBUG = 6
 MOE_KNOB_L2_KEEP_KB = 7
 MOE_KNOB_TILE_SCHED = 8
 MOE_KNOB_ROUTER_TC = 9
+MOE_KNOB_FUSE_COMBINE = 10
 
 EXPORTED = (
     "moe_version", "moe_status_string", "moe_workspace_bytes", "moe_ffn_workspace_bytes",

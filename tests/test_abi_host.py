@@ -110,6 +110,9 @@ def test_knobs_and_timeouts():
     assert lib.moe_set_knob(moe.MOE_KNOB_ROUTER_TC, 2) == moe.MOE_ERR_INVALID_ARG
     assert lib.moe_set_knob(moe.MOE_KNOB_ROUTER_TC, 0) == moe.MOE_OK
     assert lib.moe_set_knob(moe.MOE_KNOB_ROUTER_TC, 1) == moe.MOE_OK
+    assert lib.moe_set_knob(moe.MOE_KNOB_FUSE_COMBINE, 2) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_set_knob(moe.MOE_KNOB_FUSE_COMBINE, 0) == moe.MOE_OK
+    assert lib.moe_set_knob(moe.MOE_KNOB_FUSE_COMBINE, 1) == moe.MOE_OK
     assert lib.moe_set_wait_timeout_ns(0) == moe.MOE_ERR_INVALID_ARG
     try:
         moe.moe_set_knob(moe.MOE_KNOB_FFN_PATH, 2)
