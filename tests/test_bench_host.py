@@ -50,3 +50,10 @@ def test_source_digests_follow_their_own_sources_only():
     assert bench._source_digest("tile_up_swiglu") == bench._source_digest("tile_down_scale")
     assert bench._source_digest("tile_up_swiglu") != bench._source_digest("stream_up")
     assert bench._profile_traffic("no_such_kernel", "mixtral_large_T16384_aux") is None
+
+
+def test_tile_units_note_names_each_claiming_kernel():
+    assert bench.tile_units_note(0).startswith("static")
+    assert bench.tile_units_note(1) == "claimed from a counter: up"
+    assert bench.tile_units_note(6) == "claimed from a counter: down, backward"
+    assert bench.tile_units_note(7) == "claimed from a counter: up, down, backward"
