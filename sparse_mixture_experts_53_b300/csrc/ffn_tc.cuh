@@ -133,6 +133,10 @@ struct TileArgs {
     const int32_t* slot_row;
     __nv_bfloat16* y;
     int* done;
+    // pair kernel (up projection): zero these counts once its predecessors are done (the down
+    // projection that follows reads them only after this kernel has completed)
+    int* zero_counts;
+    int n_zero_counts;
     // pair kernel: nullptr = pair p takes units p, p + pairs, ...; otherwise a counter, zero at launch,
     // from which the pairs claim units in order as they become free (any pair may compute any unit: the
     // results do not depend on the assignment)
@@ -652,6 +656,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     }
     pdl_trigger();
     pdl_wait();
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < args.n_zero_counts; i += gridDim.x * blockDim.x)
+        args.zero_counts[i] = 0;
     if (threadIdx.x == 0) {
         int tiles = 0;
         if (args.offsets != nullptr) {
@@ -970,6 +976,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                                     raise_abort(ctl, kid, W_EPILOGUE);
                                     break;
                                 }
+                                __nanosleep(256);
                             }
                         }
                     }

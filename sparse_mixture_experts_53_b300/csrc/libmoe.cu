@@ -568,6 +568,10 @@ moe_status run_pair_ffn(const moe_shape& s, const void* x_perm, const int32_t* o
     TileArgs up{offsets, perm_w, H, E, d, F / kTileM, F, F, g.timeout_ns, u_out, v_out};
     const int64_t units_up = ((R + kPairM - 1) / kPairM + E) * (F / kTileM);
     const int grid_up = pair_grid(units_up, cap_up);
+    if (y != nullptr) {
+        up.zero_counts = done;
+        up.n_zero_counts = (int)(((R + kPairM - 1) / kPairM + E) * (d / kTileN));
+    }
     const int sched_bits = g.tile_sched;
     if (sched_bits & 3) {
         // the kernels claim their units from counters that start at zero
@@ -583,8 +587,8 @@ moe_status run_pair_ffn(const moe_shape& s, const void* x_perm, const int32_t* o
     if (sched_bits & 2) down.sched = sched + 32;
     const int64_t units_down = ((R + kPairM - 1) / kPairM + E) * (d / kTileN);
     if (y != nullptr) {
-        // the combine fused into the down projection's epilogue: per-unit completion counts from zero
-        if (cudaMemsetAsync(done, 0, (size_t)units_down * sizeof(int), st) != cudaSuccess) return MOE_ERR_CUDA;
+        // the combine fused into the down projection's epilogue: per-unit completion counts, zeroed by
+        // the up projection (launched above) so that no memset separates the two kernels
         down.perm_token = perm_token;
         down.slot_row = slot_row;
         down.y = y;
