@@ -29,6 +29,18 @@ def test_every_declared_function_is_exported():
     assert set(names) == set(moe.EXPORTED)
 
 
+def test_header_constants_match_the_binding():
+    """Every MOE_* enumerator of the header has the same value in moe.py (knobs, statuses, dtypes)."""
+    text = re.sub(r"/\*.*?\*/", "", HEADER.read_text(), flags=re.S)
+    found = {}
+    for body in re.findall(r"enum\s*\w*\s*\{(.*?)\}", text, flags=re.S):
+        for name, value in re.findall(r"\b(MOE_[A-Z0-9_]+)\s*=\s*(\d+)", body):
+            found[name] = int(value)
+    assert len(found) >= 19
+    for name, value in found.items():
+        assert getattr(moe, name) == value, name
+
+
 def test_version_and_status_strings():
     assert "sm_103a" in moe.version()
     assert moe.status_string(moe.MOE_OK) == "ok"
