@@ -465,7 +465,9 @@ moe_status moe_set_wait_timeout_ns(uint64_t ns);
  *                       token's row of y (bf16), so y_slot is written only for
  *                       the other slots and the separate combine pass is
  *                       skipped; 0 = y_slot for every slot, then the combine.
- *                       Results are bit-identical.
+ *                       Results are bit-identical. The fused form needs all
+ *                       CTA pairs resident at once, so with MOE_KNOB_GRID above
+ *                       one CTA per SM the separate combine runs.
  *   MOE_KNOB_DEBUG      1 = debug mode: every launch is followed by a wait on
  *                       its stream and a look at the device status word, so a
  *                       device-side error (timeout, index check) is returned by

@@ -1371,8 +1371,11 @@ moe_status moe_layer_forward(const moe_shape* s, const void* x, const void* w_ga
     MOE_TRY(run_permute(*s, idx, gw, x, counts, offsets, perm_token, slot_row, perm_w, x_perm, w + L.perm_ws,
                         permute_ws_bytes(*s), st));
     bool combined = false;
+    // The fused combine makes a pair wait for units of other pairs, so it needs every pair resident at
+    // once: with MOE_KNOB_GRID above one CTA per SM the separate combine pass runs instead.
+    const bool all_pairs_resident = g.grid == 0 || g.grid <= sm_count();
     MOE_TRY(run_ffn(*s, x_perm, offsets, perm_w, w1, w3, w2, y_slot, w + L.ffn, L.f, st, slot_row, y, &combined,
-                    nullptr, nullptr, perm_token));
+                    nullptr, nullptr, all_pairs_resident ? perm_token : nullptr));
     if (!combined) MOE_TRY(run_combine(*s, y_slot, slot_row, y, st));
     if (aux) MOE_TRY(run_aux(*s, logits, counts, aux_f, aux_P, aux_l_aux, st));
     return MOE_OK;
